@@ -1,0 +1,113 @@
+"""Pins for the oracle's softmax, nucleus and multinomial draw."""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+from oracle.fp32 import F32, F64
+from oracle.philox import uniform
+from oracle.sampling import draw_from_weights, nucleus_kept, sample_row, softmax_weights
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def chi2_ok(counts, probs, alpha=1e-3):
+    counts = np.asarray(counts, dtype=np.float64)
+    exp = np.asarray(probs, dtype=np.float64) * counts.sum()
+    keep = exp > 5
+    stat = np.sum((counts[keep] - exp[keep]) ** 2 / exp[keep])
+    return stat < stats.chi2.ppf(1 - alpha, keep.sum() - 1), stat
+
+
+@pytest.mark.parametrize("V,T,top_p", [(8, 0.7, 1.0), (64, 1.0, 0.9), (64, 0.5, 0.95)])
+def test_draws_follow_q(V, T, top_p):
+    rng = np.random.default_rng(V)
+    s = (rng.standard_normal(V) * 2).astype(F32)
+    z, zmax, w = softmax_weights(s, T)
+    kept, _, _ = nucleus_kept(w, top_p)
+    n = 1_000_000
+    u = uniform(99, np.arange(n, dtype=np.uint64), 0, 0)
+    tok, wsum = draw_from_weights(w, kept, u)
+    counts = np.bincount(tok, minlength=V)
+    q = np.zeros(V)
+    q[kept] = w[kept].astype(F64) / wsum
+    assert counts[q == 0].sum() == 0
+    ok, stat = chi2_ok(counts, q)
+    assert ok, stat
+    # the reference distribution is the plain softmax at T, restricted to the nucleus
+    ref = np.exp((s.astype(F64) - s.max()) / T)
+    ref /= ref.sum()
+    if top_p >= 1:
+        np.testing.assert_allclose(q, ref, rtol=1e-5)
+
+
+def thresholded_nucleus(w, top_p):
+    """Independent construction of the nucleus by threshold rounds (openvino.genai PR #4847,
+    commit on the thresholded TopPFilter): keep tokens with p >= p_max * e^-10, then e^-20,
+    e^-40, then all; sort the survivors by probability with ties by index; walk them until
+    the mass exceeds top_p."""
+    total = np.cumsum(w.astype(F64))[-1]
+    p = w.astype(F64) / total
+    pmax = p.max()
+    for thr in (pmax * np.exp(-10.0), pmax * np.exp(-20.0), pmax * np.exp(-40.0), 0.0):
+        cand = [i for i in range(len(p)) if p[i] >= thr and p[i] > 0]
+        cand.sort(key=lambda i: (-p[i], i))
+        mass = 0.0
+        for k, i in enumerate(cand):
+            mass += p[i]
+            if mass > float(F32(top_p)):
+                return sorted(cand[:k + 1])
+    return sorted(i for i in range(len(p)) if p[i] > 0)
+
+
+def test_nucleus_is_full_sort_prefix():
+    rng = np.random.default_rng(7)
+    for trial in range(10000):
+        V = int(rng.integers(2, 64))
+        scale = float(rng.choice([0.1, 1.0, 4.0, 20.0]))
+        s = (rng.standard_normal(V) * scale).astype(F32)
+        if trial % 3 == 0:
+            s = np.round(s)            # many exact ties
+        top_p = float(rng.choice([0.1, 0.5, 0.9, 0.95, 0.999]))
+        _, _, w = softmax_weights(s, 1.0)
+        kept, w_cut, i_cut = nucleus_kept(w, top_p)
+        assert list(kept) == thresholded_nucleus(w, top_p)
+        idx = np.arange(V)
+        by_cut = np.nonzero((w > 0) & ((w > w_cut) | ((w == w_cut) & (idx <= i_cut))))[0]
+        assert list(by_cut) == list(kept)
+
+
+def test_worked_example_tail_is_drawn():
+    g = json.load(open(os.path.join(GOLDEN, "worked_example_float_sums.json")))
+    w = np.concatenate([np.array(g["head_weights"], dtype=F32),
+                        np.full(g["tail_count"], g["tail_weight"], dtype=F32)])
+    kept = np.arange(w.shape[0])
+    n = 1_000_000
+    u = uniform(2024, np.arange(n, dtype=np.uint64), 0, 0)
+    tok, wsum = draw_from_weights(w, kept, u)
+    tail = np.mean(tok >= 2)
+    se = np.sqrt(g["tail_mass"] * (1 - g["tail_mass"]) / n)
+    assert abs(tail - g["tail_mass"]) < 5 * se
+    # the pin has teeth: running sums in float32 never reach the tail
+    c32 = np.cumsum(w, dtype=F32)
+    tok32 = np.minimum(np.searchsorted(c32, (u * c32[-1]).astype(F32), side="right"), w.shape[0] - 1)
+    assert np.mean(tok32 >= 2) < 1e-4
+
+
+def test_low_temperature_is_argmax_and_greedy_ties():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        s = (rng.standard_normal(1000) * 2).astype(F32)
+        tok, _ = sample_row(s, 1e-3, 1.0, float(rng.random()))
+        assert tok == int(np.argmax(s))
+    s = np.array([1.0, 3.0, 3.0, -0.0, 0.0], dtype=F32)
+    assert sample_row(s, 0.0, 1.0, 0.5)[0] == 1
+    assert sample_row(s, -1.0, 1.0, 0.5)[0] == 1
+
+
+def test_flush_below_minus_64():
+    s = np.array([0.0, -63.5, -64.5, -200.0], dtype=F32)
+    _, _, w = softmax_weights(s, 1.0)
+    assert w[0] == 1 and w[1] > 0 and w[2] == 0 and w[3] == 0
