@@ -1,0 +1,313 @@
+// dspark_common.cuh - device helpers shared by the libdspark kernels (sm_103a).
+//
+// Status words, bf16 widening, order-preserving float keys, the Philox4x32-10 stream and
+// its double uniform, the float32 softmax weight, warp reductions, and the inline-PTX
+// wrappers for mbarriers and the tcgen05 tensor-core path.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+#define DS_DEV __device__ __forceinline__
+
+// ----------------------------------------------------------------------------------------
+// status
+// ----------------------------------------------------------------------------------------
+// First error wins: a status word only ever moves from 0 to one nonzero code.
+DS_DEV void ds_set_error(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ----------------------------------------------------------------------------------------
+// element access
+// ----------------------------------------------------------------------------------------
+DS_DEV float ds_bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+template <typename T>
+DS_DEV float ds_load_elem(const T* p);
+template <>
+DS_DEV float ds_load_elem<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return ds_bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(p));
+}
+template <>
+DS_DEV float ds_load_elem<float>(const float* p) { return *p; }
+
+// Element e of a 16-byte vector holding bf16 (8 per vector) or float (4 per vector).
+template <typename T>
+DS_DEV float ds_vec_elem(const uint4& v, int e);
+template <>
+DS_DEV float ds_vec_elem<__nv_bfloat16>(const uint4& v, int e) {
+  const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+  return (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+}
+template <>
+DS_DEV float ds_vec_elem<float>(const uint4& v, int e) {
+  const uint32_t w = (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+  return __uint_as_float(w);
+}
+
+// Streaming 16-byte load (read once: evict-first in L1 and L2).
+DS_DEV uint4 ds_ld_stream(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+
+// ----------------------------------------------------------------------------------------
+// ordering keys: larger float <-> larger unsigned key; -0.0 is folded onto +0.0 first
+// ----------------------------------------------------------------------------------------
+DS_DEV float ds_canon_zero(float x) { return __fadd_rn(x, 0.0f); }
+DS_DEV uint32_t ds_key32(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+DS_DEV float ds_key32_to_float(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+// (value descending, index ascending) as one descending 64-bit key
+DS_DEV uint64_t ds_key64(float x, uint32_t idx) {
+  return (uint64_t(ds_key32(x)) << 32) | uint64_t(0xFFFFFFFFu - idx);
+}
+DS_DEV uint32_t ds_key64_idx(uint64_t k) { return 0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull); }
+DS_DEV float ds_key64_val(uint64_t k) { return ds_key32_to_float(uint32_t(k >> 32)); }
+
+// ----------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) and the 53-bit double uniform
+// ----------------------------------------------------------------------------------------
+struct DsU4 {
+  uint32_t x, y, z, w;
+};
+
+DS_DEV DsU4 ds_philox4x32_10(DsU4 c, uint32_t k0, uint32_t k1) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+    const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+    c = DsU4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+    k0 += W0;
+    k1 += W1;
+  }
+  return c;
+}
+
+enum : uint32_t { DS_PURPOSE_DRAFT = 0, DS_PURPOSE_ACCEPT = 1, DS_PURPOSE_RESIDUAL = 2 };
+
+// Double uniform in [0, 1) for (seed, step, position, purpose, draw).
+DS_DEV double ds_uniform(uint64_t seed, uint64_t step, uint32_t position, uint32_t purpose,
+                         uint32_t draw = 0) {
+  const DsU4 c{uint32_t(step), position, (purpose << 20) + draw, uint32_t(step >> 32)};
+  const DsU4 o = ds_philox4x32_10(c, uint32_t(seed), uint32_t(seed >> 32));
+  const double a = double(o.x >> 5), b = double(o.y >> 6);
+  return (a * 67108864.0 + b) * (1.0 / 9007199254740992.0);
+}
+
+// ----------------------------------------------------------------------------------------
+// softmax weight of an exponent d = z - zmax <= 0, in float32 (flush below -64):
+//   t = fl32(d log2 e), n = rint(t), f = t - n (exact), w = 2^n * P(f),
+//   P = degree-7 Taylor polynomial of 2^f = e^(f ln 2), coefficients (ln 2)^k / k!
+//   rounded to float32, evaluated with correctly rounded FMAs.
+// Every step is one correctly rounded float32 operation, so the CPU reference computes the
+// same bits.
+// ----------------------------------------------------------------------------------------
+DS_DEV float ds_weight(float d) {
+  if (!(d >= -64.0f)) return 0.0f;
+  const float t = __fmul_rn(d, 0x1.715476p+0f);   // 1 / ln 2
+  const float n = rintf(t);
+  const float f = __fsub_rn(t, n);
+  float p = 0x1.ffcbfcp-17f;                       // (ln 2)^7 / 7!
+  p = __fmaf_rn(p, f, 0x1.430912p-13f);            // (ln 2)^6 / 6!
+  p = __fmaf_rn(p, f, 0x1.5d87fep-10f);            // (ln 2)^5 / 5!
+  p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);             // (ln 2)^4 / 4!
+  p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);             // (ln 2)^3 / 3!
+  p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);             // (ln 2)^2 / 2!
+  p = __fmaf_rn(p, f, 0x1.62e430p-1f);             // ln 2
+  p = __fmaf_rn(p, f, 1.0f);
+  const int ni = int(n);                           // -93 <= n <= 0: 2^n is a normal float
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+// z = s / T in float32 (the identity for T == 1)
+DS_DEV float ds_temper(float s, float T) { return (T == 1.0f) ? s : __fdiv_rn(s, T); }
+
+// ----------------------------------------------------------------------------------------
+// warp helpers
+// ----------------------------------------------------------------------------------------
+DS_DEV float ds_warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+DS_DEV double ds_warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+DS_DEV float ds_warp_sumf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+DS_DEV uint64_t ds_warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = (w > v) ? w : v;
+  }
+  return v;
+}
+
+// ----------------------------------------------------------------------------------------
+// shared-memory bitonic sort of n2 (power of two) 64-bit keys, descending; whole block
+// ----------------------------------------------------------------------------------------
+DS_DEV void ds_block_sort_desc(uint64_t* s, int n2) {
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = s[i], b = s[ixj];
+          const bool desc = ((i & k) == 0);
+          if (desc ? (a < b) : (a > b)) {
+            s[i] = b;
+            s[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// mbarrier + tcgen05 inline PTX (sm_100 family). Every wait is bounded.
+// ----------------------------------------------------------------------------------------
+DS_DEV uint32_t ds_smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+DS_DEV void ds_mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ds_smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Waits for phase `parity` of an mbarrier to complete; gives up after `limit` polls.
+DS_DEV bool ds_mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = ds_smem_addr(bar);
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+DS_DEV void ds_fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMEM allocation: one full warp executes these.
+DS_DEV void ds_tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   ds_smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+DS_DEV void ds_tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+DS_DEV void ds_tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+DS_DEV void ds_tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate); one thread.
+DS_DEV void ds_umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
+DS_DEV void ds_umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          ds_smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
+// (8-row x 128-byte atoms, atoms 1024 bytes apart along M/N).
+DS_DEV uint64_t ds_smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= uint64_t(1) << 16;                        // leading byte offset (unused with swizzle)
+  d |= uint64_t(1024 >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+  d |= uint64_t(1) << 46;                        // descriptor version
+  d |= uint64_t(2) << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t ds_idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                    // D format: f32
+         | (1u << 7)                  // A format: bf16
+         | (1u << 10)                 // B format: bf16
+         | (uint32_t(N >> 3) << 17)   // N / 8
+         | (uint32_t(M >> 4) << 24);  // M / 16
+}
+
+// 32 lanes x 32 bits, 64 consecutive columns into 64 registers (one warp).
+DS_DEV void ds_tmem_ld_32x32b_x64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+        "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+        "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+        "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Ampere-style 16-byte async copy global -> shared (any 16-byte-aligned destination).
+DS_DEV void ds_cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ds_smem_addr(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+DS_DEV void ds_cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Bounded-wait limits (polls); a wait that runs out reports DSPARK_ETIMEOUT.
+#define DS_WAIT_LIMIT (1u << 26)

@@ -1,0 +1,269 @@
+/*
+ * dspark.h - C ABI of libdspark: draft-side candidate selection and target-side
+ * rejection-sampling verification for DFlash/DSpark block speculative decoding,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [G] openvino.genai PR #4847, "Add DSpark and DFlash v2 drafts and sampled drafting
+ *       to DFlash speculative decoding" - Description > Change (Markov heads, sampled
+ *       drafting), Fixes (split validation windows), Known issues (host argmax), and its
+ *       commits on the thresholded top-p filter, the block sampler / candidate selector,
+ *       exact sampled speculative decoding, double-precision multinomial sums, the double
+ *       uniform, and the d2t checks.
+ *   [E] optimum-intel PR #2098, "[OpenVINO] Export DFlash v2 and DSpark drafts for
+ *       PagedAttention and continuous batching" - What does this PR do > DFlash v2
+ *       (packed Top-K lattice, transitions gated by the draft hidden states).
+ *   [P] optimum-intel PR #2099, "[OpenVINO] Support MiniCPM-OCR-1.0-DSpark: DSpark drafts
+ *       with a pruned vocabulary" - What does this PR do > Pruned draft vocabulary, Markov
+ *       head (top_k = min(64, draft_vocab_size); table zero outside the draft vocabulary).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless the argument says "host". The caller owns every
+ *     buffer; the library allocates nothing except where a function says it uses a
+ *     caller-provided workspace `ws` of at least dspark_workspace_size() bytes.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream). Outputs are valid once the stream reaches the call.
+ *   - Host-checkable errors (null pointers, sizes, ranges) return before anything is
+ *     launched. Errors found on the device are written to `*dev_status` (a device int32
+ *     the caller zeroes; the first error wins) and read by the caller after a sync.
+ *   - Layouts are row-major. A request r owns block rows row_start[r] + j, j < B, of a
+ *     packed row tensor (every block follows at least one context row in [G], so blocks
+ *     need not be adjacent); row_start == NULL means row_start[r] = r * B.
+ *   - Token ids are int32; d2t offsets are int64 with target id m(i) = i + d2t[i] [P];
+ *     d2t == NULL means the identity map (V_t == V_d).
+ *   - Ties in any ordering go to the lowest index; -0.0 and +0.0 compare equal.
+ *   - Random numbers: Philox4x32-10 keyed by the request's 64-bit seed; counter words
+ *     (step mod 2^32, position j, purpose * 2^20 + draw, step >> 32), purpose 0 = draft draw,
+ *     1 = acceptance test, 2 = residual or bonus draw; a double uniform takes two output
+ *     words: ((x0 >> 5) * 2^26 + (x1 >> 6)) * 2^-53 [G: commit on the double uniform]. The
+ *     draft and the verifier take separate seeds [G: exact sampled speculative decoding].
+ *   - Softmax weights: z = s / T in float32, w = 2^n P(f) for d = z - zmax >= -64 (t =
+ *     fl32(d log2 e), n = rint(t), f = t - n, P the degree-7 Taylor polynomial of 2^f in
+ *     float32 FMAs), w = 0 below -64 [G: thresholded top-p commit]; weights are summed in
+ *     double [G: double-precision multinomial sums].
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dspark_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_EINVAL = 1,      /* bad argument; nothing was launched */
+  DSPARK_ERANGE = 2,      /* a d2t entry maps a draft index outside [0, V_t) */
+  DSPARK_EDUP = 3,        /* d2t is not one-to-one where sampled drafting needs it */
+  DSPARK_EPROPOSAL = 4,   /* the recorded q of a drafted token is zero */
+  DSPARK_ENONFINITE = 5,  /* a row's maximum is not finite */
+  DSPARK_ETIMEOUT = 6,    /* a bounded device wait ran out (the kernel returned early) */
+  DSPARK_ECUDA = 7,       /* a CUDA runtime call or launch failed */
+  DSPARK_EWORKSPACE = 8   /* the workspace is missing, misaligned or too small */
+} dspark_status;
+
+typedef enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 } dspark_dtype;
+
+typedef enum {
+  DSPARK_MAXSUM = 0, /* max-sum (Viterbi) chain over the K'xK' lattice */
+  DSPARK_WALK = 1,   /* greedy walk: best candidate after the token before [G] */
+  DSPARK_SAMPLE = 2  /* sampled walk with the request's draft RNG [G] */
+} dspark_chain_mode;
+
+typedef enum {
+  DSPARK_OP_TOPK = 0,
+  DSPARK_OP_LATTICE = 1,
+  DSPARK_OP_CHAIN = 2,
+  DSPARK_OP_SAMPLE = 3,
+  DSPARK_OP_DENSE_WALK = 4,
+  DSPARK_OP_VERIFY = 5,
+  DSPARK_OP_D2T_CHECK = 6
+} dspark_op;
+
+/*
+ * Record of the proposal distribution q of drafted tokens [G: exact sampled speculative
+ * decoding - the post-filter q each token was drawn from, sparse over the kept tokens or
+ * dense, in target ids]. One record row per (request, position); exactly one of the two
+ * forms is used (the other form's pointers are NULL).
+ *  Sparse: ids[row*cap + k], p[row*cap + k] for k < n[row]: the kept target ids in
+ *          ascending draft (or candidate) index order and their renormalised float32 q.
+ *  Dense:  z[row*ldz + i] = s_i / T over draft indices i < V_d (float32), zmax[row],
+ *          wsum[row] = double sum of the kept weights, and the nucleus cut: index i is
+ *          kept iff w_i > wcut[row], or w_i == wcut[row] and i <= icut[row] (w_i > 0
+ *          always required). q(i) = kept ? w(z_i - zmax) / wsum : 0.
+ */
+typedef struct {
+  int32_t* ids;
+  float* p;
+  int32_t* n;
+  int32_t cap;
+  float* z;
+  int64_t ldz;
+  float* zmax;
+  double* wsum;
+  float* wcut;
+  int32_t* icut;
+} dspark_qrecord;
+
+/* Bytes of workspace `op` needs for R requests x B positions over V columns with K
+ * candidates (0: none). Workspaces need 256-byte alignment and no initial contents. */
+size_t dspark_workspace_size(dspark_op op, int64_t R, int32_t B, int64_t V, int32_t K);
+
+/* Human-readable name of a status code (static string). */
+const char* dspark_status_string(dspark_status s);
+
+/*
+ * d2t validation [G: commit on the d2t checks - one entry per draft logit; the mapping
+ * must be one-to-one for sampled drafting, greedy drafting accepts any mapping].
+ * d2t[V_d] int64: checks 0 <= i + d2t[i] < V_t for every i (DSPARK_ERANGE) and, when
+ * require_injective != 0, that no two draft indices share a target id (DSPARK_EDUP).
+ * The verdict goes to *dev_status. ws: dspark_workspace_size(DSPARK_OP_D2T_CHECK, 1, 1,
+ * V_t, 0) bytes (a bitmap over the target vocabulary, cleared by the call).
+ */
+dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64_t V_t,
+                               int32_t require_injective, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * Row transform + Top-K + d2t map [G: Change > Markov heads, Top-K candidate scorer;
+ * block-sampler commit - rows are backbone logits times the output multiplier, then
+ * soft-capped; P: top_k = min(64, draft_vocab_size), target id i + d2t[i]].
+ * logits: [rows, ld] of `dtype` (bf16 or float32), V_d <= ld used columns; the block rows of
+ *   request r are row_start[r] + j (row_start may be NULL).
+ * s_i = l_i * mult; if softcap > 0, s_i = softcap * tanh(s_i / softcap).
+ * Outputs, K' = min(K, V_d), 1 <= K <= 64, ordered by (s descending, draft index ascending):
+ *   cand_draft [R, B, K'] int32 draft index, cand_tgt [R, B, K'] int32 target id (-1 and
+ *   DSPARK_ERANGE on *dev_status when a chosen index maps outside [0, V_t)), cand_val
+ *   [R, B, K'] float32 s. The kernel needs no workspace.
+ */
+dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
+                          int64_t V_d, int64_t ld, const int64_t* row_start, int32_t K,
+                          float mult, float softcap, const int64_t* d2t, int64_t V_t,
+                          int32_t* cand_draft, int32_t* cand_tgt, float* cand_val,
+                          int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * Markov-head transition lattice [G: Change > Markov heads - the scorer rates the K best
+ * candidates of neighbouring positions; E: DFlash v2 - packed Top-K lattice gated by the
+ * draft hidden states; P: Markov head - the next-token table lives over the target
+ * vocabulary]. Head form: tau(a, b) = E[a] . W[b], E and W [V_t, rank] row-major in
+ * `table_dtype`; gate gamma_{r,j} = sigmoid(h_{r,j} . g) with h the hidden row of block
+ * row (r, j) ([rows, ldh], `hidden_dtype`) and g [H]; gamma = 1 when hidden == NULL.
+ *   trans[r, 0, 0, b]  = gamma_{r,0} tau(prev[r], cand_tgt[r,0,b]),  trans[r,0,a>0,:] = 0;
+ *   trans[r, j, a, b]  = gamma_{r,j} tau(cand_tgt[r,j-1,a], cand_tgt[r,j,b]),  j >= 1;
+ *   gate[r, j] = gamma_{r,j}.
+ * cand_tgt [R, B, K] int32 (K = K' of dspark_topk, 1..64); prev [R] int32 target ids.
+ * trans [R, B, K, K] float32, gate [R, B] float32. bf16 tables with rank % 64 == 0 and
+ * rank <= 512 use the tensor cores (tcgen05); other tables use CUDA-core FMAs.
+ * Out-of-range ids set DSPARK_ERANGE and give zero transitions.
+ */
+dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int32_t* prev, int64_t R,
+                                   int32_t B, int32_t K, const void* E, const void* W,
+                                   dspark_dtype table_dtype, int64_t V_t, int32_t rank,
+                                   const void* hidden, const void* g, dspark_dtype hidden_dtype,
+                                   int32_t H, int64_t ldh, const int64_t* row_start,
+                                   float* trans, float* gate, int32_t* dev_status,
+                                   dspark_stream_t stream);
+
+/*
+ * Chain selection over the lattice [G: block-sampler commit - greedy requests walk the
+ * lattice taking the best candidate after the token before; sampled requests walk it
+ * with the draft RNG]. Unary scores u = cand_val [R, B, K], transitions trans
+ * [R, B, K, K] as written by dspark_lattice_score, all float32.
+ *   DSPARK_MAXSUM: delta_0 = u_0 + A_0[0]; delta_j[b] = u_j[b] + max_a(delta_{j-1}[a] +
+ *     A_j[a, b]) (lowest a on ties); the chain ends at argmax delta_{B-1}; score = its max.
+ *   DSPARK_WALK: b_j = argmax_b fl32(u_j[b] + A_j[b_{j-1}, b]) (A_0 row 0 for j = 0).
+ *   DSPARK_SAMPLE: the same row, sampled at `temperature`/`top_p` over the K candidates
+ *     (candidate rank is the index), uniform U(seed[r], step[r], j, purpose 0); the sparse
+ *     q of every position goes to q->ids/p/n with q->cap >= K. temperature <= 0 is greedy.
+ * Outputs: chain_rank [R, B] int32, chain_tgt [R, B] int32 (= cand_tgt at the rank),
+ * score [R] float32 (sum of the chosen row entries; the max for MAXSUM).
+ * seed, step: [R] uint64 (SAMPLE only). No workspace.
+ */
+dspark_status dspark_chain_select(const float* cand_val, const float* trans,
+                                  const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
+                                  dspark_chain_mode mode, float temperature, float top_p,
+                                  const uint64_t* seed, const uint64_t* step,
+                                  int32_t* chain_rank, int32_t* chain_tgt, float* score,
+                                  const dspark_qrecord* q, int32_t* dev_status,
+                                  dspark_stream_t stream);
+
+/*
+ * Full-row multinomial drafting without a head [G: Change > Sampled drafting; commits on
+ * the thresholded top-p filter, double sums and the double uniform]. Rows as in
+ * dspark_topk (transform included). Per block row (r, j): z = s / T, weights, top-p
+ * nucleus (shortest prefix of (w desc, index asc) whose double mass exceeds top_p), draw
+ * with U(seed[r], step[r], j, purpose 0) walking kept indices in ascending order.
+ * temperature <= 0: argmax. out_tgt [R, B] int32 target ids, out_idx [R, B] int32 draft
+ * indices (nullable). q: NULL, or a record (sparse with cap >= the nucleus size, else
+ * DSPARK_EINVAL on *dev_status and n = -1; or dense with ldz >= V_d). ws: see
+ * dspark_workspace_size(DSPARK_OP_SAMPLE, R, B, V_d, 0).
+ */
+dspark_status dspark_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
+                            int64_t V_d, int64_t ld, const int64_t* row_start,
+                            const int64_t* d2t, int64_t V_t, float mult, float softcap,
+                            float temperature, float top_p, const uint64_t* seed,
+                            const uint64_t* step, int32_t* out_tgt, int32_t* out_idx,
+                            const dspark_qrecord* q, void* ws, size_t ws_bytes,
+                            int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * Dense Markov walk, markov_head_top_k = 0 [G: Change > Markov heads - the dense walk
+ * corrects every drafted position with one head inference per position; block-sampler
+ * commit - a dense step biases the scaled rows by the token drafted before].
+ * For j = 0..B-1, per request: v_j[i] = s_j[i] + gamma_j tau(prev_j, m(i)) over draft
+ * indices i < V_d; x_j = argmax (temperature <= 0) or a draw as in dspark_sample with
+ * U(seed[r], step[r], j, purpose 0); out_tgt[r, j] = m(x_j) = prev_{j+1}; prev_0 = prev[r].
+ * Head and gate arguments as in dspark_lattice_score (bf16 tables, rank % 64 == 0, rank
+ * <= 256, use the tensor cores). q: NULL or a dense record (ldz >= V_d). R <= 128.
+ * ws: dspark_workspace_size(DSPARK_OP_DENSE_WALK, R, B, V_d, 0).
+ */
+dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
+                                int64_t V_d, int64_t ld, const int64_t* row_start,
+                                const int32_t* prev, const void* E, const void* W,
+                                dspark_dtype table_dtype, int32_t rank, int64_t V_t,
+                                const int64_t* d2t, const void* hidden, const void* g,
+                                dspark_dtype hidden_dtype, int32_t H, int64_t ldh, float mult,
+                                float softcap, float temperature, float top_p,
+                                const uint64_t* seed, const uint64_t* step, int32_t* out_tgt,
+                                int32_t* out_idx, const dspark_qrecord* q, void* ws,
+                                size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
+
+/*
+ * Rejection-sampling verification [G: commit on exact sampled speculative decoding -
+ * accept with probability min(1, p/q), otherwise emit a sample of norm(max(0, p - q)) and
+ * drop the later candidates; accepted tokens report the target's log-probability; ids
+ * beyond a model's row have zero probability; Fixes > split validation windows - row j
+ * validates candidate j, row n is the bonus row].
+ * tgt_logits: [rows, ld] of `dtype`; request r owns rows row_start[r] + j, j <= B (B + 1
+ * rows; row_start NULL means r * (B + 1)). draft_tgt [R, B] int32 target ids, n_draft [R]
+ * int32 (0..B). q: the proposal record of the drafted tokens, one record row per (r, j)
+ * at r * B + j: sparse (ids in target space) or dense over draft indices with the
+ * identity map (V_q = its width; ids >= V_q have q = 0). Ignored when temperature <= 0.
+ * p_j is the post-filter target distribution at (temperature, top_p). For j < n: accept
+ * iff U(vseed[r], step[r], j, 1) < p_j(x_j)/q_j(x_j) (double); first rejection: emit a
+ * draw from norm(max(0, p_j - q_j)) with U(..., j, 2) and stop; all accepted: bonus draw
+ * from p_n with U(..., n, 2). temperature <= 0: accept iff x_j == argmax p_j, emit argmax.
+ * Outputs: out_tokens [R, B+1] (accepted tokens then the correction or bonus; -1 after),
+ * n_accepted [R] (-1 with DSPARK_EPROPOSAL when q(x_j) = 0), logprob [R, B+1] float32
+ * (log p_j of each emitted token; greedy reports the temperature-1 log-probability).
+ * ws: dspark_workspace_size(DSPARK_OP_VERIFY, R, B, V_t, 0).
+ */
+dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B,
+                            int64_t V_t, int64_t ld, const int64_t* row_start,
+                            const int32_t* draft_tgt, const int32_t* n_draft,
+                            const dspark_qrecord* q, int64_t V_q, float temperature,
+                            float top_p, const uint64_t* vseed, const uint64_t* step,
+                            int32_t* out_tokens, int32_t* n_accepted, float* logprob,
+                            void* ws, size_t ws_bytes, int32_t* dev_status,
+                            dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */
