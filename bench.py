@@ -1,0 +1,393 @@
+"""Benchmark of the block-draft hot path on GB300: drafted blocks/s and logit HBM GB/s.
+
+Default workload: the Qwen3-4B-shaped greedy draft (32 requests x block 7, V = 151,936 bf16
+logits with one +8 peak per row, K = 64, rank-256 bf16 Markov head, max-sum chain). One step is
+one pass of the draft path over one batch: dspark_topk -> dspark_lattice_score ->
+dspark_chain_select. Inputs are seeded synthetic tensors of the pages' shapes, resident in HBM;
+the logits rotate over several independent sets whose total exceeds the 129 MB L2, so every step
+reads cold logits. Steps are replayed as CUDA graphs (one graph per input set).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2..5]
+
+Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak scaling, no
+collective on the data path); timing is the max over ranks after a barrier.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")  # the CPU baseline runs the oracle on one core
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dspark_inputs as di  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+METRIC = "drafted blocks/s and logit HBM GB/s (fraction of ~8 TB/s peak), 1×GB300"
+UNIT = "blocks/s"
+PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_cluster_kernel_qwen3_4b_R32_B7_V151936.md")
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampler running while the timed regions run."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
+        busy = [r for r in rows if r[4].strip().isdigit() and int(r[4]) > 0] or rows
+        sm = [float(r[1]) for r in busy if _isnum(r[1])]
+        mx = [float(r[2]) for r in rows if _isnum(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in busy for n, v in zip(names, r[6:10]) if v.strip().lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(busy)}
+
+
+def _isnum(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+def workload_for(config):
+    return {2: di.config2, 3: di.config3, 4: di.config4, 5: di.config5}[config]
+
+
+def algorithmic_logit_bytes(w):
+    return w["R"] * w["B"] * w["V_d"] * (2 if w["dtype"] == "bf16" else 4)
+
+
+def traffic_from_profile():
+    """dram bytes per top-k launch from the committed ncu summary, if the kernel source is unchanged."""
+    try:
+        text = open(PROFILE_TOPK).read()
+        sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
+        dram = float(re.search(r"dram_bytes_per_launch:\s*([0-9.e+]+)", text).group(1))
+    except Exception:
+        return None
+    src = open(os.path.join(ROOT, "dspark_draft_selection_gb300", "csrc", "topk.cu"), "rb").read()
+    return dram if hashlib.sha256(src).hexdigest() == sha else None
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import dspark_draft_selection_gb300 as ds
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if args.config != 2:
+        raise SystemExit("only the Qwen3-4B-shaped greedy draft (--config 2) is timed by this bench")
+
+    def to_dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w0 = di.config2()
+    R, B, K = w0["R"], w0["B"], w0["K"]
+    logit_bytes = algorithmic_logit_bytes(w0)
+    nsets = max(2, int(np.ceil(2 * L2_BYTES / logit_bytes)))
+    sets = []
+    for s in range(nsets):
+        w = w0 if s == 0 else di.lattice_workload(2 + 100 * s, R=R, B=B, V_d=w0["V_d"], K=K, rank=256, peak=8.0)
+        sets.append(dict(logits=to_dev(w["logits"]), prev=to_dev(w["prev"])))
+    E, W = to_dev(w0["E"]), to_dev(w0["W"])
+    Kp = min(K, w0["V_d"])
+    cand = (torch.empty((R, B, Kp), dtype=torch.int32, device=dev), torch.empty((R, B, Kp), dtype=torch.int32, device=dev),
+            torch.empty((R, B, Kp), dtype=torch.float32, device=dev))
+    trans = (torch.empty((R, B, Kp, Kp), dtype=torch.float32, device=dev), torch.empty((R, B), dtype=torch.float32,
+                                                                                      device=dev))
+    chain = (torch.empty((R, B), dtype=torch.int32, device=dev), torch.empty((R, B), dtype=torch.int32, device=dev),
+             torch.empty((R,), dtype=torch.float32, device=dev))
+    status = ds.new_status(dev)
+
+    def topk(s):
+        ds.dspark_topk(sets[s]["logits"], B, K, out=cand, status=status)
+
+    def lattice(s):
+        ds.dspark_lattice_score(cand[1], sets[s]["prev"], E, W, out=trans, status=status)
+
+    def chain_sel(s):
+        ds.dspark_chain_select(cand[2], trans[0], cand[1], "maxsum", out=chain, status=status)
+
+    def step(s):
+        topk(s)
+        lattice(s)
+        chain_sel(s)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(nsets):       # first calls configure the kernels outside any capture
+            step(s)
+    torch.cuda.synchronize()
+    assert ds.read_status(status) == 0
+
+    def capture(fn_list):
+        """One graph that runs fn_list over every input set in turn."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(nsets):
+                for fn in fn_list:
+                    fn(s)
+        return g
+
+    g_step = capture([step])
+    g_topk = capture([topk])
+    g_lat = capture([lattice])
+    g_chain = capture([chain_sel])
+
+    # end to end through the same entry points with host buffers: H2D of the step's logits and
+    # previous tokens, the draft path, D2H of the chosen chain and its score
+    host_logits = [sets[s]["logits"].cpu().pin_memory() for s in range(nsets)]
+    host_prev = [sets[s]["prev"].cpu().pin_memory() for s in range(nsets)]
+    dev_logits = torch.empty_like(sets[0]["logits"])
+    dev_prev = torch.empty_like(sets[0]["prev"])
+    host_out = torch.empty((R, B), dtype=torch.int32).pin_memory()
+    host_score = torch.empty((R,), dtype=torch.float32).pin_memory()
+
+    def e2e(s):
+        dev_logits.copy_(host_logits[s], non_blocking=True)
+        dev_prev.copy_(host_prev[s], non_blocking=True)
+        ds.dspark_topk(dev_logits, B, K, out=cand, status=status)
+        ds.dspark_lattice_score(cand[1], dev_prev, E, W, out=trans, status=status)
+        ds.dspark_chain_select(cand[2], trans[0], cand[1], "maxsum", out=chain, status=status)
+        host_out.copy_(chain[1], non_blocking=True)
+        host_score.copy_(chain[2], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e(0)
+    torch.cuda.synchronize()
+    g_e2e = capture([e2e])
+    h2d_bytes = host_logits[0].numel() * host_logits[0].element_size() + host_prev[0].numel() * 4
+    d2h_bytes = host_out.numel() * 4 + host_score.numel() * 4
+
+    reps = max(1, -(-args.steps // nsets))
+    steps = reps * nsets
+
+    def timed(graph):
+        """ms for `steps` steps (replays of the all-sets graph), max over ranks."""
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        if ws > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    clocks = Clocks(dev.index)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-args.warmup // nsets))):
+            g_step.replay()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.2)
+        ms_total = timed(g_step)
+        ms_topk = timed(g_topk) / steps
+        ms_lat = timed(g_lat) / steps
+        ms_chain = timed(g_chain) / steps
+        g_e2e.replay()
+        ms_e2e = timed(g_e2e)
+        clk = clocks.stop()
+    assert ds.read_status(status) == 0, "device status set during the bench"
+    ms_step = ms_total / steps
+    value = ws * R * steps / (ms_total / 1e3)
+    hbm, hbm_kind = peaks()
+    achieved = logit_bytes / (ms_topk / 1e3) / 1e9
+    traffic = traffic_from_profile()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Gaussian logits and head tables)",
+        "config": {"workload": w0["name"], "requests": R, "block": B, "vocab": w0["V_d"], "k": K, "rank": 256,
+                   "chain": "maxsum", "per_gpu_batch": R, "parallelism": f"replicas x{ws} (requests sharded)",
+                   "l2": f"{nsets} rotating logit sets of {logit_bytes / 1e6:.1f} MB (> 129 MB L2)",
+                   "graphs": "each step replayed as a CUDA graph"},
+        "logit_gbs": round(achieved, 1),
+        "kernels_ms": {"topk": round(ms_topk, 5), "lattice": round(ms_lat, 5), "chain": round(ms_chain, 5)},
+        "roofline": {"kernel": "topk_cluster_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "algorithmic_bytes": logit_bytes},
+        "e2e": {"value": round(ws * R * steps / (ms_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes)},
+        "gpu_launches": 3 * steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle legs
+# ------------------------------------------------------------------------------------------------
+
+def oracle_blocks(w, reqs):
+    from oracle import draft as od
+    s = di.bf16_bits_to_f32(w["logits"])
+    E, W = di.bf16_bits_to_f32(w["E"]), di.bf16_bits_to_f32(w["W"])
+    B = w["B"]
+    for r in reqs:
+        od.select_request(s[r * B:(r + 1) * B], w["K"], E, W, int(w["prev"][r]), w["mode"])
+    return len(reqs)
+
+
+def cpu_baseline(w, nreq=10):
+    t0 = time.perf_counter()
+    n = oracle_blocks(w, list(range(nreq)))
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {w['R']} requests of {w['name']} (numpy oracle, one thread)"}
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step drafts a bounded sample of the
+    workload (whole requests when the run fits in about two minutes, else single block rows whose
+    Top-K is the bulk of the work, plus the lattice and chain of every request they complete)."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    from oracle import draft as od
+    w = di.config2()
+    s = di.bf16_bits_to_f32(w["logits"])
+    E, W = di.bf16_bits_to_f32(w["E"]), di.bf16_bits_to_f32(w["W"])
+    B, R, K = w["B"], w["R"], w["K"]
+    t0 = time.perf_counter()
+    oracle_blocks(w, [0])
+    t_req = time.perf_counter() - t0
+    budget = 120.0
+    rows_per_step = int(max(1, min(B * 4, budget * B / (t_req * max(1, args.steps + args.warmup)))))
+    cols = w["V_d"]
+    if rows_per_step == 1 and t_req / B * (args.steps + args.warmup) > budget:
+        cols = max(K, int(w["V_d"] * budget * B / (t_req * (args.steps + args.warmup))))
+    state = {"row": 0, "cand": [], "vals": []}
+
+    def one_step():
+        done = 0.0
+        for _ in range(rows_per_step):
+            r, j = divmod(state["row"] % (R * B), B)
+            idx, val = od.topk_row(od.row_transform(s[r * B + j, :cols]), K)
+            state["cand"].append(idx)
+            state["vals"].append(val)
+            state["row"] += 1
+            if j == B - 1:
+                A = od.lattice_request(np.array(state["cand"]), int(w["prev"][r]), E, W, [1.0] * B)
+                od.chain_maxsum(np.array(state["vals"]), A)
+                state["cand"], state["vals"] = [], []
+            done += (1.0 / B) * (cols / w["V_d"])
+        return done
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    done = 0.0
+    for _ in range(args.steps):
+        done += one_step()
+    dt = time.perf_counter() - t0
+    value = done / dt
+    sample = (f"{rows_per_step} block rows x {cols} of {w['V_d']} columns of {w['name']} per step "
+              f"(numpy oracle, one thread)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Gaussian logits and head tables)",
+        "config": {"workload": w["name"], "requests": R, "block": B, "vocab": w["V_d"], "k": K, "rank": 256,
+                   "chain": "maxsum"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
