@@ -8,7 +8,10 @@
 // (nucleus = shortest prefix of (probability desc, index asc) whose mass exceeds top_p), the
 // double-sum commit and the double-uniform commit; the candidate rank is the row index.
 //
-// One CTA per request; the lattice is read once (coalesced over candidates b).
+// One CTA of 256 threads per request. The K'xK' tile of position j + 1 streams into shared
+// memory (cp.async, double buffered) while position j is decided, so the lattice is read once
+// and its latency hides behind the recurrence. Max-sum uses all threads (4 threads per column b,
+// 16 predecessors each); the walks use warp 0 with the row after the previous choice.
 #include "dspark_common.cuh"
 #include "host_common.h"
 
@@ -36,52 +39,233 @@ struct ChainArgs {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(CH_THREADS) chain_maxsum_kernel(const ChainArgs a) {
+// cp.async one position's K x K tile (K*K floats; K*K*4 is a multiple of 16 when K % 2 == 0,
+// otherwise the tail goes element-wise)
+DS_DEV void ch_load_tile(float* dst, const float* src, int n) {
+  const int nvec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0) ? n / 4 : 0;
+  for (int i = threadIdx.x; i < nvec; i += CH_THREADS) ds_cp_async16(dst + 4 * i, src + 4 * i);
+  for (int i = 4 * nvec + threadIdx.x; i < n; i += CH_THREADS) dst[i] = src[i];
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+DS_DEV void ch_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+DS_DEV void ch_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// warp inclusive scan of doubles
+DS_DEV double ch_warp_scan(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
+  __shared__ __align__(16) float s_tile[2][CH_MAXK * CH_MAXK];
+  __shared__ float s_u[CH_MAXB * CH_MAXK];
   __shared__ float s_delta[CH_MAXK];
   __shared__ float s_bv[4][CH_MAXK];
   __shared__ int s_ba[4][CH_MAXK];
   __shared__ uint8_t s_back[CH_MAXB][CH_MAXK];
+  __shared__ float s_w[CH_MAXK];
+  __shared__ int s_order[CH_MAXK];
+
   const int r = blockIdx.x, K = a.K, B = a.B, t = threadIdx.x;
+  const int KK = K * K;
   const float* u = a.u + int64_t(r) * B * K;
-  const float* A = a.trans + int64_t(r) * B * K * K;
-  if (t < K) s_delta[t] = __fadd_rn(u[t], A[t]);        // delta_0 = u_0 + A_0[0, :]
-  __syncthreads();
-  const int b = t & 63, part = t >> 6;
-  for (int j = 1; j < B; ++j) {
-    const float* Aj = A + int64_t(j) * K * K;
-    if (b < K) {
-      float best = -INFINITY;
-      int ba = -1;
-      const int a0 = part * 16, a1 = min(K, a0 + 16);
-      for (int aa = a0; aa < a1; ++aa) {
-        const float v = __fadd_rn(s_delta[aa], Aj[aa * K + b]);
-        if (v > best || ba < 0) {
-          best = v;
-          ba = aa;
-        }
-      }
-      s_bv[part][b] = best;
-      s_ba[part][b] = ba;
+  const float* A = a.trans + int64_t(r) * B * KK;
+  for (int i = t; i < B * K; i += CH_THREADS) s_u[i] = u[i];
+  ch_load_tile(s_tile[0], A, KK);
+
+  const bool maxsum = a.mode == DSPARK_MAXSUM;
+  const bool sample = (a.mode == DSPARK_SAMPLE) && (a.T > 0.0f);
+  const uint64_t seed = sample ? a.seed[r] : 0, step = sample ? a.step[r] : 0;
+  const int warp = t >> 5, lane = t & 31;
+  int prevb = 0;
+  double score = 0.0;
+
+  for (int j = 0; j < B; ++j) {
+    if (j + 1 < B) {
+      ch_load_tile(s_tile[(j + 1) & 1], A + int64_t(j + 1) * KK, KK);
+      ch_wait_prev();
+    } else {
+      ch_wait_all();
     }
     __syncthreads();
-    float nd = 0.0f;
-    if (t < K) {
-      float best = s_bv[0][t];
-      int ba = s_ba[0][t];
-      for (int p = 1; p < 4; ++p) {
-        if (s_ba[p][t] >= 0 && (ba < 0 || s_bv[p][t] > best)) {
-          best = s_bv[p][t];
-          ba = s_ba[p][t];
+    const float* Aj = s_tile[j & 1];
+    const float* uj = s_u + j * K;
+    if (maxsum) {
+      if (j == 0) {
+        if (t < K) s_delta[t] = __fadd_rn(uj[t], Aj[t]);          // delta_0 = u_0 + A_0[0, :]
+      } else {
+        const int b = t & 63, part = t >> 6;
+        if (b < K) {
+          float best = -INFINITY;
+          int ba = -1;
+          const int a0 = part * 16, a1 = min(K, a0 + 16);
+          for (int aa = a0; aa < a1; ++aa) {
+            const float v = __fadd_rn(s_delta[aa], Aj[aa * K + b]);
+            if (v > best || ba < 0) {
+              best = v;
+              ba = aa;
+            }
+          }
+          s_bv[part][b] = best;
+          s_ba[part][b] = ba;
+        }
+        __syncthreads();
+        float nd = 0.0f;
+        if (t < K) {
+          float best = s_bv[0][t];
+          int ba = s_ba[0][t];
+          for (int p = 1; p < 4; ++p) {
+            if (s_ba[p][t] >= 0 && (ba < 0 || s_bv[p][t] > best)) {
+              best = s_bv[p][t];
+              ba = s_ba[p][t];
+            }
+          }
+          nd = __fadd_rn(uj[t], best);
+          s_back[j][t] = uint8_t(ba < 0 ? 0 : ba);
+        }
+        __syncthreads();
+        if (t < K) s_delta[t] = nd;
+      }
+    } else if (warp == 0) {
+      const float* row = (j == 0) ? Aj : Aj + prevb * K;
+      float v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = lane + 32 * h;
+        v[h] = (b < K) ? __fadd_rn(uj[b], row[b]) : -INFINITY;
+      }
+      int pick;
+      const int64_t qrow = int64_t(r) * B + j;
+      if (!sample) {
+        const uint64_t k0 = (lane < K) ? ds_key64(ds_canon_zero(v[0]), lane) : 0;
+        const uint64_t k1 = (lane + 32 < K) ? ds_key64(ds_canon_zero(v[1]), lane + 32) : 0;
+        pick = int(ds_key64_idx(ds_warp_max_u64(k0 > k1 ? k0 : k1)));
+        if (a.mode == DSPARK_SAMPLE && lane == 0 && a.q_n) {
+          a.q_n[qrow] = 1;
+          a.q_ids[qrow * a.q_cap] = a.cand_tgt[qrow * K + pick];
+          a.q_p[qrow * a.q_cap] = 1.0f;
+        }
+      } else {
+        float zmax = -INFINITY, z[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          z[h] = (lane + 32 * h < K) ? ds_temper(v[h], a.T) : -INFINITY;
+          zmax = fmaxf(zmax, z[h]);
+        }
+        zmax = ds_warp_max(zmax);
+        float w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int b = lane + 32 * h;
+          w[h] = (b < K) ? ds_weight(__fsub_rn(z[h], zmax)) : 0.0f;
+          if (b < K) s_w[b] = w[h];
+        }
+        __syncwarp();
+        const double wall = ds_warp_sum(double(w[0]) + double(w[1]));
+        // kept[h]: nucleus membership of candidate lane + 32h
+        bool kept[2] = {w[0] > 0.0f, w[1] > 0.0f};
+        if (a.top_p < 1.0f) {
+          // rank in (weight desc, rank asc) order, then the running mass in that order
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int b = lane + 32 * h;
+            if (b < K) {
+              int rk = 0;
+              for (int c = 0; c < K; ++c) {
+                const float wc = s_w[c];
+                rk += (wc > w[h] || (wc == w[h] && c < b)) ? 1 : 0;
+              }
+              s_order[rk] = b;
+            }
+          }
+          __syncwarp();
+          // sorted position sp = 2 * lane + h holds candidate s_order[sp]
+          double pw[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int sp = 2 * lane + h;
+            pw[h] = (sp < K) ? double(s_w[s_order[sp]]) / wall : 0.0;
+          }
+          const double incl = ch_warp_scan(pw[0] + pw[1]);
+          const double c0 = incl - pw[1];           // running mass through sorted position 2*lane
+          const double tp = double(a.top_p);
+          const bool over0 = (2 * lane < K) && c0 > tp && pw[0] > 0.0;
+          const bool over1 = (2 * lane + 1 < K) && incl > tp && pw[1] > 0.0;
+          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, over0), b1 = __ballot_sync(0xFFFFFFFFu, over1);
+          int cut = K;                              // first sorted position whose running mass > top_p
+          if (b0 | b1) {
+            const int l0 = b0 ? __ffs(b0) - 1 : 32, l1 = b1 ? __ffs(b1) - 1 : 32;
+            cut = min(2 * l0, 2 * l1 + 1);
+          }
+          // candidate b is kept iff its sorted position is <= cut (and its weight is positive)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int b = lane + 32 * h;
+            if (b < K && cut < K) {
+              int rk = 0;
+              for (int c = 0; c < K; ++c) {
+                const float wc = s_w[c];
+                rk += (wc > w[h] || (wc == w[h] && c < b)) ? 1 : 0;
+              }
+              kept[h] = kept[h] && rk <= cut;
+            }
+          }
+        }
+        // draw: kept candidates in ascending rank order; running sums by warp scan
+        // (lane holds ranks lane and lane + 32: scan the first half, then the second)
+        const double k0w = kept[0] ? double(w[0]) : 0.0, k1w = kept[1] ? double(w[1]) : 0.0;
+        const double inc0 = ch_warp_scan(k0w);
+        const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
+        const double inc1 = tot0 + ch_warp_scan(k1w);
+        const double wk = __shfl_sync(0xFFFFFFFFu, inc1, 31);
+        const double target = ds_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT) * wk;
+        const unsigned c0 = __ballot_sync(0xFFFFFFFFu, kept[0] && inc0 > target);
+        const unsigned c1 = __ballot_sync(0xFFFFFFFFu, kept[1] && inc1 > target);
+        if (c0) pick = __ffs(c0) - 1;
+        else if (c1) pick = 32 + __ffs(c1) - 1;
+        else {
+          const unsigned l0 = __ballot_sync(0xFFFFFFFFu, kept[0]), l1 = __ballot_sync(0xFFFFFFFFu, kept[1]);
+          pick = l1 ? 32 + (31 - __clz(int(l1))) : (l0 ? 31 - __clz(int(l0)) : 0);
+        }
+        if (a.q_n) {
+          // kept candidates in ascending rank order with q = w / W_kept
+          const unsigned m0 = __ballot_sync(0xFFFFFFFFu, kept[0]), m1 = __ballot_sync(0xFFFFFFFFu, kept[1]);
+          const unsigned below = (1u << lane) - 1u;
+          const int n0 = __popc(m0);
+          if (kept[0]) {
+            const int o = __popc(m0 & below);
+            if (o < a.q_cap) {
+              a.q_ids[qrow * a.q_cap + o] = a.cand_tgt[qrow * K + lane];
+              a.q_p[qrow * a.q_cap + o] = float(double(w[0]) / wk);
+            }
+          }
+          if (kept[1]) {
+            const int o = n0 + __popc(m1 & below);
+            if (o < a.q_cap) {
+              a.q_ids[qrow * a.q_cap + o] = a.cand_tgt[qrow * K + lane + 32];
+              a.q_p[qrow * a.q_cap + o] = float(double(w[1]) / wk);
+            }
+          }
+          if (lane == 0) a.q_n[qrow] = n0 + __popc(m1);
         }
       }
-      nd = __fadd_rn(u[j * K + t], best);
-      s_back[j][t] = uint8_t(ba < 0 ? 0 : ba);
+      const float vp = __shfl_sync(0xFFFFFFFFu, pick < 32 ? v[0] : v[1], pick & 31);
+      score += double(vp);
+      if (lane == 0) {
+        a.chain_rank[r * B + j] = pick;
+        a.chain_tgt[r * B + j] = a.cand_tgt[(int64_t(r) * B + j) * K + pick];
+      }
+      prevb = pick;
     }
-    __syncthreads();
-    if (t < K) s_delta[t] = nd;
     __syncthreads();
   }
-  if (t == 0) {
+  if (maxsum && t == 0) {
     int bb = 0;
     float best = s_delta[0];
     for (int k = 1; k < K; ++k)
@@ -96,139 +280,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_maxsum_kernel(const ChainArg
       if (j > 0) bb = s_back[j][bb];
     }
   }
-}
-
-// Greedy and sampled walks: warp 0 of the CTA walks the lattice position by position.
-__global__ void __launch_bounds__(32) chain_walk_kernel(const ChainArgs a) {
-  __shared__ float s_w[CH_MAXK];
-  __shared__ int s_order[CH_MAXK];
-  __shared__ uint8_t s_kept[CH_MAXK];
-  const int r = blockIdx.x, K = a.K, B = a.B, lane = threadIdx.x;
-  const float* u = a.u + int64_t(r) * B * K;
-  const float* A = a.trans + int64_t(r) * B * K * K;
-  const bool sample = (a.mode == DSPARK_SAMPLE) && (a.T > 0.0f);
-  const uint64_t seed = sample ? a.seed[r] : 0, step = sample ? a.step[r] : 0;
-  int prevb = 0;
-  double score = 0.0;
-  for (int j = 0; j < B; ++j) {
-    const float* row = (j == 0) ? A : A + (int64_t(j) * K + prevb) * K;
-    float v[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int b = lane + 32 * h;
-      v[h] = (b < K) ? __fadd_rn(u[j * K + b], row[b]) : -INFINITY;
-    }
-    int pick;
-    const int64_t qrow = int64_t(r) * B + j;
-    if (!sample) {
-      uint64_t k0 = (lane < K) ? ds_key64(ds_canon_zero(v[0]), lane) : 0;
-      uint64_t k1 = (lane + 32 < K) ? ds_key64(ds_canon_zero(v[1]), lane + 32) : 0;
-      pick = int(ds_key64_idx(ds_warp_max_u64(k0 > k1 ? k0 : k1)));
-      if (a.mode == DSPARK_SAMPLE && lane == 0 && a.q_n) {
-        a.q_n[qrow] = 1;
-        a.q_ids[qrow * a.q_cap] = a.cand_tgt[qrow * K + pick];
-        a.q_p[qrow * a.q_cap] = 1.0f;
-      }
-    } else {
-      float z[2], zmax = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        z[h] = (lane + 32 * h < K) ? ds_temper(v[h], a.T) : -INFINITY;
-        zmax = fmaxf(zmax, z[h]);
-      }
-      zmax = ds_warp_max(zmax);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = lane + 32 * h;
-        if (b < K) {
-          s_w[b] = ds_weight(__fsub_rn(z[h], zmax));
-          s_kept[b] = 0;
-        }
-      }
-      __syncwarp();
-      if (a.top_p < 1.0f) {
-        // rank of every candidate in (weight desc, rank asc) order
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int b = lane + 32 * h;
-          if (b < K) {
-            const float wb = s_w[b];
-            int rk = 0;
-            for (int c = 0; c < K; ++c) {
-              const float wc = s_w[c];
-              rk += (wc > wb || (wc == wb && c < b)) ? 1 : 0;
-            }
-            s_order[rk] = b;
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        double wall = 0.0;
-        for (int b = 0; b < K; ++b) wall += double(s_w[b]);
-        if (a.top_p < 1.0f) {
-          double cum = 0.0;
-          const double tp = double(a.top_p);
-          bool over = false;
-          for (int k = 0; k < K; ++k) {
-            const int b = s_order[k];
-            if (!(s_w[b] > 0.0f)) break;
-            cum += double(s_w[b]) / wall;
-            s_kept[b] = 1;
-            if (cum > tp) {
-              over = true;
-              break;
-            }
-          }
-          if (!over)
-            for (int b = 0; b < K; ++b) s_kept[b] = s_w[b] > 0.0f;
-        } else {
-          for (int b = 0; b < K; ++b) s_kept[b] = s_w[b] > 0.0f;
-        }
-        double wk = 0.0;
-        int last = -1, nk = 0;
-        for (int b = 0; b < K; ++b)
-          if (s_kept[b]) {
-            wk += double(s_w[b]);
-            last = b;
-          }
-        const double target = ds_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT) * wk;
-        double c = 0.0;
-        int chosen = last;
-        for (int b = 0; b < K; ++b)
-          if (s_kept[b]) {
-            c += double(s_w[b]);
-            if (c > target) {
-              chosen = b;
-              break;
-            }
-          }
-        if (a.q_n) {
-          for (int b = 0; b < K; ++b)
-            if (s_kept[b]) {
-              if (nk < a.q_cap) {
-                a.q_ids[qrow * a.q_cap + nk] = a.cand_tgt[qrow * K + b];
-                a.q_p[qrow * a.q_cap + nk] = float(double(s_w[b]) / wk);
-              }
-              ++nk;
-            }
-          a.q_n[qrow] = nk;
-        }
-        s_order[0] = chosen < 0 ? 0 : chosen;
-      }
-      __syncwarp();
-      pick = s_order[0];
-      __syncwarp();
-    }
-    const float vp = __shfl_sync(0xFFFFFFFFu, pick < 32 ? v[0] : v[1], pick & 31);
-    score += double(vp);
-    if (lane == 0) {
-      a.chain_rank[r * B + j] = pick;
-      a.chain_tgt[r * B + j] = a.cand_tgt[(int64_t(r) * B + j) * K + pick];
-    }
-    prevb = pick;
-  }
-  if (lane == 0) a.score[r] = float(score);
+  if (!maxsum && t == 0) a.score[r] = float(score);
 }
 
 }  // namespace
@@ -271,9 +323,6 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
     }
   }
   if (R == 0) return DSPARK_OK;
-  if (mode == DSPARK_MAXSUM)
-    chain_maxsum_kernel<<<unsigned(R), CH_THREADS, 0, stream>>>(a);
-  else
-    chain_walk_kernel<<<unsigned(R), 32, 0, stream>>>(a);
+  chain_kernel<<<unsigned(R), CH_THREADS, 0, stream>>>(a);
   return ds_launch_status();
 }

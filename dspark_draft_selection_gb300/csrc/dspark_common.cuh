@@ -159,6 +159,23 @@ DS_DEV uint64_t ds_warp_max_u64(uint64_t v) {
 }
 
 // ----------------------------------------------------------------------------------------
+// gate gamma = sigmoid(h . g) of one hidden row, whole block: float32 partial dots per thread,
+// summed in double; s_red holds one float per warp.
+// ----------------------------------------------------------------------------------------
+template <typename HT>
+DS_DEV float ds_block_gate(const HT* h, const HT* g, int H, float* s_red) {
+  float acc = 0.0f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) acc = __fmaf_rn(ds_load_elem<HT>(h + k), ds_load_elem<HT>(g + k), acc);
+  acc = ds_warp_sumf(acc);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  double dot = 0.0;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) dot += double(s_red[w]);
+  __syncthreads();
+  return float(1.0 / (1.0 + exp(-dot)));
+}
+
+// ----------------------------------------------------------------------------------------
 // shared-memory bitonic sort of n2 (power of two) 64-bit keys, descending; whole block
 // ----------------------------------------------------------------------------------------
 DS_DEV void ds_block_sort_desc(uint64_t* s, int n2) {
@@ -297,6 +314,25 @@ DS_DEV void ds_tmem_ld_32x32b_x64(uint32_t taddr, float (&v)[64]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns into 32 registers (one warp).
+DS_DEV void ds_tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Ampere-style 16-byte async copy global -> shared (any 16-byte-aligned destination).

@@ -41,25 +41,13 @@ struct LatticeArgs {
   int hidden_bf16;
 };
 
-template <typename HT>
-DS_DEV float lt_gate(const LatticeArgs& a, int64_t hrow, float* s_red) {
-  // gamma = sigmoid(h . g): float32 partial dots per thread, summed in double
-  const HT* h = reinterpret_cast<const HT*>(a.hidden) + hrow * a.ldh;
-  const HT* g = reinterpret_cast<const HT*>(a.g);
-  float acc = 0.0f;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) acc = __fmaf_rn(ds_load_elem<HT>(h + k), ds_load_elem<HT>(g + k), acc);
-  acc = ds_warp_sumf(acc);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
-  __syncthreads();
-  double dot = 0.0;
-  for (int w = 0; w < int(blockDim.x >> 5); ++w) dot += double(s_red[w]);
-  __syncthreads();
-  return float(1.0 / (1.0 + exp(-dot)));
-}
-
 DS_DEV float lt_gate_any(const LatticeArgs& a, int64_t hrow, float* s_red) {
   if (a.hidden == nullptr) return 1.0f;
-  return a.hidden_bf16 ? lt_gate<__nv_bfloat16>(a, hrow, s_red) : lt_gate<float>(a, hrow, s_red);
+  if (a.hidden_bf16)
+    return ds_block_gate(reinterpret_cast<const __nv_bfloat16*>(a.hidden) + hrow * a.ldh,
+                         reinterpret_cast<const __nv_bfloat16*>(a.g), a.H, s_red);
+  return ds_block_gate(reinterpret_cast<const float*>(a.hidden) + hrow * a.ldh, reinterpret_cast<const float*>(a.g),
+                       a.H, s_red);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -155,16 +143,24 @@ __global__ void __launch_bounds__(LT_THREADS) lattice_tc_kernel(const LatticeArg
     ok = ds_mbar_wait(&s_bar, 0, DS_WAIT_LIMIT);     // let in-flight MMAs drain before freeing TMEM
   }
   ds_tc_fence_after();
+  // stage the K x K tile through shared memory (the operand buffers are free once the MMAs
+  // completed) so that the stores below are coalesced
+  float* stage = reinterpret_cast<float*>(base);     // [64][65] floats
   if (ok) {
     float v[64];
     ds_tmem_ld_32x32b_x64(tmem + (uint32_t(warp * 32) << 16), v);
     const int arow = warp * 32 + lane;
     if (arow < K) {
-      float* out = a.trans + (int64_t(tile) * K + arow) * K;
-      const bool live = arow < Ka;
 #pragma unroll
-      for (int b = 0; b < 64; ++b)
-        if (b < K) out[b] = live ? __fmul_rn(gamma, v[b]) : 0.0f;
+      for (int b = 0; b < 64; ++b) stage[arow * 65 + b] = v[b];
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    float* out = a.trans + int64_t(tile) * K * K;
+    for (int e = threadIdx.x; e < K * K; e += LT_THREADS) {
+      const int arow = e / K, b = e - arow * K;
+      out[e] = (arow < Ka) ? __fmul_rn(gamma, stage[arow * 65 + b]) : 0.0f;
     }
   }
   if (threadIdx.x == 0 && a.gate) a.gate[tile] = gamma;
@@ -273,7 +269,7 @@ extern "C" dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int
   const bool tc = table_dtype == DSPARK_BF16 && rank % 64 == 0 && rank <= 512 &&
                   ds_aligned(E, 16) && ds_aligned(W, 16);
   if (tc) {
-    const size_t smem = size_t(rank / 64) * (LT_M + LT_N) * 128 + 1024;
+    const size_t smem = std::max<size_t>(size_t(rank / 64) * (LT_M + LT_N) * 128, 64 * 65 * 4) + 1024;
     static size_t configured = 0;
     if (smem > configured) {
       DS_CUDA_TRY(cudaFuncSetAttribute(lattice_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
