@@ -63,8 +63,7 @@ DS_DEV double ch_warp_scan(double v) {
 }
 
 __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
-  __shared__ __align__(16) float s_tile[2][CH_MAXK * CH_MAXK];
-  __shared__ float s_u[CH_MAXB * CH_MAXK];
+  extern __shared__ __align__(16) float ch_dyn[];      // [2][K*K] tiles, then [B*K] unary scores
   __shared__ float s_delta[CH_MAXK];
   __shared__ float s_bv[4][CH_MAXK];
   __shared__ int s_ba[4][CH_MAXK];
@@ -74,10 +73,13 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 
   const int r = blockIdx.x, K = a.K, B = a.B, t = threadIdx.x;
   const int KK = K * K;
+  float* s_tile0 = ch_dyn;
+  float* s_tile1 = ch_dyn + ((KK + 3) & ~3);
+  float* s_u = s_tile1 + ((KK + 3) & ~3);
   const float* u = a.u + int64_t(r) * B * K;
   const float* A = a.trans + int64_t(r) * B * KK;
   for (int i = t; i < B * K; i += CH_THREADS) s_u[i] = u[i];
-  ch_load_tile(s_tile[0], A, KK);
+  ch_load_tile(s_tile0, A, KK);
 
   const bool maxsum = a.mode == DSPARK_MAXSUM;
   const bool sample = (a.mode == DSPARK_SAMPLE) && (a.T > 0.0f);
@@ -88,13 +90,13 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 
   for (int j = 0; j < B; ++j) {
     if (j + 1 < B) {
-      ch_load_tile(s_tile[(j + 1) & 1], A + int64_t(j + 1) * KK, KK);
+      ch_load_tile(((j + 1) & 1) ? s_tile1 : s_tile0, A + int64_t(j + 1) * KK, KK);
       ch_wait_prev();
     } else {
       ch_wait_all();
     }
     __syncthreads();
-    const float* Aj = s_tile[j & 1];
+    const float* Aj = (j & 1) ? s_tile1 : s_tile0;
     const float* uj = s_u + j * K;
     if (maxsum) {
       if (j == 0) {
@@ -323,6 +325,12 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
     }
   }
   if (R == 0) return DSPARK_OK;
-  chain_kernel<<<unsigned(R), CH_THREADS, 0, stream>>>(a);
+  const size_t smem = (2 * size_t((K * K + 3) & ~3) + size_t(B) * K) * sizeof(float);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+    configured = smem;
+  }
+  chain_kernel<<<unsigned(R), CH_THREADS, smem, stream>>>(a);
   return ds_launch_status();
 }

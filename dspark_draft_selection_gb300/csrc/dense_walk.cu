@@ -161,9 +161,10 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
     bool ok = ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);
     if (!ok) {
       ds_set_error(a.status, DSPARK_ETIMEOUT);
-      ok = ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);
-      alive = false;
+      ok = ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);   // let in-flight MMAs drain
     }
+    ok = __syncthreads_and(ok) != 0;                     // one verdict for the whole CTA
+    alive = ok;
     phase ^= 1;
     ds_tc_fence_after();
     if (ok) {

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(LT_THREADS) lattice_tc_kernel(const LatticeArg
     ds_set_error(a.status, DSPARK_ETIMEOUT);
     ok = ds_mbar_wait(&s_bar, 0, DS_WAIT_LIMIT);     // let in-flight MMAs drain before freeing TMEM
   }
+  ok = __syncthreads_and(ok) != 0;                 // one verdict for the whole CTA
   ds_tc_fence_after();
   // stage the K x K tile through shared memory (the operand buffers are free once the MMAs
   // completed) so that the stores below are coalesced

@@ -344,7 +344,13 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   for (int i = nk + tid; i < n2; i += TK_THREADS) s_keys[i] = 0;
   __syncthreads();
   ds_block_sort_desc(s_keys, n2);
-  if (tid < a.Kp) {
+  if (tid < a.Kp && tid >= nk) {               // unreachable: >= K' keys always reach the sort
+    ds_set_error(a.status, DSPARK_EINVAL);
+    const int64_t o = row_id * a.Kp + tid;
+    a.cand_draft[o] = -1;
+    a.cand_tgt[o] = -1;
+    a.cand_val[o] = -INFINITY;
+  } else if (tid < a.Kp) {
     const uint64_t k64 = s_keys[tid];
     const uint32_t idx = ds_key64_idx(k64);
     int64_t tgt = idx;
