@@ -219,6 +219,12 @@ struct SampleArgs {
   int q_mode;                // 0 none, 1 sparse, 2 dense
   int write_z;
   int64_t q_row_mul, q_row_add;  // record row = row_id * mul + add
+  // verification hooks: skip the draw; report the weight of a probed index and the argmax
+  int no_draw;
+  const int32_t* probe_tgt;      // [R, B - 1] drafted target ids probed in row j < n_draft[r]
+  const int32_t* n_draft;        // [R]; rows j > n_draft[r] are skipped
+  float* probe_w;                // [rows] weight of the probed id if kept, else 0
+  int32_t* amax_out;             // [rows] argmax index (lowest on ties)
   int32_t* status;
 };
 

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(rs::THREADS, 1) sample_cluster_kernel(const rs
   const int64_t row_id = blockIdx.x / C;
   const int64_t r = row_id / a.B, j = row_id % a.B;
   const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
+  if (a.n_draft && j > a.n_draft[r]) return;        // every CTA of the cluster leaves together
   const T* row = reinterpret_cast<const T*>(a.rows) + prow * a.ld;
   const rs::RowGeom g = rs::row_geom<T>(row, a.V, C, crank);
   const int tid = threadIdx.x;
@@ -287,10 +288,49 @@ __global__ void __launch_bounds__(rs::THREADS, 1) sample_cluster_kernel(const rs
     const double cpre = rs::cluster_sum_d(cl, cr, ctot, 2, &wtot);
     const int64_t last_kept = int64_t(rs::cluster_max_u64(cl, cr, rs::block_max_u64(lastk, bs))) - 1;
     wkept = wtot;
-    const double u = ds_uniform(a.seed[r], a.step[r], uint32_t(a.position >= 0 ? a.position : int32_t(j)),
+    if (a.amax_out) {
+      // argmax of z (lowest index on ties), for greedy verification
+      unsigned long long best = 0;
+#pragma unroll
+      for (int k = 0; k < rs::MAXV; ++k) {
+        const int64_t v = g.vec_index(k);
+        if (v >= 0) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(ds_vec_elem<T>(buf[k], e))), uint32_t(g.head + v * EPV + e)));
+        }
+      }
+      if (g.has_head()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rh)), uint32_t(ih)));
+      if (g.has_tail()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rt)), uint32_t(it)));
+      best = rs::cluster_max_u64(cl, cr, rs::block_max_u64(best, bs));
+      if (crank == 0 && tid == 0) a.amax_out[row_id] = int32_t(ds_key64_idx(best));
+    }
+    if (a.probe_w) {
+      const int64_t x = (a.probe_tgt && j < a.n_draft[r]) ? int64_t(a.probe_tgt[r * (a.B - 1) + j]) : -1;
+      if (crank == 0 && tid == 0 && (x < 0 || x >= a.V)) a.probe_w[row_id] = 0.0f;
+      if (x >= 0 && x < a.V) {
+        auto probe = [&](float raw, int64_t i) {
+          if (i == x) {
+            const float w = wof(raw);
+            a.probe_w[row_id] = sp_keep(w, i, wcut, icut) ? w : 0.0f;
+          }
+        };
+        if (g.has_head()) probe(rh, ih);
+        if (g.has_tail()) probe(rt, it);
+#pragma unroll
+        for (int k = 0; k < rs::MAXV; ++k) {
+          const int64_t v = g.vec_index(k);
+          if (v >= 0 && x >= g.head + v * EPV && x < g.head + (v + 1) * EPV) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) probe(ds_vec_elem<T>(buf[k], e), g.head + v * EPV + e);
+          }
+        }
+      }
+    }
+    const double u = a.no_draw ? 2.0 : ds_uniform(a.seed[r], a.step[r], uint32_t(a.position >= 0 ? a.position : int32_t(j)),
                                 DS_PURPOSE_DRAFT);
     const double target = u * wtot;
-    if (target >= cpre && target < cpre + ctot) {
+    if (!a.no_draw && target >= cpre && target < cpre + ctot) {
       // this CTA holds the crossing: find the segment, then the thread, then the element
       const int warp = tid >> 5, lane = tid & 31;
       if (warp < SEGS) {
@@ -381,7 +421,7 @@ __global__ void __launch_bounds__(rs::THREADS, 1) sample_cluster_kernel(const rs
         }
         if (pick < 0) pick = lastmine;
       }
-    } else if (crank == C - 1 && tid == 0 && !(target < wtot)) {
+    } else if (!a.no_draw && crank == C - 1 && tid == 0 && !(target < wtot)) {
       pick = last_kept;      // rounding left the target at the very end
     }
   }

@@ -402,8 +402,8 @@ cudaError_t tk_launch(const TopkArgs& a, int64_t rows, cudaStream_t stream) {
 }  // namespace
 
 extern "C" size_t dspark_internal_ws_topk(int64_t R, int32_t B, int64_t V) {
-  // bf16 rows split finest; the layout for float32 rows needs no more
-  return tk_layout(R * B, V, 2).total;
+  // float32 rows hold 4 elements per 16-byte vector, so they split into the most parts
+  return std::max(tk_layout(R * B, V, 4).total, tk_layout(R * B, V, 2).total);
 }
 
 extern "C" dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
