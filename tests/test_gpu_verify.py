@@ -85,11 +85,14 @@ def test_verify_sparse_record_pruned_draft(T, top_p):
     drafted = host(chain_tgt)
     ids_h, qp_h, qn_h = host(ids), host(qp), host(qn)
     target = di.normal(di.generator(80, 20), (R * (B + 1), 7000), 2.0, "bf16")
-    # make acceptance likely: the target puts mass where the draft did
+    # requests 1.. get targets close to their proposals (p ~ q: mostly accepted); request 0 keeps a
+    # random target (mostly rejected)
     tf = as_f32(target).copy()
-    for r in range(R):
+    for r in range(1, R):
         for j in range(B):
-            tf[r * (B + 1) + j, ids_h[r, j, :qn_h[r, j]]] += 6.0
+            k = qn_h[r, j]
+            tf[r * (B + 1) + j] = -40.0
+            tf[r * (B + 1) + j, ids_h[r, j, :k]] = T * np.log(qp_h[r, j, :k].astype(np.float64))
     target = di.f32_to_bf16_bits(tf)
     vseed = np.arange(R, dtype=np.uint64) * 7919 + 3
     n = np.full(R, B, dtype=np.int32)
@@ -103,7 +106,7 @@ def test_verify_sparse_record_pruned_draft(T, top_p):
         return full
 
     assert oracle_check(target, B, drafted, n, qfun, T, top_p, vseed, w["step"], toks, nacc, lp) == 0
-    assert nacc.sum() > 0
+    assert nacc[1:].mean() > 2
 
 
 def test_verify_greedy_is_argmax_matching():
