@@ -38,7 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2**20
 METRIC = "drafted blocks/s and logit HBM GB/s (fraction of ~8 TB/s peak), 1×GB300"
 UNIT = "blocks/s"
-PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_cluster_kernel_qwen3_4b_R32_B7_V151936.md")
+PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_part_kernel_qwen3_4b_R32_B7_V151936.md")
 
 
 def peaks():
@@ -276,7 +276,7 @@ def run_ours(args):
                    "graphs": "each step replayed as a CUDA graph"},
         "logit_gbs": round(achieved, 1),
         "kernels_ms": {"topk": round(ms_topk, 5), "lattice": round(ms_lat, 5), "chain": round(ms_chain, 5)},
-        "roofline": {"kernel": "topk_cluster_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "topk_part_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": traffic, "algorithmic_bytes": logit_bytes},
         "e2e": {"value": round(ws * R * steps / (ms_e2e / 1e3), 1), "unit": UNIT,

@@ -100,14 +100,16 @@ __global__ void __launch_bounds__(LT_THREADS) lattice_tc_kernel(const LatticeArg
   const int cpr = rank / 8;                          // 16-byte chunks per table row
   const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(a.E);
   const __nv_bfloat16* W = reinterpret_cast<const __nv_bfloat16*>(a.W);
-  for (int t = threadIdx.x; t < LT_M * cpr; t += LT_THREADS) {
+  // rows past Ka (A) and K (B) only feed accumulator rows/columns that are never read, so they
+  // are left as they are; a live row with an out-of-range id is zeroed (zero transitions)
+  for (int t = threadIdx.x; t < Ka * cpr; t += LT_THREADS) {
     const int m = t / cpr, c = t % cpr, kb = c >> 3, cc = c & 7;
     uint8_t* dst = sA + kb * (LT_M * 128) + m * 128 + ((cc ^ (m & 7)) << 4);
     const int32_t id = s_ida[m];
     if (id >= 0) ds_cp_async16(dst, E + int64_t(id) * rank + c * 8);
     else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
-  for (int t = threadIdx.x; t < LT_N * cpr; t += LT_THREADS) {
+  for (int t = threadIdx.x; t < K * cpr; t += LT_THREADS) {
     const int m = t / cpr, c = t % cpr, kb = c >> 3, cc = c & 7;
     uint8_t* dst = sB + kb * (LT_N * 128) + m * 128 + ((cc ^ (m & 7)) << 4);
     const int32_t id = s_idb[m];

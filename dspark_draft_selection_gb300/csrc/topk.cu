@@ -226,27 +226,43 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
 #pragma unroll
   for (int w = 1; w < TK_WARPS; ++w) thr = fminf(thr, s_wthr[w]);
 
-  // survivors: elements >= thr (packed compares screen 8 elements at a time)
+  // survivors: elements >= thr. Each round k gives every lane an 8-bit mask of its survivors
+  // (packed compares screen 8 bf16 at a time); the warp then drains the masks together, one
+  // survivor per lane per pass, with one shared-memory atomic per pass (a per-lane loop would
+  // run for the whole warp whenever any lane had a survivor).
   {
     const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact: thr is an element value or -inf
+    const unsigned below = (1u << lane) - 1u;
 #pragma unroll
     for (int k = 0; k < TK_MAXV; ++k) {
       const int64_t v = v0 + k * TK_THREADS + tid;
+      uint32_t m8 = 0;
       if (v < v1) {
-        bool any = true;
         if constexpr (PACKED) {
-          any = (__hge2_mask(tk_b2(buf[k].x), thr2) | __hge2_mask(tk_b2(buf[k].y), thr2) |
-                 __hge2_mask(tk_b2(buf[k].z), thr2) | __hge2_mask(tk_b2(buf[k].w), thr2)) != 0u;
-        }
-        if (any) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float x = tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap);
-            if (x >= thr) {
-              const uint32_t slot = atomicAdd(&s_n, 1u);
-              if (slot < TK_PART_CAP) s_keys[slot] = ds_key64(ds_canon_zero(x), uint32_t(head + v * EPV + e));
-            }
+          const uint32_t c0 = __hge2_mask(tk_b2(buf[k].x), thr2), c1 = __hge2_mask(tk_b2(buf[k].y), thr2);
+          const uint32_t c2 = __hge2_mask(tk_b2(buf[k].z), thr2), c3 = __hge2_mask(tk_b2(buf[k].w), thr2);
+          if ((c0 | c1 | c2 | c3) != 0u) {
+            m8 = (c0 & 1u) | ((c0 >> 15) & 2u) | ((c1 & 1u) << 2) | ((c1 >> 13) & 8u) | ((c2 & 1u) << 4) |
+                 ((c2 >> 11) & 32u) | ((c3 & 1u) << 6) | ((c3 >> 9) & 128u);
           }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            m8 |= (tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap) >= thr) ? (1u << e) : 0u;
+        }
+      }
+      while (true) {
+        const unsigned act = __ballot_sync(0xFFFFFFFFu, m8 != 0u);
+        if (act == 0u) break;
+        uint32_t slot = 0;
+        const int leader = __ffs(act) - 1;
+        if (lane == leader) slot = atomicAdd(&s_n, uint32_t(__popc(act)));
+        slot = __shfl_sync(0xFFFFFFFFu, slot, leader) + uint32_t(__popc(act & below));
+        if (m8 != 0u) {
+          const int e = __ffs(m8) - 1;
+          m8 &= m8 - 1u;
+          const float x = tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap);
+          if (slot < TK_PART_CAP) s_keys[slot] = ds_key64(ds_canon_zero(x), uint32_t(head + v * EPV + e));
         }
       }
     }
