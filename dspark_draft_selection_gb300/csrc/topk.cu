@@ -155,11 +155,14 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   __shared__ uint32_t s_n;
   __shared__ int s_last;
 
-  const int P = a.P;
-  const int64_t row_id = blockIdx.x / P;             // r * B + j
-  const int p = int(blockIdx.x % P);
-  const int64_t r = row_id / a.B, j = row_id % a.B;
-  const int64_t prow = a.row_start ? a.row_start[r] + j : row_id;
+  const int P = a.P;                                  // a power of two
+  const uint32_t row_id = blockIdx.x >> (31 - __clz(P));   // r * B + j
+  const int p = int(blockIdx.x & uint32_t(P - 1));
+  int64_t prow = row_id;
+  if (a.row_start) {
+    const uint32_t r = row_id / uint32_t(a.B);
+    prow = a.row_start[r] + (row_id - r * uint32_t(a.B));
+  }
   const T* row = reinterpret_cast<const T*>(a.logits) + prow * a.ld;
   const int64_t V = a.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -173,11 +176,11 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   const int64_t v0 = int64_t(p) * a.nvp, v1 = min(nvec, v0 + a.nvp);
   const uint4* vbase = reinterpret_cast<const uint4*>(row + head);
 
+  const int32_t lv0 = int32_t(v0) + tid, lv1 = int32_t(v1);   // this lane's vector indices (V < 2^31)
   uint4 buf[TK_MAXV];
 #pragma unroll
   for (int k = 0; k < TK_MAXV; ++k) {
-    const int64_t v = v0 + k * TK_THREADS + tid;
-    if (v < v1) buf[k] = ds_ld_stream(vbase + v);
+    if (lv0 + k * TK_THREADS < lv1) buf[k] = ds_ld_stream(vbase + (lv0 + k * TK_THREADS));
   }
   float xextra = -INFINITY;
   int64_t iextra = -1;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
     __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
 #pragma unroll
     for (int k = 0; k < TK_MAXV; ++k) {
-      if (v0 + k * TK_THREADS + tid < v1) {
+      if (lv0 + k * TK_THREADS < lv1) {
         m2 = __hmax2(m2, tk_b2(buf[k].x));
         m2 = __hmax2(m2, tk_b2(buf[k].y));
         m2 = __hmax2(m2, tk_b2(buf[k].z));
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   } else {
 #pragma unroll
     for (int k = 0; k < TK_MAXV; ++k) {
-      if (v0 + k * TK_THREADS + tid < v1) {
+      if (lv0 + k * TK_THREADS < lv1) {
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
           tmax = fmaxf(tmax, tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap));
@@ -215,10 +218,13 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   const int m = (a.Kp + TK_WARPS - 1) / TK_WARPS;
   uint32_t key = ds_key32(ds_canon_zero(tmax));
   uint32_t kth = 0;
-  for (int t = 0; t < m; ++t) {
-    kth = __reduce_max_sync(0xFFFFFFFFu, key);
-    const unsigned who = __ballot_sync(0xFFFFFFFFu, key == kth);
-    if (lane == __ffs(who) - 1) key = 0;
+#pragma unroll
+  for (int t = 0; t < (64 + TK_WARPS - 1) / TK_WARPS; ++t) {
+    if (t < m) {
+      kth = __reduce_max_sync(0xFFFFFFFFu, key);
+      const unsigned who = __ballot_sync(0xFFFFFFFFu, key == kth);
+      if (lane == __ffs(who) - 1) key = 0;
+    }
   }
   if (lane == 0) s_wthr[warp] = (kth <= ds_key32(-INFINITY)) ? -INFINITY : ds_key32_to_float(kth);
   __syncthreads();
@@ -226,44 +232,54 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
 #pragma unroll
   for (int w = 1; w < TK_WARPS; ++w) thr = fminf(thr, s_wthr[w]);
 
-  // survivors: elements >= thr. Each round k gives every lane an 8-bit mask of its survivors
-  // (packed compares screen 8 bf16 at a time); the warp then drains the masks together, one
-  // survivor per lane per pass, with one shared-memory atomic per pass (a per-lane loop would
-  // run for the whole warp whenever any lane had a survivor).
+  // survivors: elements >= thr. Every round k adds an 8-bit mask of this lane's survivors to one
+  // 64-bit mask (packed compares, no branches); the warp then drains all masks together, one
+  // survivor per lane per pass with one shared-memory atomic per pass, so a lane's rare
+  // survivors do not hold the whole warp in a per-element loop.
   {
     const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact: thr is an element value or -inf
-    const unsigned below = (1u << lane) - 1u;
+    const int32_t vv0 = lv0, vv1 = lv1;
+    unsigned long long mm = 0;
 #pragma unroll
     for (int k = 0; k < TK_MAXV; ++k) {
-      const int64_t v = v0 + k * TK_THREADS + tid;
       uint32_t m8 = 0;
-      if (v < v1) {
+      if (vv0 + k * TK_THREADS < vv1) {
         if constexpr (PACKED) {
           const uint32_t c0 = __hge2_mask(tk_b2(buf[k].x), thr2), c1 = __hge2_mask(tk_b2(buf[k].y), thr2);
           const uint32_t c2 = __hge2_mask(tk_b2(buf[k].z), thr2), c3 = __hge2_mask(tk_b2(buf[k].w), thr2);
-          if ((c0 | c1 | c2 | c3) != 0u) {
-            m8 = (c0 & 1u) | ((c0 >> 15) & 2u) | ((c1 & 1u) << 2) | ((c1 >> 13) & 8u) | ((c2 & 1u) << 4) |
-                 ((c2 >> 11) & 32u) | ((c3 & 1u) << 6) | ((c3 >> 9) & 128u);
-          }
+          // bytes [e0 e1 e2 e3] and [e4 e5 e6 e7] (0x00 / 0xFF), then one bit per element
+          const uint32_t w01 = __byte_perm(c0, c1, 0x6420), w23 = __byte_perm(c2, c3, 0x6420);
+          uint32_t f = (w01 & 0x08040201u) | (w23 & 0x80402010u);
+          f |= f >> 16;
+          f |= f >> 8;
+          m8 = f & 0xFFu;
         } else {
 #pragma unroll
           for (int e = 0; e < EPV; ++e)
             m8 |= (tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap) >= thr) ? (1u << e) : 0u;
         }
       }
-      while (true) {
-        const unsigned act = __ballot_sync(0xFFFFFFFFu, m8 != 0u);
-        if (act == 0u) break;
-        uint32_t slot = 0;
-        const int leader = __ffs(act) - 1;
-        if (lane == leader) slot = atomicAdd(&s_n, uint32_t(__popc(act)));
-        slot = __shfl_sync(0xFFFFFFFFu, slot, leader) + uint32_t(__popc(act & below));
-        if (m8 != 0u) {
-          const int e = __ffs(m8) - 1;
-          m8 &= m8 - 1u;
-          const float x = tk_xform<XFORM>(ds_vec_elem<T>(buf[k], e), a.mult, a.softcap);
-          if (slot < TK_PART_CAP) s_keys[slot] = ds_key64(ds_canon_zero(x), uint32_t(head + v * EPV + e));
-        }
+      mm |= (unsigned long long)m8 << (8 * k);
+    }
+    const unsigned below = (1u << lane) - 1u;
+    while (true) {
+      const unsigned act = __ballot_sync(0xFFFFFFFFu, mm != 0ull);
+      if (act == 0u) break;
+      uint32_t slot = 0;
+      const int leader = __ffs(act) - 1;
+      if (lane == leader) slot = atomicAdd(&s_n, uint32_t(__popc(act)));
+      slot = __shfl_sync(0xFFFFFFFFu, slot, leader) + uint32_t(__popc(act & below));
+      if (mm != 0ull) {
+        const int bit = __ffsll(mm) - 1;
+        mm &= mm - 1ull;
+        const int k = bit >> 3, e = bit & 7;
+        uint4 q = buf[0];
+#pragma unroll
+        for (int kk = 1; kk < TK_MAXV; ++kk)
+          if (k == kk) q = buf[kk];
+        const float x = tk_xform<XFORM>(ds_vec_elem<T>(q, e), a.mult, a.softcap);
+        if (slot < TK_PART_CAP)
+          s_keys[slot] = ds_key64(ds_canon_zero(x), uint32_t(head) + uint32_t(vv0 + k * TK_THREADS) * EPV + uint32_t(e));
       }
     }
     if (iextra >= 0 && xextra >= thr) {
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   }
   __syncthreads();
   const uint32_t n = s_n;
-  const int64_t part = row_id * P + p;
+  const int64_t part = int64_t(row_id) * P + p;
   for (uint32_t i = tid; i < min(n, uint32_t(TK_PART_CAP)); i += TK_THREADS) a.ws_keys[part * TK_PART_CAP + i] = s_keys[i];
   if (tid == 0) {
     a.ws_cnt[part] = n;
@@ -301,8 +317,8 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
     uint32_t off = 0;
     int bad = 0;
     for (int q = 0; q < P; ++q) {
-      const uint32_t c = __ldcg(&a.ws_cnt[row_id * P + q]);
-      rthr = fmaxf(rthr, __ldcg(&a.ws_thr[row_id * P + q]));
+      const uint32_t c = __ldcg(&a.ws_cnt[int64_t(row_id) * P + q]);
+      rthr = fmaxf(rthr, __ldcg(&a.ws_thr[int64_t(row_id) * P + q]));
       bad |= c > uint32_t(TK_PART_CAP);
       s_off[q] = off;
       off += min(c, uint32_t(TK_PART_CAP));
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
     int q = 0;
     for (uint32_t g = tid; g < s_off[P]; g += TK_THREADS) {
       while (g >= s_off[q + 1]) ++q;
-      const uint64_t k = __ldcg(&a.ws_keys[(row_id * P + q) * TK_PART_CAP + (g - s_off[q])]);
+      const uint64_t k = __ldcg(&a.ws_keys[(int64_t(row_id) * P + q) * TK_PART_CAP + (g - s_off[q])]);
       if (ds_key64_val(k) >= rthr) {
         const uint32_t slot = atomicAdd(&s_n, 1u);
         if (slot < TK_MERGE_CAP) s_keys[slot] = k;
@@ -332,8 +348,11 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   int nk;
   if (!s_bad && ngot <= uint32_t(TK_MERGE_CAP)) {
     // exact K'-th largest value among them, by bisection on the value key
+    // (bf16 values without a transform have keys whose low 16 bits carry no order, so the
+    // bisection stops after the top 16 bits)
     uint32_t vres = 0;
-    for (int b = 31; b >= 0; --b) {
+    const int blo = PACKED ? 16 : 0;
+    for (int b = 31; b >= blo; --b) {
       const uint32_t cand = vres | (1u << b);
       uint32_t c = 0;
       for (uint32_t i = tid; i < ngot; i += TK_THREADS) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
@@ -362,7 +381,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
   ds_block_sort_desc(s_keys, n2);
   if (tid < a.Kp && tid >= nk) {               // unreachable: >= K' keys always reach the sort
     ds_set_error(a.status, DSPARK_EINVAL);
-    const int64_t o = row_id * a.Kp + tid;
+    const int64_t o = int64_t(row_id) * a.Kp + tid;
     a.cand_draft[o] = -1;
     a.cand_tgt[o] = -1;
     a.cand_val[o] = -INFINITY;
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(TK_THREADS, 4) topk_part_kernel(const TopkArgs
         tgt = -1;
       }
     }
-    const int64_t o = row_id * a.Kp + tid;
+    const int64_t o = int64_t(row_id) * a.Kp + tid;
     a.cand_draft[o] = int32_t(idx);
     a.cand_tgt[o] = int32_t(tgt);
     a.cand_val[o] = ds_key64_val(k64);
