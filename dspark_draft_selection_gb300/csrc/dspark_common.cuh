@@ -226,6 +226,22 @@ DS_DEV bool ds_mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   return false;
 }
 
+// Arrive on an mbarrier and add `bytes` to the transaction count its phase waits for.
+DS_DEV void ds_mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ds_smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Bulk asynchronous copy global -> shared (16-byte aligned, size a multiple of 16) that
+// completes `bytes` of the mbarrier's transaction count.
+DS_DEV void ds_bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          ds_smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(ds_smem_addr(bar))
+      : "memory");
+}
+
 DS_DEV void ds_fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
