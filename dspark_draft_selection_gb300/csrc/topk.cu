@@ -8,16 +8,17 @@
 // draft vocabulary (target id i + d2t[i]). optimum-intel PR #2098 runs this selection with the
 // OpenVINO GPU plugin's radix TopK; this kernel is a different, exact design for sm_103a.
 //
-// Design: persistent CTAs (one per SM) stream row parts of up to 42 KB through a 3-stage
+// Design: persistent CTAs (two per SM) stream row parts of up to 42 KB through a 2-stage
 // shared-memory ring filled by bulk asynchronous copies (cp.async.bulk + mbarrier transaction
 // counts), so HBM keeps streaming while a part is processed; the logits are read once.
 // Per part (~85 elements per lane):
 //  1. Each warp takes the m-th largest of its lanes' maxima (m = ceil(K'/8), warp REDUX rounds):
 //     each lane maximum is a distinct element, so 8 warps x m >= K' elements are >= the minimum
 //     T_p over the warps; T_p bounds the part's K'-th largest value from below.
-//  2. Elements >= T_p survive (a few K' per part): packed bf16x2 compares give each lane an 8-bit
-//     mask per 16-byte vector, and the warp drains the masks together (one survivor per lane per
-//     pass, one shared-memory atomic per pass), reading values back from shared memory.
+//  2. Elements >= T_p survive (a few K' per part). The vectors whose maximum (kept from the first
+//     pass) clears T_p are queued per warp; the warp takes them 32 at a time, builds 8-bit
+//     survivor masks with packed bf16x2 compares and drains them together (one survivor per lane
+//     per pass, one shared-memory atomic per pass), reading values back from shared memory.
 //  3. Survivors go, as 64-bit (value, lower index first) keys, to a per-part workspace slot.
 //  4. The CTA that completes a row's last part (a ticket counter) merges: max_p T_p bounds the
 //     row's K'-th value, a bisection over the surviving values finds the exact K'-th value, and
@@ -33,10 +34,12 @@ namespace {
 
 constexpr int TK_THREADS = 256;
 constexpr int TK_WARPS = TK_THREADS / 32;
-constexpr int TK_STAGES = 3;
+constexpr int TK_STAGES = 2;
 constexpr int TK_STAGE_VEC = 2688;      // 16-byte vectors per stage (42 KB)
 constexpr int TK_PART_CAP = 512;        // survivor keys kept per part
 constexpr int TK_MERGE_CAP = 2048;      // keys gathered by the merging CTA
+constexpr int TK_ROUNDS = (TK_STAGE_VEC + TK_THREADS - 1) / TK_THREADS;   // vectors per lane per part
+constexpr int TK_QCAP = 32 * TK_ROUNDS;  // per-warp queue of candidate vectors
 static_assert(TK_PART_CAP <= TK_MERGE_CAP, "part survivors are staged in the merge buffer");
 
 struct TopkArgs {
@@ -168,7 +171,7 @@ __device__ __noinline__ int tk_row_exact(const TopkArgs& a, const T* row, uint64
 }
 
 template <typename T, bool XFORM>
-__global__ void __launch_bounds__(TK_THREADS, 1) topk_stream_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkArgs a) {
   constexpr int EPV = 16 / sizeof(T);
   constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
   extern __shared__ __align__(128) uint8_t tk_dyn[];      // TK_STAGES x TK_STAGE_VEC x 16 bytes
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1) topk_stream_kernel(const TopkAr
   __shared__ uint32_t s_n;
   __shared__ int s_last, s_bad;
   __shared__ float s_rthr;
+  __shared__ uint16_t s_queue[TK_WARPS][TK_QCAP];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = a.P;
@@ -241,20 +245,23 @@ __global__ void __launch_bounds__(TK_THREADS, 1) topk_stream_kernel(const TopkAr
       return;
     }
 
-    // lane maximum
+    // lane maximum, keeping every vector's own maximum for the screening pass
     float tmax = xextra;
-    if constexpr (PACKED) {
-      __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
-      for (int i = tid; i < nv; i += TK_THREADS) {
-        const uint4 w = sv[i];
-        m2 = __hmax2(m2, __hmax2(__hmax2(tk_b2(w.x), tk_b2(w.y)), __hmax2(tk_b2(w.z), tk_b2(w.w))));
-      }
-      tmax = fmaxf(tmax, fmaxf(__low2float(m2), __high2float(m2)));
-    } else {
-      for (int i = tid; i < nv; i += TK_THREADS) {
-        const uint4 w = sv[i];
+    float vmax[TK_ROUNDS];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) tmax = fmaxf(tmax, tk_xform<XFORM>(ds_vec_elem<T>(w, e), a.mult, a.softcap));
+    for (int k = 0; k < TK_ROUNDS; ++k) {
+      const int i = tid + k * TK_THREADS;
+      vmax[k] = -INFINITY;
+      if (i < nv) {
+        const uint4 w = sv[i];
+        if constexpr (PACKED) {
+          const __nv_bfloat162 m2 = __hmax2(__hmax2(tk_b2(w.x), tk_b2(w.y)), __hmax2(tk_b2(w.z), tk_b2(w.w)));
+          vmax[k] = fmaxf(__low2float(m2), __high2float(m2));
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) vmax[k] = fmaxf(vmax[k], tk_xform<XFORM>(ds_vec_elem<T>(w, e), a.mult, a.softcap));
+        }
+        tmax = fmaxf(tmax, vmax[k]);
       }
     }
     // the warp's m-th largest lane maximum (removed lanes drop to key 0, below every value)
@@ -273,12 +280,26 @@ __global__ void __launch_bounds__(TK_THREADS, 1) topk_stream_kernel(const TopkAr
 #pragma unroll
     for (int w = 1; w < TK_WARPS; ++w) thr = fminf(thr, s_wthr[w]);
 
-    // survivors: per round an 8-bit mask per lane, drained by the warp together
+    // survivors: vectors whose maximum clears thr (a few percent) are queued per warp; the warp
+    // then takes them 32 at a time, builds each one's 8-bit survivor mask from packed compares, and
+    // drains the masks together (one survivor per lane per pass, one shared-memory atomic per pass)
+    uint16_t* q = s_queue[warp];
+    int qn = 0;
+#pragma unroll
+    for (int k = 0; k < TK_ROUNDS; ++k) {
+      const bool cand = vmax[k] >= thr;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, cand);
+      if (cand) q[qn + __popc(bal & below)] = uint16_t(tid + k * TK_THREADS);
+      qn += __popc(bal);
+    }
+    __syncwarp();
     const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact for bf16 rows: thr is an element value
-    for (int i0 = 0; i0 < nv; i0 += TK_THREADS) {
-      const int i = i0 + tid;
+    for (int q0 = 0; q0 < qn; q0 += 32) {
+      const int qi = q0 + lane;
       uint32_t m8 = 0;
-      if (i < nv) {
+      int i = 0;
+      if (qi < qn) {
+        i = q[qi];
         const uint4 w = sv[i];
         if constexpr (PACKED) {
           const uint32_t c0 = __hge2_mask(tk_b2(w.x), thr2), c1 = __hge2_mask(tk_b2(w.y), thr2);
@@ -473,7 +494,7 @@ cudaError_t tk_launch(const TopkArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = std::min(a.nitems, ds_num_sms());
+  const int grid = std::min(a.nitems, 2 * ds_num_sms());
   kern<<<unsigned(grid), TK_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
 }
