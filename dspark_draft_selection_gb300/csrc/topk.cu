@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
     int qn = 0;
 #pragma unroll
     for (int k = 0; k < TK_ROUNDS; ++k) {
-      const bool cand = vmax[k] >= thr;
+      const bool cand = (tid + k * TK_THREADS < nv) && vmax[k] >= thr;
       const unsigned bal = __ballot_sync(0xFFFFFFFFu, cand);
       if (cand) q[qn + __popc(bal & below)] = uint16_t(tid + k * TK_THREADS);
       qn += __popc(bal);
