@@ -276,12 +276,12 @@ def run_ours(args):
                    "graphs": "each step replayed as a CUDA graph"},
         "logit_gbs": round(achieved, 1),
         "kernels_ms": {"topk": round(ms_topk, 5), "lattice": round(ms_lat, 5), "chain": round(ms_chain, 5)},
-        "roofline": {"kernel": "topk_part_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "dspark_topk (topk_stream_kernel + topk_merge_kernel)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": traffic, "algorithmic_bytes": logit_bytes},
         "e2e": {"value": round(ws * R * steps / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes)},
-        "gpu_launches": 3 * steps,
+        "gpu_launches": 4 * steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

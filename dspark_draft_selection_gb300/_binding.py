@@ -149,7 +149,7 @@ _topk_ws = {}
 
 
 def topk_workspace(R, B, V, device="cuda"):
-    """A zero-filled Top-K workspace (its completion counters must start at zero), cached per size."""
+    """A Top-K workspace, cached per size."""
     n = int(lib().dspark_workspace_size(OP_TOPK, R, B, V, 0))
     key = (str(device), n)
     if key not in _topk_ws:

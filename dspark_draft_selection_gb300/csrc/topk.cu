@@ -20,11 +20,11 @@
 //     survivor masks with packed bf16x2 compares and drains them together (one survivor per lane
 //     per pass, one shared-memory atomic per pass), reading values back from shared memory.
 //  3. Survivors go, as 64-bit (value, lower index first) keys, to a per-part workspace slot.
-//  4. The CTA that completes a row's last part (a ticket counter) merges: max_p T_p bounds the
-//     row's K'-th value, a bisection over the surviving values finds the exact K'-th value, and
-//     a short bitonic sort orders the keys at or above it. A part whose survivors overflow its
-//     slot first tightens T_p to its own exact K'-th value; ties that still overflow send the row
-//     to an exact bisection over the row itself (slow, rare).
+//  4. A second kernel merges each row (one CTA per row): max_p T_p bounds the row's K'-th value,
+//     a bisection over the surviving values finds the exact K'-th value, and a short bitonic sort
+//     orders the keys at or above it. A part whose survivors overflow its slot first tightens T_p
+//     to its own exact K'-th value; ties that still overflow send the row to an exact bisection
+//     over the row itself (slow, rare). No CTA waits for another and the workspace keeps no state.
 #include <type_traits>
 
 #include "dspark_common.cuh"
@@ -59,7 +59,6 @@ struct TopkArgs {
   uint64_t* ws_keys;               // [rows * P * TK_PART_CAP]
   uint32_t* ws_cnt;                // [rows * P]
   float* ws_thr;                   // [rows * P]
-  uint32_t* ws_ticket;             // [rows], zero between calls
 };
 
 DS_DEV __nv_bfloat162 tk_b2(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); }
@@ -179,10 +178,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
   __shared__ uint64_t s_keys[TK_MERGE_CAP];
   __shared__ uint32_t s_red[TK_WARPS];
   __shared__ float s_wthr[TK_WARPS];
-  __shared__ uint32_t s_off[65];
   __shared__ uint32_t s_n;
-  __shared__ int s_last, s_bad;
-  __shared__ float s_rthr;
   __shared__ uint16_t s_queue[TK_WARPS][TK_QCAP];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -363,111 +359,130 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
     if (tid == 0) {
       a.ws_cnt[part] = ns;
       a.ws_thr[part] = thr;
-      __threadfence();
-      const uint32_t old = atomicAdd(&a.ws_ticket[row_id], 1u);
-      s_last = (old == uint32_t(P - 1));
     }
-    __syncthreads();
-    if (!s_last) continue;
-
-    // ---- merge: this CTA completed the row's last part ----
-    __threadfence();
-    if (tid == 0) {
-      float rthr = -INFINITY;
-      uint32_t off = 0;
-      int bad = 0;
-      for (int q = 0; q < P; ++q) {
-        const uint32_t c = __ldcg(&a.ws_cnt[int64_t(row_id) * P + q]);
-        rthr = fmaxf(rthr, __ldcg(&a.ws_thr[int64_t(row_id) * P + q]));
-        bad |= c > uint32_t(TK_PART_CAP);
-        s_off[q] = off;
-        off += min(c, uint32_t(TK_PART_CAP));
-      }
-      s_off[P] = off;
-      s_rthr = rthr;
-      s_bad = bad;
-      s_n = 0;
-    }
-    __syncthreads();
-    const float rthr = s_rthr;
-    {
-      int q = 0;
-      for (uint32_t gi = tid; gi < s_off[P]; gi += TK_THREADS) {
-        while (gi >= s_off[q + 1]) ++q;
-        const uint64_t k = __ldcg(&a.ws_keys[(int64_t(row_id) * P + q) * TK_PART_CAP + (gi - s_off[q])]);
-        if (ds_key64_val(k) >= rthr) {
-          const uint32_t slot = atomicAdd(&s_n, 1u);
-          if (slot < TK_MERGE_CAP) s_keys[slot] = k;
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t ngot = s_n;
-    int nk;
-    if (!s_bad && ngot <= uint32_t(TK_MERGE_CAP)) {
-      // exact K'-th largest value among them, by bisection on the value key (bf16 values without a
-      // transform carry no order in the low 16 key bits, so the bisection stops after the top 16)
-      uint32_t vres = 0;
-      const int blo = PACKED ? 16 : 0;
-      for (int b = 31; b >= blo; --b) {
-        const uint32_t cand = vres | (1u << b);
-        uint32_t c = 0;
-        for (uint32_t i = tid; i < ngot; i += TK_THREADS) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
-        if (tk_block_sum(c, s_red) >= uint32_t(a.Kp)) vres = cand;
-      }
-      // compact the keys at or above it to the front, a block-wide pass at a time
-      if (tid == 0) s_n = 0;
-      __syncthreads();
-      for (uint32_t i0 = 0; i0 < ngot; i0 += TK_THREADS) {
-        const uint32_t i = i0 + tid;
-        const uint64_t k = (i < ngot) ? s_keys[i] : 0;
-        const bool keep = (i < ngot) && uint32_t(k >> 32) >= vres;
-        __syncthreads();
-        if (keep) s_keys[atomicAdd(&s_n, 1u)] = k;
-        __syncthreads();
-      }
-      nk = int(s_n);
-    } else {
-      nk = tk_row_exact<T, XFORM>(a, row, s_keys, s_red, &s_n);
-    }
-    int n2 = 1;
-    while (n2 < nk) n2 <<= 1;
-    for (int i = nk + tid; i < n2; i += TK_THREADS) s_keys[i] = 0;
-    __syncthreads();
-    ds_block_sort_desc(s_keys, n2);
-    if (tid < a.Kp) {
-      const int64_t o = int64_t(row_id) * a.Kp + tid;
-      if (tid >= nk) {                              // unreachable: >= K' keys always reach the sort
-        ds_set_error(a.status, DSPARK_EINVAL);
-        a.cand_draft[o] = -1;
-        a.cand_tgt[o] = -1;
-        a.cand_val[o] = -INFINITY;
-      } else {
-        const uint64_t k64 = s_keys[tid];
-        const uint32_t idx = ds_key64_idx(k64);
-        int64_t tgt = idx;
-        if (a.d2t) {
-          tgt = int64_t(idx) + a.d2t[idx];
-          if (tgt < 0 || tgt >= a.V_t) {
-            ds_set_error(a.status, DSPARK_ERANGE);
-            tgt = -1;
-          }
-        }
-        a.cand_draft[o] = int32_t(idx);
-        a.cand_tgt[o] = int32_t(tgt);
-        a.cand_val[o] = ds_key64_val(k64);
-      }
-    }
-    if (tid == 0) a.ws_ticket[row_id] = 0;
     __syncthreads();
   }
 }
+
+// One CTA per row merges the row's part survivors: max_p T_p bounds the row's K'-th value, a
+// bisection over the surviving values finds the exact K'-th value, and a short bitonic sort orders
+// the keys at or above it.
+template <typename T, bool XFORM>
+__global__ void __launch_bounds__(TK_THREADS) topk_merge_kernel(const TopkArgs a) {
+  constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
+  __shared__ uint64_t s_keys[TK_MERGE_CAP];
+  __shared__ uint32_t s_red[2][TK_WARPS];
+  __shared__ uint32_t s_off[65];
+  __shared__ uint32_t s_n;
+  __shared__ int s_bad;
+  __shared__ float s_rthr;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = a.P;
+  const uint32_t row_id = blockIdx.x;
+  if (tid == 0) {
+    float rthr = -INFINITY;
+    uint32_t off = 0;
+    int bad = 0;
+    for (int q = 0; q < P; ++q) {
+      const uint32_t c = a.ws_cnt[int64_t(row_id) * P + q];
+      rthr = fmaxf(rthr, a.ws_thr[int64_t(row_id) * P + q]);
+      bad |= c > uint32_t(TK_PART_CAP);
+      s_off[q] = off;
+      off += min(c, uint32_t(TK_PART_CAP));
+    }
+    s_off[P] = off;
+    s_rthr = rthr;
+    s_bad = bad;
+    s_n = 0;
+  }
+  __syncthreads();
+  const float rthr = s_rthr;
+  {
+    int q = 0;
+    for (uint32_t gi = tid; gi < s_off[P]; gi += TK_THREADS) {
+      while (gi >= s_off[q + 1]) ++q;
+      const uint64_t k = a.ws_keys[(int64_t(row_id) * P + q) * TK_PART_CAP + (gi - s_off[q])];
+      if (ds_key64_val(k) >= rthr) {
+        const uint32_t slot = atomicAdd(&s_n, 1u);
+        if (slot < TK_MERGE_CAP) s_keys[slot] = k;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t ngot = s_n;
+  const TkRow g = tk_row<T>(a, row_id);
+  const T* row = reinterpret_cast<const T*>(g.row);
+  int nk;
+  if (!s_bad && ngot <= uint32_t(TK_MERGE_CAP)) {
+    // exact K'-th largest value among them, by bisection on the value key (bf16 values without a
+    // transform carry no order in the low 16 key bits, so the bisection stops after the top 16);
+    // one barrier per step, alternating the partial-count slots
+    uint32_t vres = 0;
+    const int blo = PACKED ? 16 : 0;
+    int ph = 0;
+    for (int b = 31; b >= blo; --b, ph ^= 1) {
+      const uint32_t cand = vres | (1u << b);
+      uint32_t c = 0;
+      for (uint32_t i = tid; i < ngot; i += TK_THREADS) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
+      c = __reduce_add_sync(0xFFFFFFFFu, c);
+      if (lane == 0) s_red[ph][warp] = c;
+      __syncthreads();
+      uint32_t tot = 0;
+#pragma unroll
+      for (int w = 0; w < TK_WARPS; ++w) tot += s_red[ph][w];
+      if (tot >= uint32_t(a.Kp)) vres = cand;
+    }
+    // compact the keys at or above it to the front, a block-wide pass at a time
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    for (uint32_t i0 = 0; i0 < ngot; i0 += TK_THREADS) {
+      const uint32_t i = i0 + tid;
+      const uint64_t k = (i < ngot) ? s_keys[i] : 0;
+      const bool keep = (i < ngot) && uint32_t(k >> 32) >= vres;
+      __syncthreads();
+      if (keep) s_keys[atomicAdd(&s_n, 1u)] = k;
+      __syncthreads();
+    }
+    nk = int(s_n);
+  } else {
+    nk = tk_row_exact<T, XFORM>(a, row, s_keys, s_red[0], &s_n);
+  }
+  int n2 = 1;
+  while (n2 < nk) n2 <<= 1;
+  for (int i = nk + tid; i < n2; i += TK_THREADS) s_keys[i] = 0;
+  __syncthreads();
+  ds_block_sort_desc(s_keys, n2);
+  if (tid < a.Kp) {
+    const int64_t o = int64_t(row_id) * a.Kp + tid;
+    if (tid >= nk) {                              // unreachable: >= K' keys always reach the sort
+      ds_set_error(a.status, DSPARK_EINVAL);
+      a.cand_draft[o] = -1;
+      a.cand_tgt[o] = -1;
+      a.cand_val[o] = -INFINITY;
+    } else {
+      const uint64_t k64 = s_keys[tid];
+      const uint32_t idx = ds_key64_idx(k64);
+      int64_t tgt = idx;
+      if (a.d2t) {
+        tgt = int64_t(idx) + a.d2t[idx];
+        if (tgt < 0 || tgt >= a.V_t) {
+          ds_set_error(a.status, DSPARK_ERANGE);
+          tgt = -1;
+        }
+      }
+      a.cand_draft[o] = int32_t(idx);
+      a.cand_tgt[o] = int32_t(tgt);
+      a.cand_val[o] = ds_key64_val(k64);
+    }
+  }
+}
+
 
 size_t tk_align(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct TopkLayout {
   int P, nvp;
-  size_t keys, cnt, thr, ticket, total;
+  size_t keys, cnt, thr, total;
 };
 
 TopkLayout tk_layout(int64_t rows, int64_t V, int elem_bytes) {
@@ -479,8 +494,7 @@ TopkLayout tk_layout(int64_t rows, int64_t V, int elem_bytes) {
   L.keys = tk_align(size_t(rows) * L.P * TK_PART_CAP * sizeof(uint64_t));
   L.cnt = tk_align(size_t(rows) * L.P * sizeof(uint32_t));
   L.thr = tk_align(size_t(rows) * L.P * sizeof(float));
-  L.ticket = tk_align(size_t(rows) * sizeof(uint32_t));
-  L.total = L.keys + L.cnt + L.thr + L.ticket;
+  L.total = L.keys + L.cnt + L.thr;
   return L;
 }
 
@@ -496,6 +510,9 @@ cudaError_t tk_launch(const TopkArgs& a, cudaStream_t stream) {
   }
   const int grid = std::min(a.nitems, 2 * ds_num_sms());
   kern<<<unsigned(grid), TK_THREADS, smem, stream>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<T, XFORM><<<unsigned(a.nitems / a.P), TK_THREADS, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -545,7 +562,6 @@ extern "C" dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int
   a.ws_keys = reinterpret_cast<uint64_t*>(w);
   a.ws_cnt = reinterpret_cast<uint32_t*>(w + L.keys);
   a.ws_thr = reinterpret_cast<float*>(w + L.keys + L.cnt);
-  a.ws_ticket = reinterpret_cast<uint32_t*>(w + L.keys + L.cnt + L.thr);
   const bool xform = (mult != 1.0f) || (softcap > 0.0f);
   cudaError_t e;
   if (dtype == DSPARK_BF16)

@@ -110,9 +110,8 @@ typedef struct {
 } dspark_qrecord;
 
 /* Bytes of workspace `op` needs for R requests x B positions over V columns with K
- * candidates (0: none). Workspaces need 256-byte alignment. Only dspark_topk's workspace has a
- * state: it must be zero-filled once before its first use, and every completed call leaves it
- * zero-filled again; calls that share one workspace must not overlap on the GPU. */
+ * candidates (0: none). Workspaces need 256-byte alignment and no initial contents; calls that
+ * share one workspace must not overlap on the GPU. */
 size_t dspark_workspace_size(dspark_op op, int64_t R, int32_t B, int64_t V, int32_t K);
 
 /* Human-readable name of a status code (static string). */
@@ -141,8 +140,7 @@ dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64_t V_t,
  *   cand_draft [R, B, K'] int32 draft index, cand_tgt [R, B, K'] int32 target id (-1 and
  *   DSPARK_ERANGE on *dev_status when a chosen index maps outside [0, V_t)), cand_val
  *   [R, B, K'] float32 s.
- * ws: dspark_workspace_size(DSPARK_OP_TOPK, R, B, V_d, K) bytes, zero-filled before first use
- * (per-part survivor slots and per-row completion counters; left zero-filled by every call).
+ * ws: dspark_workspace_size(DSPARK_OP_TOPK, R, B, V_d, K) bytes (per-part survivor slots).
  */
 dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
                           int64_t V_d, int64_t ld, const int64_t* row_start, int32_t K,
