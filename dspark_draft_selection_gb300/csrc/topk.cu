@@ -175,10 +175,10 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
   constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
   extern __shared__ __align__(128) uint8_t tk_dyn[];      // TK_STAGES x TK_STAGE_VEC x 16 bytes
   __shared__ uint64_t s_full[TK_STAGES];
-  __shared__ uint64_t s_keys[TK_MERGE_CAP];
+  __shared__ uint64_t s_keysbuf[2][TK_PART_CAP];
   __shared__ uint32_t s_red[TK_WARPS];
   __shared__ float s_wthr[TK_WARPS];
-  __shared__ uint32_t s_n;
+  __shared__ uint32_t s_nbuf[2];
   __shared__ uint16_t s_queue[TK_WARPS][TK_QCAP];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -223,6 +223,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
     const int64_t v0 = int64_t(p) * a.nvp, v1 = min(g.nvec, v0 + a.nvp);
     const int nv = v1 > v0 ? int(v1 - v0) : 0;
     const uint4* sv = stages + size_t(s) * TK_STAGE_VEC;
+    uint64_t* s_keys = s_keysbuf[n & 1];   // warp 0 may still be finishing the previous part's buffer
+    uint32_t& s_n = s_nbuf[n & 1];
 
     // scalar head (first part) and tail (last part) elements, loaded directly
     int64_t iextra = -1;
@@ -353,14 +355,35 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
         __syncthreads();
       }
     }
-    const uint32_t ns = s_n;
-    const int64_t part = int64_t(row_id) * P + p;
-    for (uint32_t i = tid; i < min(ns, uint32_t(TK_PART_CAP)); i += TK_THREADS) a.ws_keys[part * TK_PART_CAP + i] = s_keys[i];
-    if (tid == 0) {
-      a.ws_cnt[part] = ns;
-      a.ws_thr[part] = thr;
+    // warp 0 keeps only the survivors at or above the part's exact K'-th largest value (the part's
+    // K' best are all survivors), so the merge sees about K' keys per part; the other warps go on
+    // to the next part meanwhile
+    if (warp == 0) {
+      const uint32_t ns = min(s_n, uint32_t(TK_PART_CAP));
+      uint32_t vres = 0;
+      const int blo = PACKED ? 16 : 0;
+      for (int b = 31; b >= blo; --b) {
+        const uint32_t cand = vres | (1u << b);
+        uint32_t c = 0;
+        for (uint32_t i = lane; i < ns; i += 32) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
+        if (__reduce_add_sync(0xFFFFFFFFu, c) >= uint32_t(a.Kp)) vres = cand;
+      }
+      if (s_n > uint32_t(TK_PART_CAP)) vres = 0;     // overflowed ties: keep the slot as collected
+      const int64_t part = int64_t(row_id) * P + p;
+      uint32_t out = 0;
+      for (uint32_t i0 = 0; i0 < ns; i0 += 32) {
+        const uint32_t i = i0 + lane;
+        const uint64_t k = (i < ns) ? s_keys[i] : 0;
+        const bool keep = (i < ns) && uint32_t(k >> 32) >= vres;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+        if (keep) a.ws_keys[part * TK_PART_CAP + out + __popc(bal & below)] = k;
+        out += __popc(bal);
+      }
+      if (lane == 0) {
+        a.ws_cnt[part] = (s_n > uint32_t(TK_PART_CAP)) ? s_n : out;
+        a.ws_thr[part] = (vres && s_n <= uint32_t(TK_PART_CAP)) ? fmaxf(thr, ds_key32_to_float(vres)) : thr;
+      }
     }
-    __syncthreads();
   }
 }
 
