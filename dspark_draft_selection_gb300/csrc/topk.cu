@@ -20,9 +20,9 @@
 //     survivor masks with packed bf16x2 compares and drains them together (one survivor per lane
 //     per pass, one shared-memory atomic per pass), reading values back from shared memory.
 //  3. Survivors go, as 64-bit (value, lower index first) keys, to a per-part workspace slot.
-//  4. A second kernel merges each row (one CTA per row): max_p T_p bounds the row's K'-th value,
-//     a bisection over the surviving values finds the exact K'-th value, and a short bitonic sort
-//     orders the keys at or above it. A part whose survivors overflow its slot first tightens T_p
+//  4. A second kernel merges each row (one CTA per row): max_p T_p bounds the row's K'-th value;
+//     the m-th largest per-thread maximum of the keys above it per warp tightens the bound; each
+//     key left (about 2K') is ranked by counting the keys above it and written to its slot. A part whose survivors overflow its slot first tightens T_p
 //     to its own exact K'-th value; ties that still overflow send the row to an exact bisection
 //     over the row itself (slow, rare). No CTA waits for another and the workspace keeps no state.
 #include <type_traits>
@@ -38,6 +38,7 @@ constexpr int TK_STAGES = 2;
 constexpr int TK_STAGE_VEC = 2688;      // 16-byte vectors per stage (42 KB)
 constexpr int TK_PART_CAP = 512;        // survivor keys kept per part
 constexpr int TK_MERGE_CAP = 2048;      // keys gathered by the merging CTA
+constexpr int TK_SEL_CAP = 512;         // keys ranked by the merging CTA
 constexpr int TK_ROUNDS = (TK_STAGE_VEC + TK_THREADS - 1) / TK_THREADS;   // vectors per lane per part
 constexpr int TK_QCAP = 32 * TK_ROUNDS;  // per-warp queue of candidate vectors
 static_assert(TK_PART_CAP <= TK_MERGE_CAP, "part survivors are staged in the merge buffer");
@@ -175,10 +176,10 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
   constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
   extern __shared__ __align__(128) uint8_t tk_dyn[];      // TK_STAGES x TK_STAGE_VEC x 16 bytes
   __shared__ uint64_t s_full[TK_STAGES];
-  __shared__ uint64_t s_keysbuf[2][TK_PART_CAP];
+  __shared__ uint64_t s_keys[TK_MERGE_CAP];
   __shared__ uint32_t s_red[TK_WARPS];
   __shared__ float s_wthr[TK_WARPS];
-  __shared__ uint32_t s_nbuf[2];
+  __shared__ uint32_t s_n;
   __shared__ uint16_t s_queue[TK_WARPS][TK_QCAP];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -223,8 +224,6 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
     const int64_t v0 = int64_t(p) * a.nvp, v1 = min(g.nvec, v0 + a.nvp);
     const int nv = v1 > v0 ? int(v1 - v0) : 0;
     const uint4* sv = stages + size_t(s) * TK_STAGE_VEC;
-    uint64_t* s_keys = s_keysbuf[n & 1];   // warp 0 may still be finishing the previous part's buffer
-    uint32_t& s_n = s_nbuf[n & 1];
 
     // scalar head (first part) and tail (last part) elements, loaded directly
     int64_t iextra = -1;
@@ -355,36 +354,32 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_stream_kernel(const TopkAr
         __syncthreads();
       }
     }
-    // warp 0 keeps only the survivors at or above the part's exact K'-th largest value (the part's
-    // K' best are all survivors), so the merge sees about K' keys per part; the other warps go on
-    // to the next part meanwhile
-    if (warp == 0) {
-      const uint32_t ns = min(s_n, uint32_t(TK_PART_CAP));
-      uint32_t vres = 0;
-      const int blo = PACKED ? 16 : 0;
-      for (int b = 31; b >= blo; --b) {
-        const uint32_t cand = vres | (1u << b);
-        uint32_t c = 0;
-        for (uint32_t i = lane; i < ns; i += 32) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
-        if (__reduce_add_sync(0xFFFFFFFFu, c) >= uint32_t(a.Kp)) vres = cand;
-      }
-      if (s_n > uint32_t(TK_PART_CAP)) vres = 0;     // overflowed ties: keep the slot as collected
-      const int64_t part = int64_t(row_id) * P + p;
-      uint32_t out = 0;
-      for (uint32_t i0 = 0; i0 < ns; i0 += 32) {
-        const uint32_t i = i0 + lane;
-        const uint64_t k = (i < ns) ? s_keys[i] : 0;
-        const bool keep = (i < ns) && uint32_t(k >> 32) >= vres;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-        if (keep) a.ws_keys[part * TK_PART_CAP + out + __popc(bal & below)] = k;
-        out += __popc(bal);
-      }
-      if (lane == 0) {
-        a.ws_cnt[part] = (s_n > uint32_t(TK_PART_CAP)) ? s_n : out;
-        a.ws_thr[part] = (vres && s_n <= uint32_t(TK_PART_CAP)) ? fmaxf(thr, ds_key32_to_float(vres)) : thr;
-      }
+    const uint32_t ns = s_n;
+    const int64_t part = int64_t(row_id) * P + p;
+    for (uint32_t i = tid; i < min(ns, uint32_t(TK_PART_CAP)); i += TK_THREADS) a.ws_keys[part * TK_PART_CAP + i] = s_keys[i];
+    if (tid == 0) {
+      a.ws_cnt[part] = ns;
+      a.ws_thr[part] = thr;
+    }
+    __syncthreads();
+  }
+}
+
+// Writes candidate `rank` of a row: draft index, target id (d2t, range-checked) and value.
+DS_DEV void tk_emit(const TopkArgs& a, uint32_t row_id, int rank, uint64_t k64) {
+  const int64_t o = int64_t(row_id) * a.Kp + rank;
+  const uint32_t idx = ds_key64_idx(k64);
+  int64_t tgt = idx;
+  if (a.d2t) {
+    tgt = int64_t(idx) + a.d2t[idx];
+    if (tgt < 0 || tgt >= a.V_t) {
+      ds_set_error(a.status, DSPARK_ERANGE);
+      tgt = -1;
     }
   }
+  a.cand_draft[o] = int32_t(idx);
+  a.cand_tgt[o] = int32_t(tgt);
+  a.cand_val[o] = ds_key64_val(k64);
 }
 
 // One CTA per row merges the row's part survivors: max_p T_p bounds the row's K'-th value, a
@@ -394,9 +389,11 @@ template <typename T, bool XFORM>
 __global__ void __launch_bounds__(TK_THREADS) topk_merge_kernel(const TopkArgs a) {
   constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
   __shared__ uint64_t s_keys[TK_MERGE_CAP];
+  __shared__ uint64_t s_sel[TK_SEL_CAP];
+  __shared__ unsigned long long s_wkey[TK_WARPS];
   __shared__ uint32_t s_red[2][TK_WARPS];
   __shared__ uint32_t s_off[65];
-  __shared__ uint32_t s_n;
+  __shared__ uint32_t s_n, s_n2;
   __shared__ int s_bad;
   __shared__ float s_rthr;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -432,74 +429,79 @@ __global__ void __launch_bounds__(TK_THREADS) topk_merge_kernel(const TopkArgs a
     }
   }
   __syncthreads();
-  const uint32_t ngot = s_n;
+  const uint32_t ngot = min(s_n, uint32_t(TK_MERGE_CAP));
   const TkRow g = tk_row<T>(a, row_id);
   const T* row = reinterpret_cast<const T*>(g.row);
-  int nk;
-  if (!s_bad && ngot <= uint32_t(TK_MERGE_CAP)) {
-    // exact K'-th largest value among them, by bisection on the value key (bf16 values without a
-    // transform carry no order in the low 16 key bits, so the bisection stops after the top 16);
-    // one barrier per step, alternating the partial-count slots
-    uint32_t vres = 0;
-    const int blo = PACKED ? 16 : 0;
-    int ph = 0;
-    for (int b = 31; b >= blo; --b, ph ^= 1) {
-      const uint32_t cand = vres | (1u << b);
-      uint32_t c = 0;
-      for (uint32_t i = tid; i < ngot; i += TK_THREADS) c += (uint32_t(s_keys[i] >> 32) >= cand) ? 1u : 0u;
-      c = __reduce_add_sync(0xFFFFFFFFu, c);
-      if (lane == 0) s_red[ph][warp] = c;
-      __syncthreads();
-      uint32_t tot = 0;
+  // a tighter row bound: the m-th largest per-thread maximum of the gathered keys in every warp
+  // (m = ceil(K'/8)); 8 warps x m distinct keys are >= its minimum over the warps
+  uint64_t mx = 0;
+  for (uint32_t i = tid; i < ngot; i += TK_THREADS) mx = max(mx, (unsigned long long)s_keys[i]);
+  {
+    const int m = (a.Kp + TK_WARPS - 1) / TK_WARPS;
+    unsigned long long key = mx, kth = 0;
 #pragma unroll
-      for (int w = 0; w < TK_WARPS; ++w) tot += s_red[ph][w];
-      if (tot >= uint32_t(a.Kp)) vres = cand;
+    for (int t = 0; t < (64 + TK_WARPS - 1) / TK_WARPS; ++t) {
+      if (t < m) {
+        kth = __reduce_max_sync(0xFFFFFFFFu, uint32_t(key >> 32)) == uint32_t(key >> 32) ? key : 0ull;
+        kth = ds_warp_max_u64(kth);   // the largest full key among the lanes holding the top value
+        const unsigned who = __ballot_sync(0xFFFFFFFFu, key == kth);
+        if (lane == __ffs(who) - 1) key = 0;
+      }
     }
-    // compact the keys at or above it to the front, a block-wide pass at a time
-    if (tid == 0) s_n = 0;
+    if (lane == 0) s_wkey[warp] = kth;
+  }
+  __syncthreads();
+  unsigned long long bound = s_wkey[0];
+#pragma unroll
+  for (int w = 1; w < TK_WARPS; ++w) bound = min(bound, s_wkey[w]);
+  // compact the keys >= bound (ballot per warp, one barrier), then each key's rank is the number
+  // of compacted keys above it: rank < K' goes straight to its output slot
+  uint32_t nsel = 0;
+  if (!s_bad && s_n <= uint32_t(TK_MERGE_CAP)) {
+    if (tid == 0) s_n2 = 0;
     __syncthreads();
     for (uint32_t i0 = 0; i0 < ngot; i0 += TK_THREADS) {
       const uint32_t i = i0 + tid;
       const uint64_t k = (i < ngot) ? s_keys[i] : 0;
-      const bool keep = (i < ngot) && uint32_t(k >> 32) >= vres;
-      __syncthreads();
-      if (keep) s_keys[atomicAdd(&s_n, 1u)] = k;
-      __syncthreads();
+      const bool keep = (i < ngot) && k >= bound;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+      uint32_t base = 0;
+      if (lane == 0 && bal) base = atomicAdd(&s_n2, uint32_t(__popc(bal)));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (keep && base + __popc(bal & ((1u << lane) - 1u)) < uint32_t(TK_SEL_CAP))
+        s_sel[base + __popc(bal & ((1u << lane) - 1u))] = k;
     }
-    nk = int(s_n);
-  } else {
-    nk = tk_row_exact<T, XFORM>(a, row, s_keys, s_red[0], &s_n);
+    __syncthreads();
+    nsel = s_n2;
   }
-  int n2 = 1;
-  while (n2 < nk) n2 <<= 1;
-  for (int i = nk + tid; i < n2; i += TK_THREADS) s_keys[i] = 0;
-  __syncthreads();
-  ds_block_sort_desc(s_keys, n2);
-  if (tid < a.Kp) {
-    const int64_t o = int64_t(row_id) * a.Kp + tid;
-    if (tid >= nk) {                              // unreachable: >= K' keys always reach the sort
-      ds_set_error(a.status, DSPARK_EINVAL);
-      a.cand_draft[o] = -1;
-      a.cand_tgt[o] = -1;
-      a.cand_val[o] = -INFINITY;
-    } else {
-      const uint64_t k64 = s_keys[tid];
-      const uint32_t idx = ds_key64_idx(k64);
-      int64_t tgt = idx;
-      if (a.d2t) {
-        tgt = int64_t(idx) + a.d2t[idx];
-        if (tgt < 0 || tgt >= a.V_t) {
-          ds_set_error(a.status, DSPARK_ERANGE);
-          tgt = -1;
-        }
+  if (!s_bad && s_n <= uint32_t(TK_MERGE_CAP) && nsel <= uint32_t(TK_SEL_CAP)) {
+    for (uint32_t i = tid; i < nsel; i += TK_THREADS) {
+      const uint64_t k = s_sel[i];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < nsel; ++j) rank += (s_sel[j] > k) ? 1u : 0u;
+      if (rank < uint32_t(a.Kp)) tk_emit(a, row_id, int(rank), k);
+    }
+  } else {
+    // ties flooded the buffers: exact selection over the row itself, then sort
+    const int nk = tk_row_exact<T, XFORM>(a, row, s_keys, s_red[0], &s_n);
+    int n2 = 1;
+    while (n2 < nk) n2 <<= 1;
+    for (int i = nk + tid; i < n2; i += TK_THREADS) s_keys[i] = 0;
+    __syncthreads();
+    ds_block_sort_desc(s_keys, n2);
+    if (tid < a.Kp) {
+      if (tid >= nk) {                              // unreachable: >= K' keys always reach the sort
+        ds_set_error(a.status, DSPARK_EINVAL);
+        const int64_t o = int64_t(row_id) * a.Kp + tid;
+        a.cand_draft[o] = -1;
+        a.cand_tgt[o] = -1;
+        a.cand_val[o] = -INFINITY;
+      } else {
+        tk_emit(a, row_id, tid, s_keys[tid]);
       }
-      a.cand_draft[o] = int32_t(idx);
-      a.cand_tgt[o] = int32_t(tgt);
-      a.cand_val[o] = ds_key64_val(k64);
     }
   }
 }
-
 
 size_t tk_align(size_t x) { return (x + 255) & ~size_t(255); }
 
