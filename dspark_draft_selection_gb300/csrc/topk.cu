@@ -382,9 +382,9 @@ DS_DEV void tk_emit(const TopkArgs& a, uint32_t row_id, int rank, uint64_t k64) 
   a.cand_val[o] = ds_key64_val(k64);
 }
 
-// One CTA per row merges the row's part survivors: max_p T_p bounds the row's K'-th value, a
-// bisection over the surviving values finds the exact K'-th value, and a short bitonic sort orders
-// the keys at or above it.
+// One CTA per row merges the row's part survivors: max_p T_p bounds the row's K'-th value, the
+// per-warp m-th largest thread maximum of the keys above it tightens the bound, and each key left
+// is ranked by counting the keys above it.
 template <typename T, bool XFORM>
 __global__ void __launch_bounds__(TK_THREADS) topk_merge_kernel(const TopkArgs a) {
   constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_merge_kernel(const TopkArgs a
   const T* row = reinterpret_cast<const T*>(g.row);
   // a tighter row bound: the m-th largest per-thread maximum of the gathered keys in every warp
   // (m = ceil(K'/8)); 8 warps x m distinct keys are >= its minimum over the warps
-  uint64_t mx = 0;
+  unsigned long long mx = 0;
   for (uint32_t i = tid; i < ngot; i += TK_THREADS) mx = max(mx, (unsigned long long)s_keys[i]);
   {
     const int m = (a.Kp + TK_WARPS - 1) / TK_WARPS;
