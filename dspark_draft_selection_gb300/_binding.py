@@ -29,7 +29,7 @@ SIGNATURES = [
     ("dspark_status_string", ctypes.c_char_p, [c_i32]),
     ("dspark_d2t_check", c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_sz, c_vp, c_vp]),
     ("dspark_topk", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_i32, c_f32, c_f32, c_vp, c_i64,
-                            c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                            c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_lattice_score", c_i32, [c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
                                      c_i32, c_i32, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_vp, c_vp, c_vp,
@@ -145,20 +145,8 @@ def dspark_d2t_check(d2t, V_t, require_injective=True, status=None, ws=None, str
     return status
 
 
-_topk_ws = {}
-
-
-def topk_workspace(R, B, V, device="cuda"):
-    """A Top-K workspace, cached per size."""
-    n = int(lib().dspark_workspace_size(OP_TOPK, R, B, V, 0))
-    key = (str(device), n)
-    if key not in _topk_ws:
-        _topk_ws[key] = torch.zeros(n + 256, dtype=torch.uint8, device=device)
-    return _topk_ws[key]
-
-
 def dspark_topk(logits, B, K, *, R=None, V_d=None, row_start=None, mult=1.0, softcap=0.0, d2t=None, V_t=None,
-                out=None, ws=None, status=None, stream=None):
+                out=None, status=None, stream=None):
     rows, ld = _rows(logits)
     V_d = logits.shape[1] if V_d is None else V_d
     R = rows // B if R is None else R
@@ -170,10 +158,8 @@ def dspark_topk(logits, B, K, *, R=None, V_d=None, row_start=None, mult=1.0, sof
                torch.empty((R, B, Kp), dtype=torch.float32, device=dev))
     status = new_status(dev) if status is None else status
     V_t = (V_d if d2t is None else V_t) if V_t is None else V_t
-    ws = topk_workspace(R, B, V_d, dev) if ws is None else ws
-    wp, wn = _ws(ws)
     _check(lib().dspark_topk(_p(logits), _dt(logits), R, B, V_d, ld, _p(row_start), K, mult, softcap, _p(d2t), V_t,
-                             _p(out[0]), _p(out[1]), _p(out[2]), wp, wn, _p(status), _stream(stream)), "dspark_topk")
+                             _p(out[0]), _p(out[1]), _p(out[2]), _p(status), _stream(stream)), "dspark_topk")
     return out + (status,)
 
 

@@ -3,7 +3,6 @@
 #include "host_common.h"
 
 // Per-op workspace layouts are defined next to their kernels; these sizes must cover them.
-extern "C" size_t dspark_internal_ws_topk(int64_t R, int32_t B, int64_t V);
 extern "C" size_t dspark_internal_ws_sample(int64_t R, int32_t B, int64_t V);
 extern "C" size_t dspark_internal_ws_dense_walk(int64_t R, int32_t B, int64_t V);
 extern "C" size_t dspark_internal_ws_verify(int64_t R, int32_t B, int64_t V);
@@ -15,7 +14,7 @@ extern "C" size_t dspark_workspace_size(dspark_op op, int64_t R, int32_t B, int6
     case DSPARK_OP_D2T_CHECK:
       return size_t(ds_ceil_div(V, 32)) * sizeof(uint32_t) + 256;
     case DSPARK_OP_TOPK:
-      return dspark_internal_ws_topk(R, B, V);
+      return 0;
     case DSPARK_OP_SAMPLE:
       return dspark_internal_ws_sample(R, B, V);
     case DSPARK_OP_DENSE_WALK:

@@ -140,13 +140,13 @@ dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64_t V_t,
  *   cand_draft [R, B, K'] int32 draft index, cand_tgt [R, B, K'] int32 target id (-1 and
  *   DSPARK_ERANGE on *dev_status when a chosen index maps outside [0, V_t)), cand_val
  *   [R, B, K'] float32 s.
- * ws: dspark_workspace_size(DSPARK_OP_TOPK, R, B, V_d, K) bytes (per-part survivor slots).
+ * Needs no workspace: each row is selected by one thread block streaming it once.
  */
 dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
                           int64_t V_d, int64_t ld, const int64_t* row_start, int32_t K,
                           float mult, float softcap, const int64_t* d2t, int64_t V_t,
-                          int32_t* cand_draft, int32_t* cand_tgt, float* cand_val, void* ws,
-                          size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream);
+                          int32_t* cand_draft, int32_t* cand_tgt, float* cand_val,
+                          int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * Markov-head transition lattice [G: Change > Markov heads - the scorer rates the K best

@@ -54,12 +54,14 @@ def test_status_strings_and_host_checks(libpath):
     assert ds.dspark_status_string(0) == "ok"
     assert "range" in ds.dspark_status_string(2)
     # null pointers and bad sizes are refused on the host, before any launch
-    assert lib.dspark_topk(None, 0, 1, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, None, None, None, None, 0, None, None) == 1
+    assert lib.dspark_topk(None, 0, 1, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, None, None, None, None, None) == 1
     fake = ctypes.c_void_p(256)
-    assert lib.dspark_topk(fake, 0, 1, 1, 10, 10, None, 65, 1.0, 0.0, None, 10, fake, fake, fake, None, 0, fake, None) == 1
-    assert lib.dspark_topk(fake, 7, 1, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, None, 0, fake, None) == 1
-    # a missing Top-K workspace is refused before any launch
-    assert lib.dspark_topk(fake, 0, 1, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, None, 0, fake, None) == 8
+    assert lib.dspark_topk(fake, 0, 1, 1, 10, 10, None, 65, 1.0, 0.0, None, 10, fake, fake, fake, fake, None) == 1
+    assert lib.dspark_topk(fake, 7, 1, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, fake, None) == 1
+    assert lib.dspark_topk(fake, 0, 1, 1, 10, 9, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, fake, None) == 1  # ld < V_d
+    # an empty batch is a no-op that launches nothing
+    assert lib.dspark_topk(fake, 0, 0, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, fake, None) == 0
+    assert ds.dspark_workspace_size(ds.OP_TOPK, 32, 7, 151936, 64) == 0
     assert lib.dspark_chain_select(fake, fake, fake, 1, 7, 65, 0, 0.0, 1.0, None, None, fake, fake, fake, None,
                                    fake, None) == 1
     assert lib.dspark_d2t_check(fake, 10, 10, 1, None, 0, fake, None) == 8      # injectivity needs a workspace

@@ -130,3 +130,67 @@ def test_full_size_configs(cfg):
     nrows = s.shape[0]
     rows = range(nrows) if nrows <= 256 else np.random.default_rng(cfg).choice(nrows, 48, replace=False)
     assert_same(got, oracle_topk(s, w["K"], d2t=w["d2t"], rows=rows), rows=rows)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 400000), ("f32", 200000)])
+def test_long_rows(dtype, V):
+    # many chunks per row: the running top-K' list carries across 19 and 38 chunks
+    w = di.lattice_workload(25, R=1, B=3, V_d=V, K=64, rank=8, dtype=dtype, peak=8.0)
+    got = run_topk(w["logits"], 3, 64)
+    assert got[3] == 0
+    assert_same(got, oracle_topk(as_f32(w["logits"]), 64))
+
+
+def test_long_rows_with_ties_and_constant_rows():
+    rng = np.random.default_rng(6)
+    V = 400000
+    s = np.round(rng.standard_normal((4, V)) * 2).astype(np.float32)
+    s[1] = 3.0
+    s[2] = -np.inf
+    bits = di.f32_to_bf16_bits(s)
+    got = run_topk(bits, 4, 64)
+    assert got[3] == 0
+    assert_same(got, oracle_topk(as_f32(bits), 64))
+
+
+def test_many_rows_per_block_with_flooded_rows():
+    # a batch of the Qwen3-4B shape, more rows than resident blocks; some rows flood the survivor
+    # buffer of their first chunk (constant, all -inf, few distinct values) and take the exact cut
+    w = di.lattice_workload(26, R=32, B=7, V_d=151936, K=64, rank=8, peak=8.0)
+    s = as_f32(w["logits"]).copy()
+    rng = np.random.default_rng(7)
+    s[5] = 1.5
+    s[77] = -np.inf
+    s[150] = np.round(s[150] / 8)
+    s[223, rng.random(151936) < 0.5] = -0.0
+    bits = di.f32_to_bf16_bits(s)
+    got = run_topk(bits, 7, 64)
+    assert got[3] == 0
+    rows = [0, 5, 6, 77, 78, 113, 150, 151, 200, 223]
+    assert_same(got, oracle_topk(as_f32(bits), 64, rows=rows), rows=rows)
+
+
+def test_small_k_and_single_part_rows_in_bulk():
+    w = di.lattice_workload(27, R=200, B=3, V_d=4099, K=3, rank=8)
+    got = run_topk(w["logits"], 3, 3)
+    assert got[3] == 0
+    rows = list(range(0, 600, 37)) + [599]
+    assert_same(got, oracle_topk(as_f32(w["logits"]), 3, rows=rows), rows=rows)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rising_falling_and_late_peak_rows(dtype):
+    # a rising row: every later chunk beats the running K'-th value everywhere (exact cut each
+    # chunk); a falling row: nothing after the first chunk enters; the peak in the scalar tail
+    V = 100003
+    s = np.zeros((4, V), dtype=np.float32)
+    s[0] = np.arange(V, dtype=np.float32) / 64.0
+    s[1] = -np.arange(V, dtype=np.float32) / 64.0
+    s[2] = di.normal(di.generator(28, 0), (1, V), 2.0, "f32")[0]
+    s[2, V - 1] = 50.0
+    s[2, V - 2] = 49.0
+    s[3] = np.round(s[0] / 512.0)                                      # rising with long runs of ties
+    data = s if dtype == "f32" else di.f32_to_bf16_bits(s)
+    got = run_topk(data, 4, 64)
+    assert got[3] == 0
+    assert_same(got, oracle_topk(as_f32(data), 64))
