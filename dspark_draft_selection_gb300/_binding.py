@@ -28,6 +28,7 @@ SIGNATURES = [
     ("dspark_workspace_size", c_sz, [c_i32, c_i64, c_i32, c_i64, c_i32]),
     ("dspark_status_string", ctypes.c_char_p, [c_i32]),
     ("dspark_d2t_check", c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_sz, c_vp, c_vp]),
+    ("dspark_d2t_check_noalloc", c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp]),
     ("dspark_topk", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_i32, c_f32, c_f32, c_vp, c_i64,
                             c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_lattice_score", c_i32, [c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
@@ -142,6 +143,14 @@ def dspark_d2t_check(d2t, V_t, require_injective=True, status=None, ws=None, str
     wp, wn = _ws(ws)
     _check(lib().dspark_d2t_check(_p(d2t), d2t.numel(), V_t, int(require_injective), wp, wn, _p(status),
                                   _stream(stream)), "dspark_d2t_check")
+    return status
+
+
+def dspark_d2t_check_noalloc(d2t, V_t, require_injective=True, status=None, stream=None):
+    """dspark_d2t_check without a workspace (the library's static bitmap; V_t <= 2**20)."""
+    status = new_status(d2t.device) if status is None else status
+    _check(lib().dspark_d2t_check_noalloc(_p(d2t), d2t.numel(), V_t, int(require_injective), _p(status),
+                                          _stream(stream)), "dspark_d2t_check_noalloc")
     return status
 
 

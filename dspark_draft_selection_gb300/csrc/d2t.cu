@@ -10,6 +10,8 @@
 // Two passes so that a range error always wins over a duplicate: the range pass, then (only if
 // the status word is still clear) a pass that sets one bit per target id in a workspace bitmap
 // and reports an id whose bit was already set.
+#include <mutex>
+
 #include "dspark_common.cuh"
 #include "host_common.h"
 
@@ -47,6 +49,59 @@ extern "C" dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64
   if (require_injective) {
     DS_CUDA_TRY(cudaMemsetAsync(ws, 0, need, stream));
     d2t_dup_kernel<<<blocks, threads, 0, stream>>>(d2t, V_d, reinterpret_cast<uint32_t*>(ws), dev_status);
+  }
+  return ds_launch_status();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free variant. Some callers cannot hand the library a device workspace: runtimes that
+// allocate nothing once serving has started, or hosts whose device memory belongs to another
+// allocator. For them the duplicate bitmap is a static array in this library's device image,
+// sized for target vocabularies of up to D2T_NOALLOC_MAX_VT ids (128 KB). Its address is looked
+// up once per device, with that device current, on the first call made there. The bitmap is
+// cleared on the caller's stream at every call; calls that overlap on the GPU share it and race.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t D2T_NOALLOC_MAX_VT = int64_t(1) << 20;
+constexpr int D2T_NOALLOC_MAX_DEVICES = 64;
+
+__device__ __align__(256) uint32_t d2t_noalloc_bitmap[D2T_NOALLOC_MAX_VT / 32];
+
+std::mutex d2t_noalloc_mu;
+uint32_t* d2t_noalloc_addr[D2T_NOALLOC_MAX_DEVICES] = {};
+
+// The bitmap's address on the current device (set-up on the first call there), or nullptr.
+uint32_t* d2t_noalloc_bitmap_ptr() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= D2T_NOALLOC_MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(d2t_noalloc_mu);
+  if (d2t_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, d2t_noalloc_bitmap) != cudaSuccess || ptr == nullptr) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    d2t_noalloc_addr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  return d2t_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_d2t_check_noalloc(const int64_t* d2t, int64_t V_d, int64_t V_t,
+                                                  int32_t require_injective, int32_t* dev_status,
+                                                  dspark_stream_t stream) {
+  DS_REQUIRE(d2t && dev_status && V_d >= 1 && V_t >= 1);
+  if (V_t > D2T_NOALLOC_MAX_VT) return DSPARK_EINVAL;
+  uint32_t* bitmap = d2t_noalloc_bitmap_ptr();
+  if (bitmap == nullptr) return DSPARK_ECUDA;
+  const int threads = 256;
+  const unsigned blocks = unsigned(std::min<int64_t>(ds_ceil_div(V_d, threads), int64_t(ds_num_sms()) * 8));
+  d2t_range_kernel<<<blocks, threads, 0, stream>>>(d2t, V_d, V_t, dev_status);
+  if (require_injective) {
+    DS_CUDA_TRY(cudaMemsetAsync(bitmap, 0, size_t(ds_ceil_div(V_t, 32)) * sizeof(uint32_t), stream));
+    d2t_dup_kernel<<<blocks, threads, 0, stream>>>(d2t, V_d, bitmap, dev_status);
   }
   return ds_launch_status();
 }

@@ -130,6 +130,22 @@ dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64_t V_t,
                                int32_t* dev_status, dspark_stream_t stream);
 
 /*
+ * d2t validation that allocates nothing: the same checks and verdicts as dspark_d2t_check, for
+ * callers that cannot provide a device workspace (runtimes that allocate nothing once serving
+ * has started, or hosts whose device memory is owned by another allocator). The pages have no
+ * counterpart: this is a library convenience, not part of the method.
+ * The duplicate bitmap is a static 128 KB array in the library's device image, so V_t is
+ * limited to 1,048,576 target ids; a larger V_t returns DSPARK_EINVAL before any launch.
+ * The first call on a device (with that device current) looks up the array's address; make
+ * that first call before any stream capture. Every call clears the bitmap on `stream` before
+ * use. Calls that overlap on the GPU share the bitmap and race: serialise them (one stream, or
+ * events). d2t: device pointer to V_d int64 offsets; *dev_status as for dspark_d2t_check.
+ */
+dspark_status dspark_d2t_check_noalloc(const int64_t* d2t, int64_t V_d, int64_t V_t,
+                                       int32_t require_injective, int32_t* dev_status,
+                                       dspark_stream_t stream);
+
+/*
  * Row transform + Top-K + d2t map [G: Change > Markov heads, Top-K candidate scorer;
  * block-sampler commit - rows are backbone logits times the output multiplier, then
  * soft-capped; P: top_k = min(64, draft_vocab_size), target id i + d2t[i]].
