@@ -20,6 +20,7 @@ namespace {
 constexpr int CH_THREADS = 256;
 constexpr int CH_MAXK = 64;
 constexpr int CH_MAXB = 128;
+constexpr int CH_MAXNS = 16;          // tiles requested together (batch path)
 
 struct ChainArgs {
   const float* u;
@@ -37,6 +38,7 @@ struct ChainArgs {
   int32_t* q_n;
   int32_t q_cap;
   int32_t* status;
+  int32_t ns;                         // tiles per batch (batch path)
 };
 
 // cp.async one position's K x K tile (K*K floats; K*K*4 is a multiple of 16 when K % 2 == 0,
@@ -46,6 +48,11 @@ DS_DEV void ch_load_tile(float* dst, const float* src, int n) {
   for (int i = threadIdx.x; i < nvec; i += CH_THREADS) ds_cp_async16(dst + 4 * i, src + 4 * i);
   for (int i = 4 * nvec + threadIdx.x; i < n; i += CH_THREADS) dst[i] = src[i];
   asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// cp.async of one tile (K*K floats, 16-byte aligned, K*K % 4 == 0) without committing the group
+DS_DEV void ch_issue_tile(float* dst, const float* src, int n) {
+  for (int i = threadIdx.x; i < n / 4; i += CH_THREADS) ds_cp_async16(dst + 4 * i, src + 4 * i);
 }
 
 DS_DEV void ch_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
@@ -62,8 +69,11 @@ DS_DEV double ch_warp_scan(double v) {
   return v;
 }
 
+template <bool RING>
 __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
-  extern __shared__ __align__(16) float ch_dyn[];      // [2][K*K] tiles, then [B*K] unary scores
+  // RING: batches of NS [K*K] tiles, each batch requested at once, else [2][K*K] double-buffered;
+  // then [B*K] unary scores
+  extern __shared__ __align__(128) float ch_dyn[];
   __shared__ float s_delta[CH_MAXK];
   __shared__ float s_bv[4][CH_MAXK];
   __shared__ int s_ba[4][CH_MAXK];
@@ -73,13 +83,38 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 
   const int r = blockIdx.x, K = a.K, B = a.B, t = threadIdx.x;
   const int KK = K * K;
+  const int KKp = (KK + 3) & ~3;
+  const int NS = RING ? a.ns : 2;
   float* s_tile0 = ch_dyn;
-  float* s_tile1 = ch_dyn + ((KK + 3) & ~3);
-  float* s_u = s_tile1 + ((KK + 3) & ~3);
+  float* s_tile1 = ch_dyn + KKp;
+  float* s_u = ch_dyn + size_t(NS) * KKp;
   const float* u = a.u + int64_t(r) * B * K;
   const float* A = a.trans + int64_t(r) * B * KK;
-  for (int i = t; i < B * K; i += CH_THREADS) s_u[i] = u[i];
-  ch_load_tile(s_tile0, A, KK);
+  // the request's candidate ids (for the outputs) and unary scores come in with the first
+  // tiles, asynchronously, so no thread stalls on a load
+  int32_t* s_ct = reinterpret_cast<int32_t*>(s_u + ((B * K + 3) & ~3));
+  const int32_t* ctg = a.cand_tgt + int64_t(r) * B * K;
+  const bool uvec = ((B * K) & 3) == 0 && (reinterpret_cast<uintptr_t>(u) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(ctg) & 15) == 0;
+  if (uvec) {
+    for (int i = t; i < (B * K) / 4; i += CH_THREADS) {
+      ds_cp_async16(s_u + 4 * i, u + 4 * i);
+      ds_cp_async16(s_ct + 4 * i, ctg + 4 * i);
+    }
+  } else {
+    for (int i = t; i < B * K; i += CH_THREADS) {
+      s_u[i] = u[i];
+      s_ct[i] = ctg[i];
+    }
+  }
+  if (RING) {
+    // the first batch of tiles is requested at once by every thread: the lattice's latency is paid
+    // once per batch of NS positions instead of once per position
+    for (int i = 0; i < NS && i < B; ++i) ch_issue_tile(ch_dyn + size_t(i) * KKp, A + int64_t(i) * KK, KK);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  } else {
+    ch_load_tile(s_tile0, A, KK);                  // commits the ids and scores with tile 0
+  }
 
   const bool maxsum = a.mode == DSPARK_MAXSUM;
   const bool sample = (a.mode == DSPARK_SAMPLE) && (a.T > 0.0f);
@@ -89,14 +124,23 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
   double score = 0.0;
 
   for (int j = 0; j < B; ++j) {
-    if (j + 1 < B) {
-      ch_load_tile(((j + 1) & 1) ? s_tile1 : s_tile0, A + int64_t(j + 1) * KK, KK);
-      ch_wait_prev();
+    const float* Aj;
+    if (RING) {
+      if (j % NS == 0) {
+        ch_wait_all();
+        __syncthreads();
+      }
+      Aj = ch_dyn + size_t(j % NS) * KKp;
     } else {
-      ch_wait_all();
+      if (j + 1 < B) {
+        ch_load_tile(((j + 1) & 1) ? s_tile1 : s_tile0, A + int64_t(j + 1) * KK, KK);
+        ch_wait_prev();
+      } else {
+        ch_wait_all();
+      }
+      __syncthreads();
+      Aj = (j & 1) ? s_tile1 : s_tile0;
     }
-    __syncthreads();
-    const float* Aj = (j & 1) ? s_tile1 : s_tile0;
     const float* uj = s_u + j * K;
     if (maxsum) {
       if (j == 0) {
@@ -104,16 +148,20 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
       } else {
         const int b = t & 63, part = t >> 6;
         if (b < K) {
-          float best = -INFINITY;
-          int ba = -1;
-          const int a0 = part * 16, a1 = min(K, a0 + 16);
-          for (int aa = a0; aa < a1; ++aa) {
-            const float v = __fadd_rn(s_delta[aa], Aj[aa * K + b]);
-            if (v > best || ba < 0) {
-              best = v;
-              ba = aa;
+          // the 16 predecessors of this part: loads first (independent), then the running max
+          // (first maximum kept: lowest predecessor index among equal sums)
+          const int a0 = part * 16, na = min(K - a0, 16);
+          float v[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = (q < na) ? __fadd_rn(s_delta[a0 + q], Aj[(a0 + q) * K + b]) : -INFINITY;
+          float best = v[0];
+          int ba = (na > 0) ? a0 : -1;
+#pragma unroll
+          for (int q = 1; q < 16; ++q)
+            if (q < na && v[q] > best) {
+              best = v[q];
+              ba = a0 + q;
             }
-          }
           s_bv[part][b] = best;
           s_ba[part][b] = ba;
         }
@@ -150,7 +198,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         pick = int(ds_key64_idx(ds_warp_max_u64(k0 > k1 ? k0 : k1)));
         if (a.mode == DSPARK_SAMPLE && lane == 0 && a.q_n) {
           a.q_n[qrow] = 1;
-          a.q_ids[qrow * a.q_cap] = a.cand_tgt[qrow * K + pick];
+          a.q_ids[qrow * a.q_cap] = s_ct[j * K + pick];
           a.q_p[qrow * a.q_cap] = 1.0f;
         }
       } else {
@@ -243,14 +291,14 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           if (kept[0]) {
             const int o = __popc(m0 & below);
             if (o < a.q_cap) {
-              a.q_ids[qrow * a.q_cap + o] = a.cand_tgt[qrow * K + lane];
+              a.q_ids[qrow * a.q_cap + o] = s_ct[j * K + lane];
               a.q_p[qrow * a.q_cap + o] = float(double(w[0]) / wk);
             }
           }
           if (kept[1]) {
             const int o = n0 + __popc(m1 & below);
             if (o < a.q_cap) {
-              a.q_ids[qrow * a.q_cap + o] = a.cand_tgt[qrow * K + lane + 32];
+              a.q_ids[qrow * a.q_cap + o] = s_ct[j * K + lane + 32];
               a.q_p[qrow * a.q_cap + o] = float(double(w[1]) / wk);
             }
           }
@@ -261,25 +309,47 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
       score += double(vp);
       if (lane == 0) {
         a.chain_rank[r * B + j] = pick;
-        a.chain_tgt[r * B + j] = a.cand_tgt[(int64_t(r) * B + j) * K + pick];
+        a.chain_tgt[r * B + j] = s_ct[j * K + pick];
       }
       prevb = pick;
     }
     __syncthreads();
+    if (RING && j % NS == NS - 1 && j + 1 < B) {
+      // the batch is consumed: request the next one
+      for (int i = j + 1; i < j + 1 + NS && i < B; ++i)
+        ch_issue_tile(ch_dyn + size_t(i % NS) * KKp, A + int64_t(i) * KK, KK);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
   }
-  if (maxsum && t == 0) {
-    int bb = 0;
-    float best = s_delta[0];
-    for (int k = 1; k < K; ++k)
-      if (s_delta[k] > best) {
-        best = s_delta[k];
-        bb = k;
+  if (maxsum) {
+    // best final score (first maximum) by warp 0, then the backtrack by thread 0 into shared
+    // memory, then every position's outputs in parallel
+    __shared__ int s_path[CH_MAXB];
+    if (warp == 0) {
+      uint64_t kbest = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = lane + 32 * h;
+        if (k < K) {
+          const uint64_t kk = ds_key64(ds_canon_zero(s_delta[k]), uint32_t(k));
+          kbest = kk > kbest ? kk : kbest;
+        }
       }
-    a.score[r] = best;
-    for (int j = B - 1; j >= 0; --j) {
+      kbest = ds_warp_max_u64(kbest);
+      if (lane == 0) {
+        int bb = int(ds_key64_idx(kbest));
+        a.score[r] = s_delta[bb];
+        for (int j = B - 1; j >= 0; --j) {
+          s_path[j] = bb;
+          if (j > 0) bb = s_back[j][bb];
+        }
+      }
+    }
+    __syncthreads();
+    for (int j = t; j < B; j += CH_THREADS) {
+      const int bb = s_path[j];
       a.chain_rank[r * B + j] = bb;
-      a.chain_tgt[r * B + j] = a.cand_tgt[(int64_t(r) * B + j) * K + bb];
-      if (j > 0) bb = s_back[j][bb];
+      a.chain_tgt[r * B + j] = s_ct[j * K + bb];
     }
   }
   if (!maxsum && t == 0) a.score[r] = float(score);
@@ -325,12 +395,33 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
     }
   }
   if (R == 0) return DSPARK_OK;
-  const size_t smem = (2 * size_t((K * K + 3) & ~3) + size_t(B) * K) * sizeof(float);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-    configured = smem;
+  const size_t tile = size_t((K * K + 3) & ~3) * sizeof(float);
+  const size_t ubytes = 2 * size_t((B * K + 3) & ~3) * sizeof(float);   // scores + candidate ids
+  // the batch path copies 16-byte pieces: tiles 16-byte aligned, K*K a multiple of 4 (K even)
+  const bool ring = (K % 2 == 0) && ds_aligned(trans, 16);
+  constexpr size_t kBudget = 192 * 1024;                   // dynamic shared memory for tiles + scores
+  int ns = 2;
+  if (ring) {
+    ns = int(std::min<size_t>({size_t(B), size_t(CH_MAXNS), (kBudget - std::min(kBudget, ubytes)) / tile}));
+    if (ns < 1) ns = 1;
   }
-  chain_kernel<<<unsigned(R), CH_THREADS, smem, stream>>>(a);
+  a.ns = ns;
+  const size_t smem = size_t(ns) * tile + ubytes;
+  if (smem > kBudget + 16 * 1024) return DSPARK_EINVAL;
+  if (ring) {
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+      DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+      configured = smem;
+    }
+    chain_kernel<true><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
+  } else {
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+      DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+      configured = smem;
+    }
+    chain_kernel<false><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
+  }
   return ds_launch_status();
 }

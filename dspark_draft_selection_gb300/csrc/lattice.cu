@@ -146,24 +146,26 @@ __global__ void __launch_bounds__(LT_THREADS) lattice_tc_kernel(const LatticeArg
   }
   ok = __syncthreads_and(ok) != 0;                 // one verdict for the whole CTA
   ds_tc_fence_after();
-  // stage the K x K tile through shared memory (the operand buffers are free once the MMAs
-  // completed) so that the stores below are coalesced
-  float* stage = reinterpret_cast<float*>(base);     // [64][65] floats
+  // each thread owns accumulator row `arow` (TMEM lane): scale it by the gate and store it
+  // straight from registers (16-byte stores when the row is 16-byte aligned)
   if (ok) {
     float v[64];
     ds_tmem_ld_32x32b_x64(tmem + (uint32_t(warp * 32) << 16), v);
     const int arow = warp * 32 + lane;
     if (arow < K) {
+      float* out = a.trans + (int64_t(tile) * K + arow) * K;
+      const bool live = arow < Ka;
 #pragma unroll
-      for (int b = 0; b < 64; ++b) stage[arow * 65 + b] = v[b];
-    }
-  }
-  __syncthreads();
-  if (ok) {
-    float* out = a.trans + int64_t(tile) * K * K;
-    for (int e = threadIdx.x; e < K * K; e += LT_THREADS) {
-      const int arow = e / K, b = e - arow * K;
-      out[e] = (arow < Ka) ? __fmul_rn(gamma, stage[arow * 65 + b]) : 0.0f;
+      for (int b = 0; b < 64; ++b) v[b] = live ? __fmul_rn(gamma, v[b]) : 0.0f;
+      if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+#pragma unroll
+        for (int b4 = 0; b4 < 16; ++b4)
+          if (4 * b4 < K) reinterpret_cast<float4*>(out)[b4] = make_float4(v[4 * b4], v[4 * b4 + 1], v[4 * b4 + 2], v[4 * b4 + 3]);
+      } else {
+#pragma unroll
+        for (int b = 0; b < 64; ++b)
+          if (b < K) out[b] = v[b];
+      }
     }
   }
   if (threadIdx.x == 0 && a.gate) a.gate[tile] = gamma;
