@@ -307,10 +307,138 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w0)
+    if rank == 0 and not args.no_secondary:
+        line["secondary"] = secondary_workloads(dev, stream, hbm)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# the other workloads of the hot path (reported beside the headline, not part of its step)
+# ------------------------------------------------------------------------------------------------
+
+def _time_sequence(calls, reps, stream):
+    """Mean ms of each call of a sequence and of the whole sequence, CUDA events on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for _, fn in calls:
+                fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+        for r in range(reps):
+            ev[r][0].record(stream)
+            for i, (_, fn) in enumerate(calls):
+                fn()
+                ev[r][i + 1].record(stream)
+        torch.cuda.synchronize()
+    per = {name: sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps for i, (name, _) in enumerate(calls)}
+    total = sum(ev[r][0].elapsed_time(ev[r][-1]) for r in range(reps)) / reps
+    return per, total
+
+
+def secondary_workloads(dev, stream, hbm, reps=10):
+    """The pruned sampled draft (C3), the gated head (C4) and the dense walk with verification (C5):
+    blocks/s, logit GB/s and each kernel's time. Inputs are seeded and synthetic; C4 and C5 are
+    larger than L2 by themselves, C3 rotates three logit sets."""
+    import torch
+
+    import dspark_draft_selection_gb300 as ds
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    out = {}
+    status = ds.new_status(dev)
+
+    # C3: pruned vocabulary, lattice walked by sampling (T = 0.8, top-p 0.95) with a sparse q record
+    w = di.config3()
+    R, B, K = w["R"], w["B"], w["K"]
+    logits = [to_dev(w["logits"])] + [torch.roll(to_dev(w["logits"]), s, 0) for s in (1, 2)]
+    d2t, E, W, prev = to_dev(w["d2t"]), to_dev(w["E"]), to_dev(w["W"]), to_dev(w["prev"])
+    seed, step = to_dev(w["seed"]), to_dev(w["step"])
+    cand = ds.dspark_topk(logits[0], B, K, d2t=d2t, V_t=w["V_t"], status=status)[:3]
+    trans = ds.dspark_lattice_score(cand[1], prev, E, W, status=status)[:2]
+    chain = ds.dspark_chain_select(cand[2], trans[0], cand[1], "sample", temperature=w["temperature"],
+                                   top_p=w["top_p"], seed=seed, step=step, status=status)
+    chain_out, qrec = chain[:3], chain[3:6]
+    it = {"i": 0}
+
+    def c3_topk():
+        it["i"] = (it["i"] + 1) % 3
+        ds.dspark_topk(logits[it["i"]], B, K, d2t=d2t, V_t=w["V_t"], out=cand, status=status)
+
+    calls = [("topk", c3_topk),
+             ("lattice", lambda: ds.dspark_lattice_score(cand[1], prev, E, W, out=trans, status=status)),
+             ("chain_sample", lambda: ds.dspark_chain_select(cand[2], trans[0], cand[1], "sample",
+                                                             temperature=w["temperature"], top_p=w["top_p"],
+                                                             seed=seed, step=step, q=qrec, out=chain_out,
+                                                             status=status))]
+    per, total = _time_sequence(calls, reps, stream)
+    lb = R * B * w["V_d"] * 2
+    out[w["name"]] = {"blocks_per_s": round(R / (total / 1e3), 1), "ms_per_step": round(total, 5),
+                      "logit_gbs": round(lb / (per["topk"] / 1e3) / 1e9, 1),
+                      "logit_frac": round(lb / (per["topk"] / 1e3) / 1e9 / hbm, 4),
+                      "kernels_ms": {k: round(v, 5) for k, v in per.items()}}
+    del logits, d2t, E, W, cand, trans, chain
+
+    # C4: gated DFlash v2 head, 896 rows of 248,320 logits (445 MB, larger than L2)
+    w = di.config4()
+    R, B, K = w["R"], w["B"], w["K"]
+    logits, E, W, prev = to_dev(w["logits"]), to_dev(w["E"]), to_dev(w["W"]), to_dev(w["prev"])
+    hidden, g = to_dev(w["hidden"]), to_dev(w["g"])
+    cand = ds.dspark_topk(logits, B, K, status=status)[:3]
+    trans = ds.dspark_lattice_score(cand[1], prev, E, W, hidden=hidden, g=g, status=status)[:2]
+    chain_out = ds.dspark_chain_select(cand[2], trans[0], cand[1], "maxsum", status=status)[:3]
+    calls = [("topk", lambda: ds.dspark_topk(logits, B, K, out=cand, status=status)),
+             ("lattice_gated", lambda: ds.dspark_lattice_score(cand[1], prev, E, W, hidden=hidden, g=g, out=trans,
+                                                               status=status)),
+             ("chain", lambda: ds.dspark_chain_select(cand[2], trans[0], cand[1], "maxsum", out=chain_out,
+                                                      status=status))]
+    per, total = _time_sequence(calls, reps, stream)
+    lb = R * B * w["V_d"] * 2
+    out[w["name"]] = {"blocks_per_s": round(R / (total / 1e3), 1), "ms_per_step": round(total, 5),
+                      "logit_gbs": round(lb / (per["topk"] / 1e3) / 1e9, 1),
+                      "logit_frac": round(lb / (per["topk"] / 1e3) / 1e9 / hbm, 4),
+                      "kernels_ms": {k: round(v, 5) for k, v in per.items()}}
+    del logits, E, W, hidden, g, cand, trans
+
+    # C5: dense Markov walk sampled at T = 1 with a dense q record, then rejection-sampling verification
+    w = di.config5()
+    R, B, V = w["R"], w["B"], w["V_d"]
+    logits, E, W, prev = to_dev(w["logits"]), to_dev(w["E"]), to_dev(w["W"]), to_dev(w["prev"])
+    target, seed, step, vseed = to_dev(w["target"]), to_dev(w["seed"]), to_dev(w["step"]), to_dev(w["vseed"])
+    q = ds.dense_record(R * B, V, dev)
+    ws_walk = ds.workspace(ds.OP_DENSE_WALK, R, B, V, 0, dev)
+    ws_ver = ds.workspace(ds.OP_VERIFY, R, B, V, 0, dev)
+    walk_out = ds.dspark_dense_walk(logits, B, prev, E, W, temperature=1.0, top_p=1.0, seed=seed, step=step, q=q,
+                                    ws=ws_walk, status=status)[:2]
+    n = torch.full((R,), B, dtype=torch.int32, device=dev)
+    ver_out = ds.dspark_verify(target, B, walk_out[0], n, q, temperature=1.0, top_p=1.0, vseed=vseed, step=step,
+                               ws=ws_ver, status=status)[:3]
+    calls = [("dense_walk", lambda: ds.dspark_dense_walk(logits, B, prev, E, W, temperature=1.0, top_p=1.0, seed=seed,
+                                                         step=step, q=q, out=walk_out, ws=ws_walk, status=status)),
+             ("verify", lambda: ds.dspark_verify(target, B, walk_out[0], n, q, temperature=1.0, top_p=1.0, vseed=vseed,
+                                                 step=step, out=ver_out, ws=ws_ver, status=status))]
+    per, total = _time_sequence(calls, max(3, reps // 2), stream)
+    draft_b, target_b = R * B * V * 2, R * (B + 1) * V * 2
+    walk_bytes = draft_b + R * B * V * 4 + V * w["rank"] * 2          # logits + z record + W once
+    out[w["name"]] = {"blocks_per_s": round(R / (total / 1e3), 1), "ms_per_step": round(total, 5),
+                      "logit_gbs": round((draft_b + target_b) / (total / 1e3) / 1e9, 1),
+                      "dense_walk_gbs": round(walk_bytes / (per["dense_walk"] / 1e3) / 1e9, 1),
+                      "dense_walk_frac": round(walk_bytes / (per["dense_walk"] / 1e3) / 1e9 / hbm, 4),
+                      "verify_logit_gbs": round(target_b / (per["verify"] / 1e3) / 1e9, 1),
+                      "verify_frac": round(target_b / (per["verify"] / 1e3) / 1e9 / hbm, 4),
+                      "kernels_ms": {k: round(v, 5) for k, v in per.items()}}
+    torch.cuda.synchronize()
+    st = ds.read_status(status)
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the secondary workloads")
+    return out
 
 
 # ------------------------------------------------------------------------------------------------
@@ -402,6 +530,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the C3-C5 workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

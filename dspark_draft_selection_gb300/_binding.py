@@ -197,7 +197,7 @@ def _qrec_sparse(ids, p, n):
 
 
 def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature=0.0, top_p=1.0, seed=None,
-                        step=None, record=True, out=None, status=None, stream=None):
+                        step=None, record=True, q=None, out=None, status=None, stream=None):
     R, B, K = cand_val.shape
     dev = cand_val.device
     m = MODES[mode] if isinstance(mode, str) else int(mode)
@@ -205,9 +205,13 @@ def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature
         out = (torch.empty((R, B), dtype=torch.int32, device=dev), torch.empty((R, B), dtype=torch.int32, device=dev),
                torch.empty((R,), dtype=torch.float32, device=dev))
     status = new_status(dev) if status is None else status
-    q = None
     qt = ()
-    if m == DSPARK_SAMPLE and record:
+    if m != DSPARK_SAMPLE:
+        q = None
+    elif q is not None:                                     # caller's sparse record (ids, p, n)
+        qt = tuple(q)
+        q = _qrec_sparse(*qt)
+    elif record:
         qt = (torch.full((R, B, K), -1, dtype=torch.int32, device=dev), torch.zeros((R, B, K), dtype=torch.float32,
                                                                                    device=dev),
               torch.zeros((R, B), dtype=torch.int32, device=dev))

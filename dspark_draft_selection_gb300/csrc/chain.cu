@@ -78,8 +78,6 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
   __shared__ float s_bv[4][CH_MAXK];
   __shared__ int s_ba[4][CH_MAXK];
   __shared__ uint8_t s_back[CH_MAXB][CH_MAXK];
-  __shared__ float s_w[CH_MAXK];
-  __shared__ int s_order[CH_MAXK];
 
   const int r = blockIdx.x, K = a.K, B = a.B, t = threadIdx.x;
   const int KK = K * K;
@@ -214,57 +212,54 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         for (int h = 0; h < 2; ++h) {
           const int b = lane + 32 * h;
           w[h] = (b < K) ? ds_weight(__fsub_rn(z[h], zmax)) : 0.0f;
-          if (b < K) s_w[b] = w[h];
         }
         __syncwarp();
         const double wall = ds_warp_sum(double(w[0]) + double(w[1]));
         // kept[h]: nucleus membership of candidate lane + 32h
         bool kept[2] = {w[0] > 0.0f, w[1] > 0.0f};
         if (a.top_p < 1.0f) {
-          // rank in (weight desc, rank asc) order, then the running mass in that order
+          // (weight desc, rank asc) order by a warp bitonic sort of the 64 keys (position i = lane
+          // + 32h holds one key), then the running mass in that order and the cut
+          const uint64_t key0 = (lane < K) ? ds_key64(w[0], uint32_t(lane)) : 0ull;
+          const uint64_t key1 = (lane + 32 < K) ? ds_key64(w[1], uint32_t(lane + 32)) : 0ull;
+          uint64_t x[2] = {key0, key1};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int b = lane + 32 * h;
-            if (b < K) {
-              int rk = 0;
-              for (int c = 0; c < K; ++c) {
-                const float wc = s_w[c];
-                rk += (wc > w[h] || (wc == w[h] && c < b)) ? 1 : 0;
+          for (int kk = 2; kk <= 64; kk <<= 1) {
+#pragma unroll
+            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+              if (jj == 32) {
+                // partner is the other key of this lane; the whole 64 sorts descending
+                const uint64_t hi = x[0] > x[1] ? x[0] : x[1], lo = x[0] > x[1] ? x[1] : x[0];
+                x[0] = hi;
+                x[1] = lo;
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int i = lane + 32 * h;
+                  const uint64_t y = __shfl_xor_sync(0xFFFFFFFFu, x[h], jj);
+                  const bool up = (i & kk) == 0;          // this run of kk sorts descending
+                  const bool keep_max = ((lane & jj) == 0) == up;
+                  x[h] = keep_max ? (x[h] > y ? x[h] : y) : (x[h] < y ? x[h] : y);
+                }
               }
-              s_order[rk] = b;
             }
           }
-          __syncwarp();
-          // sorted position sp = 2 * lane + h holds candidate s_order[sp]
+          // sorted position i = lane + 32h: mass w / wall, running sums over positions 0..63
           double pw[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int sp = 2 * lane + h;
-            pw[h] = (sp < K) ? double(s_w[s_order[sp]]) / wall : 0.0;
-          }
-          const double incl = ch_warp_scan(pw[0] + pw[1]);
-          const double c0 = incl - pw[1];           // running mass through sorted position 2*lane
+          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? double(ds_key64_val(x[h])) / wall : 0.0;
+          const double inc0 = ch_warp_scan(pw[0]);
+          const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
+          const double inc1 = tot0 + ch_warp_scan(pw[1]);
           const double tp = double(a.top_p);
-          const bool over0 = (2 * lane < K) && c0 > tp && pw[0] > 0.0;
-          const bool over1 = (2 * lane + 1 < K) && incl > tp && pw[1] > 0.0;
-          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, over0), b1 = __ballot_sync(0xFFFFFFFFu, over1);
-          int cut = K;                              // first sorted position whose running mass > top_p
+          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && inc0 > tp && pw[0] > 0.0);
+          const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && inc1 > tp && pw[1] > 0.0);
           if (b0 | b1) {
-            const int l0 = b0 ? __ffs(b0) - 1 : 32, l1 = b1 ? __ffs(b1) - 1 : 32;
-            cut = min(2 * l0, 2 * l1 + 1);
-          }
-          // candidate b is kept iff its sorted position is <= cut (and its weight is positive)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int b = lane + 32 * h;
-            if (b < K && cut < K) {
-              int rk = 0;
-              for (int c = 0; c < K; ++c) {
-                const float wc = s_w[c];
-                rk += (wc > w[h] || (wc == w[h] && c < b)) ? 1 : 0;
-              }
-              kept[h] = kept[h] && rk <= cut;
-            }
+            // first sorted position whose running mass exceeds top_p: keys at or above it are kept
+            const int cl_ = b0 ? __ffs(b0) - 1 : __ffs(b1) - 1;
+            const uint64_t cutk = __shfl_sync(0xFFFFFFFFu, b0 ? x[0] : x[1], cl_);
+            kept[0] = kept[0] && key0 >= cutk;
+            kept[1] = kept[1] && key1 >= cutk;
           }
         }
         // draw: kept candidates in ascending rank order; running sums by warp scan

@@ -8,12 +8,14 @@
 // gathered by thresholds p_max e^-10, e^-20, e^-40, then all; exponents below -64 flushed); the
 // commit on double-precision multinomial sums; the commit on the double uniform.
 //
-// One cluster of C CTAs per row (layout in rowsample.cuh); the row is read from HBM once and
-// stays in registers through: the maximum of z = s / T, the nucleus (threshold rounds with the
-// candidates sorted in the leader CTA; a 64-step bisection over (weight, index) keys when the
-// candidates overflow the leader), the kept mass per (thread, segment), the cluster prefix that
-// locates the CTA, segment and thread whose running sum crosses u * W_kept, and the walk over that
-// thread's <= 8 elements.
+// One block of 512 threads per row (persistent over rows, one block per SM), no clusters: the
+// row streams through the block in passes (16-byte loads, several chunks in flight per thread;
+// repeated passes mostly hit L2): the maximum of z = s / T (and the dense record's z row), the
+// nucleus when top-p < 1 (threshold rounds with the candidates sorted in shared memory; a
+// 64-step bisection over (weight, index) keys when they overflow), then the kept mass of every
+// cell of 32 vectors (float pairs per thread, double per warp). A block scan over the cells
+// locates the one whose running sum crosses u * W_kept; its warp re-reads those 32 vectors and
+// finds the lane, then the element.
 #include <cfloat>
 
 #include "host_common.h"
@@ -38,155 +40,171 @@ DS_DEV bool sp_keep(float w, int64_t i, float wcut, int64_t icut) {
   return w > 0.0f && (w > wcut || (w == wcut && i <= icut));
 }
 
-template <typename T, bool XFORM>
-__global__ void __launch_bounds__(rs::THREADS, 1) sample_cluster_kernel(const rs::SampleArgs a) {
+// Geometry of one row: scalar head up to 16-byte alignment, vectors in chunks of SR_THREADS (one
+// per thread), scalar tail. Index order: head, chunk 0 (thread order), chunk 1, ..., tail; the
+// vectors of warp w in chunk c form cell c * WARPS + w.
+constexpr int SR_THREADS = rs::THREADS;
+constexpr int SR_WARPS = rs::WARPS;
+constexpr int SR_U = 4;                      // chunks loaded together by a thread (bytes in flight)
+constexpr int SR_MAXCHUNK = 128;             // rows of up to 128 x 512 vectors
+constexpr int SR_CELLS = SR_MAXCHUNK * SR_WARPS;
+
+template <typename T>
+struct SrRow {
+  const T* row;
+  int64_t head, nvec, tail0, ntail;
+  int nchunk;
+};
+
+template <typename T>
+DS_DEV SrRow<T> sr_row(const T* row, int64_t V) {
   constexpr int EPV = 16 / sizeof(T);
-  constexpr int SEGS = rs::SEGS;
+  SrRow<T> g;
+  g.row = row;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+  g.head = int64_t(((16u - (addr & 15u)) & 15u) / sizeof(T));
+  if (g.head > V) g.head = V;
+  g.nvec = (V - g.head) / EPV;
+  g.tail0 = g.head + g.nvec * EPV;
+  g.ntail = V - g.tail0;
+  g.nchunk = int((g.nvec + SR_THREADS - 1) / SR_THREADS);
+  return g;
+}
+
+// Calls f(raw value, index, chunk) for every element this thread holds (head elements with chunk
+// -1, tail elements with chunk nchunk), and fc(chunk) after each chunk, with every thread of the
+// block taking part (fc may use warp collectives). SR_U chunks are loaded at a time.
+template <typename T, typename F, typename FC>
+DS_DEV void sr_pass(const SrRow<T>& g, F&& f, FC&& fc) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int tid = threadIdx.x;
+  if (tid < g.head) f(ds_load_elem<T>(g.row + tid), int64_t(tid), -1);
+  const uint4* vp = reinterpret_cast<const uint4*>(g.row + g.head);
+  for (int c0 = 0; c0 < g.nchunk; c0 += SR_U) {
+    uint4 buf[SR_U];
+#pragma unroll
+    for (int u = 0; u < SR_U; ++u) {
+      const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
+      if (c0 + u < g.nchunk && v < g.nvec) buf[u] = __ldg(vp + v);
+    }
+#pragma unroll
+    for (int u = 0; u < SR_U; ++u) {
+      if (c0 + u >= g.nchunk) break;
+      const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
+      if (v < g.nvec) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) f(ds_vec_elem<T>(buf[u], e), g.head + v * EPV + e, c0 + u);
+      }
+      fc(c0 + u);
+    }
+  }
+  if (tid < g.ntail) f(ds_load_elem<T>(g.row + g.tail0 + tid), g.tail0 + tid, g.nchunk);
+}
+
+template <typename T, bool XFORM>
+__global__ void __launch_bounds__(SR_THREADS, 1) sample_row_kernel(const rs::SampleArgs a, int64_t rows) {
+  constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(16) uint8_t dsm[];
-  double(*s_mass)[rs::THREADS] = reinterpret_cast<double(*)[rs::THREADS]>(dsm);
-  uint64_t* s_keys = reinterpret_cast<uint64_t*>(dsm + sizeof(double) * SEGS * rs::THREADS);
+  double* s_cell = reinterpret_cast<double*>(dsm);                        // [SR_CELLS] per-cell sums
+  uint64_t* s_keys = reinterpret_cast<uint64_t*>(dsm + sizeof(double) * SR_CELLS);   // [SP_CAP]
   __shared__ rs::BlockScratch bs;
-  __shared__ rs::ClusterRed cr;
   __shared__ uint32_t s_cnt;
-  __shared__ int s_seg;
+  __shared__ int s_cellpick;
   __shared__ double s_tau, s_cut[2];
 
-  cg::cluster_group cl = cg::this_cluster();
-  const int C = a.C, crank = int(cl.block_rank());
-  const int64_t row_id = blockIdx.x / C;
-  const int64_t r = row_id / a.B, j = row_id % a.B;
-  const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
-  if (a.n_draft && j > a.n_draft[r]) return;        // every CTA of the cluster leaves together
-  const T* row = reinterpret_cast<const T*>(a.rows) + prow * a.ld;
-  const rs::RowGeom g = rs::row_geom<T>(row, a.V, C, crank);
-  const int tid = threadIdx.x;
-  rs::cred_init(cr);
-  if (tid == 0) s_cnt = 0;
-
-  uint4 buf[rs::MAXV];
-#pragma unroll
-  for (int k = 0; k < rs::MAXV; ++k) {
-    const int64_t v = g.vec_index(k);
-    if (v >= 0) buf[k] = ds_ld_stream(reinterpret_cast<const uint4*>(row + g.head) + v);
-  }
-  const float rh = g.has_head() ? ds_load_elem<T>(row + tid) : 0.0f;
-  const float rt = g.has_tail() ? ds_load_elem<T>(row + g.tail0 + tid) : 0.0f;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool greedy = !(a.T > 0.0f);
   const float Tz = greedy ? 1.0f : a.T;
   auto zof = [&](float raw) { return ds_temper(sp_xform<XFORM>(raw, a.mult, a.softcap), Tz); };
-  const int64_t ih = tid, it = g.tail0 + tid;
 
-  int64_t pick = -1;
-  float zmax = 0.0f, wcut = 0.0f;
-  int64_t icut = -1;
-  double wkept = 1.0;
+  for (int64_t row_id = blockIdx.x; row_id < rows; row_id += gridDim.x) {
+    const int64_t r = row_id / a.B, j = row_id % a.B;
+    if (a.n_draft && j > a.n_draft[r]) continue;          // the whole block skips the row
+    const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
+    const SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
+    const int64_t qrow = row_id * a.q_row_mul + a.q_row_add;
+    float* zr = (a.q_mode == 2 && a.write_z) ? a.q.z + qrow * a.q.ldz : nullptr;
+    const int ncells = g.nchunk * SR_WARPS;
 
-  if (greedy) {
-    // argmax, lowest index on ties
-    unsigned long long best = 0;
-#pragma unroll
-    for (int k = 0; k < rs::MAXV; ++k) {
-      const int64_t v = g.vec_index(k);
-      if (v >= 0) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const unsigned long long kk = ds_key64(ds_canon_zero(zof(ds_vec_elem<T>(buf[k], e))), uint32_t(g.head + v * EPV + e));
-          best = max(best, kk);
-        }
-      }
-    }
-    if (g.has_head()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rh)), uint32_t(ih)));
-    if (g.has_tail()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rt)), uint32_t(it)));
-    best = rs::cluster_max_u64(cl, cr, rs::block_max_u64(best, bs));
-    zmax = ds_key64_val(best);
-    wcut = 1.0f;
-    icut = ds_key64_idx(best);
-    if (crank == 0 && tid == 0) pick = icut;
-  } else {
-    // ---- maximum of z ----
+    // ---- pass 1: maximum of z and the argmax key (lowest index on ties); the z row of a dense
+    // record is written on the way ----
     float tmax = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < rs::MAXV; ++k)
-      if (g.vec_index(k) >= 0) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) tmax = fmaxf(tmax, zof(ds_vec_elem<T>(buf[k], e)));
-      }
-    if (g.has_head()) tmax = fmaxf(tmax, zof(rh));
-    if (g.has_tail()) tmax = fmaxf(tmax, zof(rt));
-    zmax = float(rs::cluster_sum_d(cl, cr, double(rs::block_max(tmax, bs)), 1));
-    if (!(zmax > -INFINITY && zmax < INFINITY)) {
-      if (tid == 0 && crank == 0) {
-        ds_set_error(a.status, DSPARK_ENONFINITE);
-        if (a.out_idx) a.out_idx[row_id * a.out_mul + a.out_add] = -1;
-        a.out_tgt[row_id * a.out_mul + a.out_add] = -1;
-        if (a.prev_out) a.prev_out[r] = -1;
-      }
-      cl.sync();
-      return;
-    }
-    auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
+    unsigned long long best = 0;
+    const bool want_key = greedy || a.amax_out != nullptr;
+    sr_pass(g,
+            [&](float raw, int64_t i, int) {
+              const float z = zof(raw);
+              tmax = fmaxf(tmax, z);
+              if (want_key) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(z), uint32_t(i)));
+              if (zr) zr[i] = z;
+            },
+            [](int) {});
+    if (want_key) best = rs::block_max_u64(best, bs);
 
-    // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order ----
-    if (a.top_p < 1.0f) {
-      rs::FF acc{0.0f, 0.0f};
-#pragma unroll
-      for (int k = 0; k < rs::MAXV; ++k)
-        if (g.vec_index(k) >= 0) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) rs::ff_add(acc, wof(ds_vec_elem<T>(buf[k], e)));
+    int64_t pick = -1;
+    float zmax, wcut = 0.0f;
+    int64_t icut = -1;
+    double wkept = 1.0;
+    if (greedy) {
+      zmax = ds_key64_val(best);
+      wcut = 1.0f;
+      icut = ds_key64_idx(best);
+      if (tid == 0) pick = icut;
+    } else {
+      zmax = rs::block_max(tmax, bs);
+      if (!(zmax > -INFINITY && zmax < INFINITY)) {
+        if (tid == 0) {
+          ds_set_error(a.status, DSPARK_ENONFINITE);
+          if (a.out_idx) a.out_idx[row_id * a.out_mul + a.out_add] = -1;
+          a.out_tgt[row_id * a.out_mul + a.out_add] = -1;
+          if (a.prev_out) a.prev_out[r] = -1;
         }
-      if (g.has_head()) rs::ff_add(acc, wof(rh));
-      if (g.has_tail()) rs::ff_add(acc, wof(rt));
-      const double wall = rs::cluster_sum_d(cl, cr, rs::block_sum(rs::ff_value(acc), bs));
-      const double tp = double(a.top_p);
-      for (int round = 0; round < 4; ++round) {
-        const float tau = round == 0 ? ds_weight(-10.0f) : round == 1 ? ds_weight(-20.0f)
-                        : round == 2 ? ds_weight(-40.0f) : FLT_MIN;
-        rs::FF m{0.0f, 0.0f};
-        double cnt = 0.0;
-        auto visit = [&](float w) {
-          if (w >= tau) {
-            rs::ff_add(m, w);
-            cnt += 1.0;
-          }
-        };
-#pragma unroll
-        for (int k = 0; k < rs::MAXV; ++k)
-          if (g.vec_index(k) >= 0) {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) visit(wof(ds_vec_elem<T>(buf[k], e)));
-          }
-        if (g.has_head()) visit(wof(rh));
-        if (g.has_tail()) visit(wof(rt));
-        const double mass = rs::cluster_sum_d(cl, cr, rs::block_sum(rs::ff_value(m), bs));
-        const double ncand = rs::cluster_sum_d(cl, cr, rs::block_sum(cnt, bs));
-        if (round < 3 && !(mass / wall > tp + 1e-12)) continue;
-        if (ncand <= double(SP_CAP)) {
-          // candidates (a prefix of the sorted order) sorted in the leader, walked in order
-          uint32_t* lcnt = cl.map_shared_rank(&s_cnt, 0);
-          uint64_t* lkeys = cl.map_shared_rank(s_keys, 0);
-          auto push = [&](float w, int64_t i) {
-            if (w >= tau) {
-              const uint32_t slot = atomicAdd(lcnt, 1u);
-              if (slot < SP_CAP) lkeys[slot] = ds_key64(w, uint32_t(i));
-            }
-          };
-#pragma unroll
-          for (int k = 0; k < rs::MAXV; ++k) {
-            const int64_t v = g.vec_index(k);
-            if (v >= 0) {
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) push(wof(ds_vec_elem<T>(buf[k], e)), g.head + v * EPV + e);
-            }
-          }
-          if (g.has_head()) push(wof(rh), ih);
-          if (g.has_tail()) push(wof(rt), it);
-          cl.sync();
-          if (crank == 0) {
+        __syncthreads();
+        continue;
+      }
+      auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
+
+      // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order ----
+      if (a.top_p < 1.0f) {
+        rs::FF acc{0.0f, 0.0f};
+        sr_pass(g, [&](float raw, int64_t, int) { rs::ff_add(acc, wof(raw)); }, [](int) {});
+        const double wall = rs::block_sum(rs::ff_value(acc), bs);
+        const double tp = double(a.top_p);
+        for (int round = 0; round < 4; ++round) {
+          const float tau = round == 0 ? ds_weight(-10.0f) : round == 1 ? ds_weight(-20.0f)
+                          : round == 2 ? ds_weight(-40.0f) : FLT_MIN;
+          rs::FF m{0.0f, 0.0f};
+          double cnt = 0.0;
+          sr_pass(g,
+                  [&](float raw, int64_t, int) {
+                    const float w = wof(raw);
+                    if (w >= tau) {
+                      rs::ff_add(m, w);
+                      cnt += 1.0;
+                    }
+                  },
+                  [](int) {});
+          const double mass = rs::block_sum(rs::ff_value(m), bs);
+          const double ncand = rs::block_sum(cnt, bs);
+          if (round < 3 && !(mass / wall > tp + 1e-12)) continue;
+          if (ncand <= double(SP_CAP)) {
+            // the candidates (a prefix of the sorted order), sorted, walked in order
+            if (tid == 0) s_cnt = 0;
+            __syncthreads();
+            sr_pass(g,
+                    [&](float raw, int64_t i, int) {
+                      const float w = wof(raw);
+                      if (w >= tau) {
+                        const uint32_t slot = atomicAdd(&s_cnt, 1u);
+                        if (slot < SP_CAP) s_keys[slot] = ds_key64(w, uint32_t(i));
+                      }
+                    },
+                    [](int) {});
+            __syncthreads();
             const int n = int(min(s_cnt, uint32_t(SP_CAP)));
             int n2 = 1;
             while (n2 < n) n2 <<= 1;
-            for (int i = n + tid; i < n2; i += blockDim.x) s_keys[i] = 0;
+            for (int i = n + tid; i < n2; i += SR_THREADS) s_keys[i] = 0;
             __syncthreads();
             ds_block_sort_desc(s_keys, n2);
             if (tid == 0) {
@@ -202,363 +220,308 @@ __global__ void __launch_bounds__(rs::THREADS, 1) sample_cluster_kernel(const rs
                   break;
                 }
               }
-              s_cnt = 0;
+            }
+          } else {
+            // bisection for the largest (weight, index) key whose upper set has mass > top_p
+            unsigned long long res = 0;
+            for (int b = 63; b >= 0; --b) {
+              const unsigned long long cand = res | (1ull << b);
+              rs::FF mm{0.0f, 0.0f};
+              sr_pass(g,
+                      [&](float raw, int64_t i, int) {
+                        const float w = wof(raw);
+                        if ((unsigned long long)ds_key64(w, uint32_t(i)) >= cand) rs::ff_add(mm, w);
+                      },
+                      [](int) {});
+              const double mb = rs::block_sum(rs::ff_value(mm), bs);
+              if (mb / wall > tp) res = cand;
+            }
+            if (tid == 0) {
+              s_cut[0] = double(ds_key64_val(res));
+              s_cut[1] = double(ds_key64_idx(res));
             }
           }
+          break;
+        }
+        __syncthreads();
+        wcut = float(s_cut[0]);
+        icut = int64_t(s_cut[1]);
+      }
+
+      // ---- pass: kept mass per cell (float pairs per thread, double per warp), head, tail and
+      // the last kept index ----
+      rs::FF m{0.0f, 0.0f}, mh{0.0f, 0.0f}, mt{0.0f, 0.0f};
+      unsigned long long lastk = 0;
+      sr_pass(g,
+              [&](float raw, int64_t i, int c) {
+                const float w = wof(raw);
+                if (sp_keep(w, i, wcut, icut)) {
+                  if (c < 0) rs::ff_add(mh, w);
+                  else if (c >= g.nchunk) rs::ff_add(mt, w);
+                  else rs::ff_add(m, w);
+                  lastk = max(lastk, (unsigned long long)(i + 1));
+                }
+              },
+              [&](int c) {
+                const double cw = ds_warp_sum(rs::ff_value(m));
+                if (lane == 0) s_cell[c * SR_WARPS + warp] = cw;
+                m = rs::FF{0.0f, 0.0f};
+              });
+      const double Hm = rs::block_sum(rs::ff_value(mh), bs);    // (also orders the cell writes)
+      const double Tm = rs::block_sum(rs::ff_value(mt), bs);
+      const int64_t last_kept = int64_t(rs::block_max_u64(lastk, bs)) - 1;
+      // cells: each thread owns a contiguous run of cells; exclusive prefix over threads
+      const int per = (ncells + SR_THREADS - 1) / SR_THREADS;
+      const int c0 = tid * per, c1 = min(ncells, c0 + per);
+      double mine = 0.0;
+      for (int c = c0; c < c1; ++c) mine += s_cell[c];
+      double ctot = 0.0;
+      const double before = rs::block_exclusive_scan(mine, &ctot, bs);
+      wkept = Hm + ctot + Tm;
+
+      if (a.probe_w) {
+        const int64_t x = (a.probe_tgt && j < a.n_draft[r]) ? int64_t(a.probe_tgt[r * (a.B - 1) + j]) : -1;
+        if (tid == 0) {
+          float pw = 0.0f;
+          if (x >= 0 && x < a.V) {
+            const float w = wof(ds_load_elem<T>(g.row + x));
+            pw = sp_keep(w, x, wcut, icut) ? w : 0.0f;
+          }
+          a.probe_w[row_id] = pw;
+        }
+      }
+
+      // ---- draw: the first kept index whose running sum exceeds u * W_kept ----
+      if (!a.no_draw) {
+        const double u = ds_uniform(a.seed[r], a.step[r], uint32_t(a.position >= 0 ? a.position : int32_t(j)),
+                                    DS_PURPOSE_DRAFT);
+        const double target = u * wkept;
+        if (tid == 0) s_cellpick = -3;                        // -3 none, -1 head, -2 tail
+        __syncthreads();
+        if (target < Hm) {
+          if (tid == 0) s_cellpick = -1;
+        } else if (target >= Hm + ctot) {
+          if (tid == 0) s_cellpick = (target < wkept) ? -2 : -4;   // -4: rounding left it past the end
         } else {
-          // bisection for the largest (weight, index) key whose upper set has mass > top_p
-          unsigned long long res = 0;
-          for (int b = 63; b >= 0; --b) {
-            const unsigned long long cand = res | (1ull << b);
-            rs::FF mm{0.0f, 0.0f};
-            auto vis2 = [&](float w, int64_t i) {
-              if ((unsigned long long)ds_key64(w, uint32_t(i)) >= cand) rs::ff_add(mm, w);
-            };
-#pragma unroll
-            for (int k = 0; k < rs::MAXV; ++k) {
-              const int64_t v = g.vec_index(k);
-              if (v >= 0) {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) vis2(wof(ds_vec_elem<T>(buf[k], e)), g.head + v * EPV + e);
+          const double t_in = target - Hm;
+          if (t_in >= before && t_in < before + mine) {
+            double acc = before;
+            int found = -1;
+            for (int c = c0; c < c1; ++c) {
+              if (found < 0 && t_in < acc + s_cell[c] && s_cell[c] > 0.0) {
+                found = c;
+                s_tau = t_in - acc;
+              }
+              acc += s_cell[c];
+            }
+            if (found < 0) {                                  // rounding: the last cell with mass
+              for (int c = c1 - 1; c >= c0; --c)
+                if (s_cell[c] > 0.0) {
+                  found = c;
+                  s_tau = INFINITY;
+                  break;
+                }
+            }
+            s_cellpick = found;
+          }
+        }
+        __syncthreads();
+        const int cp = s_cellpick;
+        if (cp == -1 || cp == -2) {
+          // the few scalar head or tail elements, walked by one thread
+          if (tid == 0) {
+            double run = (cp == -1) ? 0.0 : Hm + ctot;
+            const int64_t i0 = (cp == -1) ? 0 : g.tail0, i1 = (cp == -1) ? g.head : a.V;
+            int64_t lastmine = -1;
+            for (int64_t i = i0; i < i1 && pick < 0; ++i) {
+              const float w = wof(ds_load_elem<T>(g.row + i));
+              if (sp_keep(w, i, wcut, icut)) {
+                run += double(w);
+                lastmine = i;
+                if (run > target) pick = i;
               }
             }
-            if (g.has_head()) vis2(wof(rh), ih);
-            if (g.has_tail()) vis2(wof(rt), it);
-            const double mb = rs::cluster_sum_d(cl, cr, rs::block_sum(rs::ff_value(mm), bs));
-            if (mb / wall > tp) res = cand;
+            if (pick < 0) pick = lastmine;
           }
-          if (tid == 0) {
-            s_cut[0] = double(ds_key64_val(res));
-            s_cut[1] = double(ds_key64_idx(res));
-          }
-        }
-        break;
-      }
-      wcut = float(rs::cluster_sum_d(cl, cr, crank == 0 ? s_cut[0] : 0.0));
-      icut = int64_t(rs::cluster_sum_d(cl, cr, crank == 0 ? s_cut[1] : 0.0));
-    }
-
-    // ---- kept mass per (thread, segment): segment 0 head, 1 + k round k, SEGS - 1 tail ----
-    double mine = 0.0;
-    unsigned long long lastk = 0;
-    {
-      double mh = 0.0;
-      if (g.has_head()) {
-        const float w = wof(rh);
-        if (sp_keep(w, ih, wcut, icut)) {
-          mh = double(w);
-          lastk = max(lastk, (unsigned long long)(ih + 1));
-        }
-      }
-      s_mass[0][tid] = mh;
-      mine += mh;
-    }
+        } else if (cp == -4 || cp == -3) {
+          if (tid == 0) pick = last_kept;                     // rounding left the target at the very end
+        } else if (warp == cp % SR_WARPS) {
+          // the crossing cell: its warp re-reads its 32 vectors and finds the lane, then the element
+          const int c = cp / SR_WARPS;
+          const double tau = s_tau;
+          const int64_t v = int64_t(c) * SR_THREADS + tid;
+          uint4 w4 = make_uint4(0, 0, 0, 0);
+          if (v < g.nvec) w4 = __ldg(reinterpret_cast<const uint4*>(g.row + g.head) + v);
+          rs::FF lm{0.0f, 0.0f};
+          if (v < g.nvec) {
 #pragma unroll
-    for (int k = 0; k < rs::MAXV; ++k) {
-      const int64_t v = g.vec_index(k);
-      rs::FF m{0.0f, 0.0f};
-      if (v >= 0) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const float w = wof(ds_vec_elem<T>(buf[k], e));
-          const int64_t i = g.head + v * EPV + e;
-          if (sp_keep(w, i, wcut, icut)) {
-            rs::ff_add(m, w);
-            lastk = max(lastk, (unsigned long long)(i + 1));
-          }
-        }
-      }
-      s_mass[1 + k][tid] = rs::ff_value(m);
-      mine += s_mass[1 + k][tid];
-    }
-    {
-      double mt = 0.0;
-      if (g.has_tail()) {
-        const float w = wof(rt);
-        if (sp_keep(w, it, wcut, icut)) {
-          mt = double(w);
-          lastk = max(lastk, (unsigned long long)(it + 1));
-        }
-      }
-      s_mass[SEGS - 1][tid] = mt;
-      mine += mt;
-    }
-    const double ctot = rs::block_sum(mine, bs);
-    double wtot = 0.0;
-    const double cpre = rs::cluster_sum_d(cl, cr, ctot, 2, &wtot);
-    const int64_t last_kept = int64_t(rs::cluster_max_u64(cl, cr, rs::block_max_u64(lastk, bs))) - 1;
-    wkept = wtot;
-    if (a.amax_out) {
-      // argmax of z (lowest index on ties), for greedy verification
-      unsigned long long best = 0;
-#pragma unroll
-      for (int k = 0; k < rs::MAXV; ++k) {
-        const int64_t v = g.vec_index(k);
-        if (v >= 0) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(ds_vec_elem<T>(buf[k], e))), uint32_t(g.head + v * EPV + e)));
-        }
-      }
-      if (g.has_head()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rh)), uint32_t(ih)));
-      if (g.has_tail()) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(zof(rt)), uint32_t(it)));
-      best = rs::cluster_max_u64(cl, cr, rs::block_max_u64(best, bs));
-      if (crank == 0 && tid == 0) a.amax_out[row_id] = int32_t(ds_key64_idx(best));
-    }
-    if (a.probe_w) {
-      const int64_t x = (a.probe_tgt && j < a.n_draft[r]) ? int64_t(a.probe_tgt[r * (a.B - 1) + j]) : -1;
-      if (crank == 0 && tid == 0 && (x < 0 || x >= a.V)) a.probe_w[row_id] = 0.0f;
-      if (x >= 0 && x < a.V) {
-        auto probe = [&](float raw, int64_t i) {
-          if (i == x) {
-            const float w = wof(raw);
-            a.probe_w[row_id] = sp_keep(w, i, wcut, icut) ? w : 0.0f;
-          }
-        };
-        if (g.has_head()) probe(rh, ih);
-        if (g.has_tail()) probe(rt, it);
-#pragma unroll
-        for (int k = 0; k < rs::MAXV; ++k) {
-          const int64_t v = g.vec_index(k);
-          if (v >= 0 && x >= g.head + v * EPV && x < g.head + (v + 1) * EPV) {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) probe(ds_vec_elem<T>(buf[k], e), g.head + v * EPV + e);
-          }
-        }
-      }
-    }
-    const double u = a.no_draw ? 2.0 : ds_uniform(a.seed[r], a.step[r], uint32_t(a.position >= 0 ? a.position : int32_t(j)),
-                                DS_PURPOSE_DRAFT);
-    const double target = u * wtot;
-    if (!a.no_draw && target >= cpre && target < cpre + ctot) {
-      // this CTA holds the crossing: find the segment, then the thread, then the element
-      const int warp = tid >> 5, lane = tid & 31;
-      if (warp < SEGS) {
-        double sacc = 0.0;
-        for (int i = lane; i < rs::THREADS; i += 32) sacc += s_mass[warp][i];
-        sacc = ds_warp_sum(sacc);
-        if (lane == 0) bs.seg[warp] = sacc;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        double acc = cpre;
-        int sfound = -1;
-        double tau = 0.0;
-        int slast = -1;
-        for (int s = 0; s < SEGS; ++s) {
-          if (bs.seg[s] > 0.0) slast = s;
-          const double nxt = acc + bs.seg[s];
-          if (sfound < 0 && target < nxt && bs.seg[s] > 0.0) {
-            sfound = s;
-            tau = target - acc;
-          }
-          acc = nxt;
-        }
-        if (sfound < 0) {
-          sfound = slast;
-          tau = INFINITY;
-        }
-        s_seg = sfound;
-        s_tau = tau;
-      }
-      __syncthreads();
-      const int seg = s_seg;
-      const double tau = s_tau;
-      // inclusive / exclusive running sums over threads with excl[t+1] == incl[t] exactly
-      const double mv = (seg >= 0) ? s_mass[seg][tid] : 0.0;
-      double incl = mv;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      __syncthreads();
-      if (lane == 31) bs.d[warp] = incl;
-      __syncthreads();
-      double before = 0.0;
-      for (int w = 0; w < warp; ++w) before += bs.d[w];
-      const double prev_incl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-      const double ex = before + (lane > 0 ? prev_incl : 0.0);
-      const double in = before + incl;
-      bool last_thread_with_mass = false;
-      {
-        // the thread that holds the segment's last positive mass takes the rounding remainder
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, mv > 0.0);
-        __syncthreads();
-        if (lane == 0) bs.u[warp] = ball;
-        __syncthreads();
-        int lw = -1;
-        for (int w = rs::WARPS - 1; w >= 0; --w)
-          if (bs.u[w]) {
-            lw = w;
-            break;
-          }
-        last_thread_with_mass = (lw == warp) && (mv > 0.0) && (31 - __clz(unsigned(bs.u[lw])) == lane);
-      }
-      if (seg >= 0 && mv > 0.0 && ((tau >= ex && tau < in) || (last_thread_with_mass && tau >= in))) {
-        double run = ex;
-        int64_t lastmine = -1;
-        auto walk = [&](float w, int64_t i) {
-          if (pick < 0 && sp_keep(w, i, wcut, icut)) {
-            run += double(w);
-            lastmine = i;
-            if (run > tau) pick = i;
-          }
-        };
-        if (seg == 0) {
-          walk(wof(rh), ih);
-        } else if (seg == SEGS - 1) {
-          walk(wof(rt), it);
-        } else {
-          const int k = seg - 1;
-          const int64_t v = g.vec_index(k);
-#pragma unroll
-          for (int kk = 0; kk < rs::MAXV; ++kk)
-            if (kk == k) {
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) walk(wof(ds_vec_elem<T>(buf[kk], e)), g.head + v * EPV + e);
+            for (int e = 0; e < EPV; ++e) {
+              const float w = wof(ds_vec_elem<T>(w4, e));
+              if (sp_keep(w, g.head + v * EPV + e, wcut, icut)) rs::ff_add(lm, w);
             }
+          }
+          const double mv = rs::ff_value(lm);
+          double incl = mv;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += nb;
+          }
+          const double ex = incl - mv;
+          const unsigned withm = __ballot_sync(0xFFFFFFFFu, mv > 0.0);
+          const int lastl = withm ? 31 - __clz(int(withm)) : -1;
+          if (mv > 0.0 && ((tau >= ex && tau < incl) || (lane == lastl && tau >= incl))) {
+            double run = ex;
+            int64_t lastmine = -1;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const int64_t i = g.head + v * EPV + e;
+              const float w = wof(ds_vec_elem<T>(w4, e));
+              if (pick < 0 && sp_keep(w, i, wcut, icut)) {
+                run += double(w);
+                lastmine = i;
+                if (run > tau) pick = i;
+              }
+            }
+            if (pick < 0) pick = lastmine;
+          }
         }
-        if (pick < 0) pick = lastmine;
       }
-    } else if (!a.no_draw && crank == C - 1 && tid == 0 && !(target < wtot)) {
-      pick = last_kept;      // rounding left the target at the very end
-    }
-  }
 
-  // ---- outputs (the thread that picked) ----
-  if (pick >= 0) {
-    int64_t tgt = pick;
-    if (a.d2t) {
-      tgt = pick + a.d2t[pick];
-      if (tgt < 0 || tgt >= a.V_t) {
-        ds_set_error(a.status, DSPARK_ERANGE);
-        tgt = -1;
+      // ---- sparse record: kept tokens in ascending index order with q = w / W_kept ----
+      if (a.q_mode == 1) {
+        // counts per cell (reusing the cell array), then positions by the same contiguous scan
+        __syncthreads();
+        uint32_t kc = 0, kh = 0, kt = 0;
+        sr_pass(g,
+                [&](float raw, int64_t i, int c) {
+                  if (sp_keep(wof(raw), i, wcut, icut)) {
+                    if (c < 0) ++kh;
+                    else if (c >= g.nchunk) ++kt;
+                    else ++kc;
+                  }
+                },
+                [&](int c) {
+                  const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, kc);
+                  if (lane == 0) s_cell[c * SR_WARPS + warp] = double(n);
+                  kc = 0;
+                });
+        const double nh = rs::block_sum(double(kh), bs), nt = rs::block_sum(double(kt), bs);
+        double cmine = 0.0;
+        for (int c = c0; c < c1; ++c) cmine += s_cell[c];
+        double cnt_tot = 0.0;
+        const double cbefore = rs::block_exclusive_scan(cmine, &cnt_tot, bs);
+        const double ntot = nh + cnt_tot + nt;
+        if (ntot > double(a.q.cap)) {
+          if (tid == 0) {
+            a.q.n[qrow] = -1;
+            ds_set_error(a.status, DSPARK_EINVAL);
+          }
+        } else {
+          if (tid == 0) a.q.n[qrow] = int32_t(ntot);
+          // cell bases: each thread rewrites its own cells as exclusive prefixes
+          double acc = nh + cbefore;
+          for (int c = c0; c < c1; ++c) {
+            const double n = s_cell[c];
+            s_cell[c] = acc;
+            acc += n;
+          }
+          __syncthreads();
+          auto emit = [&](float w, int64_t i, int64_t pos) {
+            int64_t tg = i;
+            if (a.d2t) tg = i + a.d2t[i];
+            const int64_t o = qrow * a.q.cap + pos;
+            a.q.ids[o] = int32_t(tg);
+            a.q.p[o] = float(double(w) / wkept);
+          };
+          if (tid == 0) {
+            int64_t pos = 0;
+            for (int64_t i = 0; i < g.head; ++i) {
+              const float w = wof(ds_load_elem<T>(g.row + i));
+              if (sp_keep(w, i, wcut, icut)) emit(w, i, pos++);
+            }
+            pos = int64_t(nh + cnt_tot);
+            for (int64_t i = g.tail0; i < a.V; ++i) {
+              const float w = wof(ds_load_elem<T>(g.row + i));
+              if (sp_keep(w, i, wcut, icut)) emit(w, i, pos++);
+            }
+          }
+          const unsigned below = (1u << lane) - 1u;
+          for (int c = 0; c < g.nchunk; ++c) {
+            const int64_t v = int64_t(c) * SR_THREADS + tid;
+            uint4 w4 = make_uint4(0, 0, 0, 0);
+            if (v < g.nvec) w4 = __ldg(reinterpret_cast<const uint4*>(g.row + g.head) + v);
+            uint32_t mk = 0;
+            if (v < g.nvec) {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e)
+                if (sp_keep(wof(ds_vec_elem<T>(w4, e)), g.head + v * EPV + e, wcut, icut)) mk |= 1u << e;
+            }
+            const uint32_t nk = uint32_t(__popc(mk));
+            uint32_t pre = nk;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, pre, o);
+              if (lane >= o) pre += y;
+            }
+            int64_t pos = int64_t(s_cell[c * SR_WARPS + warp]) + int64_t(pre - nk);
+            (void)below;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+              if (mk & (1u << e)) emit(wof(ds_vec_elem<T>(w4, e)), g.head + v * EPV + e, pos++);
+          }
+        }
       }
     }
-    if (a.out_idx) a.out_idx[row_id * a.out_mul + a.out_add] = int32_t(pick);
-    a.out_tgt[row_id * a.out_mul + a.out_add] = int32_t(tgt);
-    if (a.prev_out) a.prev_out[r] = int32_t(tgt);
-    if (a.q_mode == 1 && greedy) {
-      const int64_t qr = row_id * a.q_row_mul + a.q_row_add;
-      a.q.n[qr] = 1;
-      a.q.ids[qr * a.q.cap] = int32_t(tgt);
-      a.q.p[qr * a.q.cap] = 1.0f;
-    }
-  }
 
-  // ---- proposal record ----
-  const int64_t qrow = row_id * a.q_row_mul + a.q_row_add;
-  if (a.q_mode == 2) {
-    if (crank == 0 && tid == 0) {
+    if (a.amax_out && tid == 0) a.amax_out[row_id] = int32_t(ds_key64_idx(best));
+
+    // ---- outputs (the thread that picked) ----
+    if (pick >= 0) {
+      int64_t tgt = pick;
+      if (a.d2t) {
+        tgt = pick + a.d2t[pick];
+        if (tgt < 0 || tgt >= a.V_t) {
+          ds_set_error(a.status, DSPARK_ERANGE);
+          tgt = -1;
+        }
+      }
+      if (a.out_idx) a.out_idx[row_id * a.out_mul + a.out_add] = int32_t(pick);
+      a.out_tgt[row_id * a.out_mul + a.out_add] = int32_t(tgt);
+      if (a.prev_out) a.prev_out[r] = int32_t(tgt);
+      if (a.q_mode == 1 && greedy) {
+        a.q.n[qrow] = 1;
+        a.q.ids[qrow * a.q.cap] = int32_t(tgt);
+        a.q.p[qrow * a.q.cap] = 1.0f;
+      }
+    }
+    if (a.q_mode == 2 && tid == 0) {
       a.q.zmax[qrow] = zmax;
       a.q.wsum[qrow] = greedy ? 1.0 : wkept;
       a.q.wcut[qrow] = wcut;
       a.q.icut[qrow] = int32_t(icut);
     }
-    if (a.write_z) {
-      float* zr = a.q.z + qrow * a.q.ldz;
-#pragma unroll
-      for (int k = 0; k < rs::MAXV; ++k) {
-        const int64_t v = g.vec_index(k);
-        if (v >= 0) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) zr[g.head + v * EPV + e] = zof(ds_vec_elem<T>(buf[k], e));
-        }
-      }
-      if (g.has_head()) zr[ih] = zof(rh);
-      if (g.has_tail()) zr[it] = zof(rt);
-    }
-  } else if (a.q_mode == 1 && !greedy) {
-    // sparse record: kept tokens in ascending index order with q = w / W_kept
-    auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
-    double cnt_seg[rs::SEGS];
-    double mine = 0.0;
-    cnt_seg[0] = (g.has_head() && sp_keep(wof(rh), ih, wcut, icut)) ? 1.0 : 0.0;
-#pragma unroll
-    for (int k = 0; k < rs::MAXV; ++k) {
-      double c = 0.0;
-      const int64_t v = g.vec_index(k);
-      if (v >= 0) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) c += sp_keep(wof(ds_vec_elem<T>(buf[k], e)), g.head + v * EPV + e, wcut, icut) ? 1.0 : 0.0;
-      }
-      cnt_seg[1 + k] = c;
-    }
-    cnt_seg[SEGS - 1] = (g.has_tail() && sp_keep(wof(rt), it, wcut, icut)) ? 1.0 : 0.0;
-#pragma unroll
-    for (int s = 0; s < SEGS; ++s) mine += cnt_seg[s];
-    const double ccnt = rs::block_sum(mine, bs);
-    double ntot = 0.0;
-    const double cbase = rs::cluster_sum_d(cl, cr, ccnt, 2, &ntot);
-    if (ntot > double(a.q.cap)) {
-      if (crank == 0 && tid == 0) {
-        a.q.n[qrow] = -1;
-        ds_set_error(a.status, DSPARK_EINVAL);
-      }
-    } else {
-      if (crank == 0 && tid == 0) a.q.n[qrow] = int32_t(ntot);
-      double base = cbase;
-#pragma unroll
-      for (int s = 0; s < SEGS; ++s) {
-        double segtot = 0.0;
-        double pos = base + rs::block_exclusive_scan(cnt_seg[s], &segtot, bs);
-        auto emit = [&](float w, int64_t i) {
-          if (sp_keep(w, i, wcut, icut)) {
-            int64_t tg = i;
-            if (a.d2t) tg = i + a.d2t[i];
-            const int64_t o = qrow * a.q.cap + int64_t(pos);
-            a.q.ids[o] = int32_t(tg);
-            a.q.p[o] = float(double(w) / wkept);
-            pos += 1.0;
-          }
-        };
-        if (s == 0) {
-          if (g.has_head()) emit(wof(rh), ih);
-        } else if (s == SEGS - 1) {
-          if (g.has_tail()) emit(wof(rt), it);
-        } else {
-          const int64_t v = g.vec_index(s - 1);
-          if (v >= 0) {
-#pragma unroll
-            for (int kk = 0; kk < rs::MAXV; ++kk)
-              if (kk == s - 1) {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) emit(wof(ds_vec_elem<T>(buf[kk], e)), g.head + v * EPV + e);
-              }
-          }
-        }
-        base += segtot;
-      }
-    }
+    __syncthreads();                                       // the next row reuses the shared arrays
   }
-  cl.sync();
 }
 
 template <typename T, bool XFORM>
 cudaError_t sp_launch(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
-  auto kern = sample_cluster_kernel<T, XFORM>;
-  const size_t smem = sizeof(double) * rs::SEGS * rs::THREADS + sizeof(uint64_t) * SP_CAP;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  auto kern = sample_row_kernel<T, XFORM>;
+  const size_t smem = sizeof(double) * SR_CELLS + sizeof(uint64_t) * SP_CAP;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured_dev = dev;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(rows * a.C), 1, 1);
-  cfg.blockDim = dim3(rs::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(a.C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  const int64_t grid = std::min<int64_t>(rows, int64_t(ds_num_sms()));
+  if (grid <= 0) return cudaSuccess;
+  kern<<<unsigned(grid), SR_THREADS, smem, stream>>>(a, rows);
+  return cudaGetLastError();
 }
 
 }  // namespace

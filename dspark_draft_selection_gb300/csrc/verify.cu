@@ -11,14 +11,15 @@
 // (2023).
 //
 // Three launches:
-//  1. the cluster row sampler of sample.cu in statistics mode over every needed target row:
+//  1. the row sampler of sample.cu in statistics mode over every needed target row:
 //     the maximum, the top-p cut and the kept mass of p_j, the weight of the drafted token x_j,
 //     and the argmax (greedy requests). The target logits are read from HBM once here.
 //  2. verify_accept_kernel - one thread per request runs the sequential tests
 //     u_j < p_j(x_j) / q_j(x_j) and leaves at most one draw job (residual at j*, or bonus at n).
 //  3. verify_draw_kernel - one 1024-thread CTA per request with a job re-reads that one row
-//     (and the dense q row), forms rho = max(0, p - q) (or p) in double and finds the crossing
-//     of u * sum(rho) with per-(round, warp) sums and short scans.
+//     (and the dense q row), forms rho = max(0, p - q) (or p) scaled by W_p * W_q so that no
+//     element needs a division (float pairs per element, double per warp), and finds the
+//     crossing of u * sum(rho) with per-(round, warp) sums and short scans.
 #include "host_common.h"
 #include "rowsample.cuh"
 
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
   __shared__ double s_wtot[VD_WARPS];
   __shared__ int32_t s_sid[VD_SPARSE_MAX];
   __shared__ float s_sq[VD_SPARSE_MAX];
-  __shared__ int s_pick, s_round, s_warp, s_ns;
+  __shared__ int s_pick, s_round, s_warp;
   __shared__ double s_tau;
 
   const int64_t r = blockIdx.x;
@@ -183,20 +184,57 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
     if (wout) *wout = w;
     return vf_keep(w, t, wcut, icut) ? double(w) / wsum : 0.0;
   };
-  auto rho = [&](int64_t t, bool use_q) -> double {
-    const double p = pval(t, nullptr);
-    if (!use_q) return p;
-    double q = 0.0;
+  // Residual masses scaled by W_p * W_q, so that no element needs a division (the draw only
+  // needs the masses up to a common factor): rho'(t) = max(0, w_p(t) W_q - w_q(t) W_p) for a
+  // dense q, max(0, w_p(t) - q(t) W_p) for a sparse q, and w_p(t) when drawing from p. Each is a
+  // float pair (about 48 bits); the double pipe only sees per-warp sums.
+  const double Wq = (resid && a.q_dense) ? a.q.wsum[qrow] : 1.0;
+  const float wp_hi = float(wsum), wp_lo = float(wsum - double(float(wsum)));
+  const float wq_hi = float(Wq), wq_lo = float(Wq - double(float(Wq)));
+  auto ff_mul = [](float x, float dh, float dl) {        // x * (dh + dl) as a float pair
+    const float pr = __fmul_rn(x, dh);
+    return rs::FF{pr, __fadd_rn(__fmaf_rn(x, dh, -pr), __fmul_rn(x, dl))};
+  };
+  auto rho_ff = [&](int64_t t, bool use_q) -> rs::FF {
+    float wp = ds_weight(__fsub_rn(ds_temper(ds_load_elem<T>(row + t), a.T), zmax));
+    if (!vf_keep(wp, t, wcut, icut)) wp = 0.0f;
+    if (!use_q) return rs::FF{wp, 0.0f};
+    rs::FF av, bv;
     if (a.q_dense) {
+      float wq = 0.0f;
       if (t < a.V_q) {
-        const float w = ds_weight(__fsub_rn(a.q.z[qrow * a.q.ldz + t], a.q.zmax[qrow]));
-        q = vf_keep(w, t, a.q.wcut[qrow], a.q.icut[qrow]) ? double(w) / a.q.wsum[qrow] : 0.0;
+        wq = ds_weight(__fsub_rn(a.q.z[qrow * a.q.ldz + t], a.q.zmax[qrow]));
+        if (!vf_keep(wq, t, a.q.wcut[qrow], a.q.icut[qrow])) wq = 0.0f;
       }
+      av = ff_mul(wp, wq_hi, wq_lo);
+      bv = ff_mul(wq, wp_hi, wp_lo);
     } else {
+      float q = 0.0f;
       for (int k = 0; k < ns; ++k)
-        if (s_sid[k] == t) q = double(s_sq[k]);
+        if (s_sid[k] == t) q = s_sq[k];
+      av = rs::FF{wp, 0.0f};
+      bv = ff_mul(q, wp_hi, wp_lo);
     }
-    return fmax(0.0, p - q);
+    // a - b with the rounding error of the leading difference kept (2Sum)
+    const float sd = __fsub_rn(av.hi, bv.hi);
+    const float bb = __fsub_rn(sd, av.hi);
+    const float err = __fadd_rn(__fsub_rn(av.hi, __fsub_rn(sd, bb)), __fsub_rn(-bv.hi, bb));
+    const float lo = __fadd_rn(err, __fsub_rn(av.lo, bv.lo));
+    if (!(__fadd_rn(sd, lo) > 0.0f)) return rs::FF{0.0f, 0.0f};
+    return rs::FF{sd, lo};
+  };
+  auto rho = [&](int64_t t, bool use_q) -> double { return rs::ff_value(rho_ff(t, use_q)); };
+  // sum of a float pair over a warp (float pairs throughout), as a double
+  auto warp_ff_sum = [](rs::FF v) -> double {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+      const float lo = __fadd_rn(v.lo, ol);
+      v.lo = 0.0f;
+      rs::ff_add(v, oh);
+      v.lo = __fadd_rn(v.lo, lo);
+    }
+    return rs::ff_value(v);
   };
 
   const double u = ds_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
@@ -205,8 +243,7 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
     // per-(round, warp) sums in index order
     for (int k = 0; k < nrounds; ++k) {
       const int64_t t = int64_t(k) * VD_THREADS + tid;
-      double v = (t < V) ? rho(t, use_q) : 0.0;
-      v = ds_warp_sum(v);
+      const double v = warp_ff_sum((t < V) ? rho_ff(t, use_q) : rs::FF{0.0f, 0.0f});
       if (lane == 0) s_rw[k * VD_WARPS + warp] = v;
     }
     __syncthreads();
@@ -238,6 +275,8 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
     int kr = -1, kw = -1;
     double tau = 0.0;
     for (int k = 0; k < nrounds && kr < 0; ++k) {
+      const double next = (k + 1 < nrounds) ? s_scan[k + 1] : total;
+      if (!(target < next)) continue;                  // the crossing is in a later round
       double acc = s_scan[k];
       for (int w = 0; w < VD_WARPS; ++w) {
         const double nx = acc + s_rw[k * VD_WARPS + w];
