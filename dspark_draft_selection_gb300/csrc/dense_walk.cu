@@ -173,11 +173,25 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
         float acc[32];
         ds_tmem_ld_32x32b_x32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), acc);
         if (i < a.V) {
+          // the 32 requests' logits first (read-only loads, all in flight together), then z
+          float sv[32];
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const int r = c0 + cc;
+            sv[cc] = 0.0f;
+            if (r < a.R) {
+              if constexpr (sizeof(T) == 2) {
+                sv[cc] = ds_bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(logits + s_lrow[r] * a.ld + i)));
+              } else {
+                sv[cc] = __ldg(reinterpret_cast<const float*>(logits + s_lrow[r] * a.ld + i));
+              }
+            }
+          }
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc) {
             const int r = c0 + cc;
             if (r < a.R) {
-              const float s = dw_xform<XFORM>(ds_load_elem<T>(logits + s_lrow[r] * a.ld + i), a.mult, a.softcap);
+              const float s = dw_xform<XFORM>(sv[cc], a.mult, a.softcap);
               const float v = __fmaf_rn(s_gate[r], acc[cc], s);
               a.z[(int64_t(r) * a.z_row_mul + a.z_row_add) * a.ldz + i] = ds_temper(v, a.Tz);
             }
