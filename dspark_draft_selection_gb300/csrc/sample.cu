@@ -101,8 +101,11 @@ DS_DEV void sr_pass(const SrRow<T>& g, F&& f, FC&& fc) {
   if (tid < g.ntail) f(ds_load_elem<T>(g.row + g.tail0 + tid), g.tail0 + tid, g.nchunk);
 }
 
-template <typename T, bool XFORM>
-__global__ void __launch_bounds__(SR_THREADS, 1) sample_row_kernel(const rs::SampleArgs a, int64_t rows) {
+// NUC: rows may need a top-p nucleus; SPQ: a sparse record is written. The common case (neither)
+// is compiled separately with a register budget for two blocks per SM.
+template <typename T, bool XFORM, bool NUC, bool SPQ>
+__global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
+    sample_row_kernel(const rs::SampleArgs a, int64_t rows) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(16) uint8_t dsm[];
   double* s_cell = reinterpret_cast<double*>(dsm);                        // [SR_CELLS] per-cell sums
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1) sample_row_kernel(const rs::Sam
       auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
 
       // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order ----
-      if (a.top_p < 1.0f) {
+      if (NUC && a.top_p < 1.0f) {
         rs::FF acc{0.0f, 0.0f};
         sr_pass(g, [&](float raw, int64_t, int) { rs::ff_add(acc, wof(raw)); }, [](int) {});
         const double wall = rs::block_sum(rs::ff_value(acc), bs);
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1) sample_row_kernel(const rs::Sam
       }
 
       // ---- sparse record: kept tokens in ascending index order with q = w / W_kept ----
-      if (a.q_mode == 1) {
+      if (SPQ && a.q_mode == 1) {
         // counts per cell (reusing the cell array), then positions by the same contiguous scan
         __syncthreads();
         uint32_t kc = 0, kh = 0, kt = 0;
@@ -505,10 +508,11 @@ __global__ void __launch_bounds__(SR_THREADS, 1) sample_row_kernel(const rs::Sam
   }
 }
 
-template <typename T, bool XFORM>
-cudaError_t sp_launch(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
-  auto kern = sample_row_kernel<T, XFORM>;
-  const size_t smem = sizeof(double) * SR_CELLS + sizeof(uint64_t) * SP_CAP;
+template <typename T, bool XFORM, bool NUC, bool SPQ>
+cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
+  auto kern = sample_row_kernel<T, XFORM, NUC, SPQ>;
+  // the nucleus' candidate keys are only needed with NUC
+  const size_t smem = sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0);
   static int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -518,10 +522,19 @@ cudaError_t sp_launch(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  const int64_t grid = std::min<int64_t>(rows, int64_t(ds_num_sms()));
+  const int per_sm = (NUC || SPQ || XFORM) ? 1 : 2;
+  const int64_t grid = std::min<int64_t>(rows, int64_t(per_sm) * ds_num_sms());
   if (grid <= 0) return cudaSuccess;
   kern<<<unsigned(grid), SR_THREADS, smem, stream>>>(a, rows);
   return cudaGetLastError();
+}
+
+template <typename T, bool XFORM>
+cudaError_t sp_launch(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
+  const bool nuc = a.T > 0.0f && a.top_p < 1.0f;
+  const bool spq = a.q_mode == 1;
+  if (nuc) return spq ? sp_launch_v<T, XFORM, true, true>(a, rows, stream) : sp_launch_v<T, XFORM, true, false>(a, rows, stream);
+  return spq ? sp_launch_v<T, XFORM, false, true>(a, rows, stream) : sp_launch_v<T, XFORM, false, false>(a, rows, stream);
 }
 
 }  // namespace
