@@ -29,6 +29,20 @@ DS_DEV void ff_add(FF& a, float b) {
 }
 DS_DEV double ff_value(const FF& a) { return double(a.hi) + double(a.lo); }
 
+// Sum of a float pair over a warp in float pairs (FP32 shuffles and 2Sum only; every lane gets
+// it). The GPU's FP64 pipe is narrow, so callers convert the result once per warp, not per lane.
+DS_DEV FF warp_ff_reduce(FF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+    const float lo = __fadd_rn(v.lo, ol);
+    v.lo = 0.0f;
+    ff_add(v, oh);
+    v.lo = __fadd_rn(v.lo, lo);
+  }
+  return v;
+}
+
 // 1 when a V-element row is within the sampler's row length, else -1 (the row-length check the
 // entry points make before any launch).
 inline int cluster_size_for(int64_t V, int elem_bytes) {
@@ -38,6 +52,7 @@ inline int cluster_size_for(int64_t V, int elem_bytes) {
 
 // ---- block reductions (all threads call; result valid in every thread) ------------------------
 struct BlockScratch {
+  double tot;
   double d[WARPS];
   float f[WARPS];
   unsigned long long u[WARPS];
@@ -53,6 +68,35 @@ DS_DEV double block_sum(double v, BlockScratch& s) {
   for (int w = 0; w < WARPS; ++w) t += s.d[w];
   return t;
 }
+// Block sum of per-thread float pairs, as a double (warp sums in float pairs, one conversion per
+// warp, the final 16 additions in one thread).
+static __device__ __noinline__ double block_sum_ff(FF v, BlockScratch& s) {
+  v = warp_ff_reduce(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s.d[threadIdx.x >> 5] = ff_value(v);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) t += s.d[w];
+    s.tot = t;
+  }
+  __syncthreads();
+  return s.tot;
+}
+
+// Block sum of per-thread counts (exact in 32 bits).
+DS_DEV uint32_t block_count(uint32_t v, BlockScratch& s) {
+  v = __reduce_add_sync(0xFFFFFFFFu, v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s.u[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) t += uint32_t(s.u[w]);
+  return t;
+}
+
 DS_DEV float block_max(float v, BlockScratch& s) {
   v = ds_warp_max(v);
   __syncthreads();

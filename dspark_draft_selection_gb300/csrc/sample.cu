@@ -18,8 +18,12 @@
 // finds the lane, then the element.
 #include <cfloat>
 
+#include <cooperative_groups.h>
+
 #include "host_common.h"
 #include "rowsample.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -48,12 +52,15 @@ constexpr int SR_WARPS = rs::WARPS;
 constexpr int SR_U = 4;                      // chunks loaded together by a thread (bytes in flight)
 constexpr int SR_MAXCHUNK = 128;             // rows of up to 128 x 512 vectors
 constexpr int SR_CELLS = SR_MAXCHUNK * SR_WARPS;
+constexpr int SR_MAXP = 8;                   // parts (cluster blocks) per row
 
 template <typename T>
 struct SrRow {
   const T* row;
   int64_t head, nvec, tail0, ntail;
   int nchunk;
+  int c_lo, c_hi;                  // this block's chunks (a part of the row when P > 1)
+  bool own_head, own_tail;
 };
 
 template <typename T>
@@ -68,28 +75,75 @@ DS_DEV SrRow<T> sr_row(const T* row, int64_t V) {
   g.tail0 = g.head + g.nvec * EPV;
   g.ntail = V - g.tail0;
   g.nchunk = int((g.nvec + SR_THREADS - 1) / SR_THREADS);
+  g.c_lo = 0;
+  g.c_hi = g.nchunk;
+  g.own_head = g.own_tail = true;
   return g;
+}
+
+// Restricts a row to part p of P (contiguous chunk ranges; the head goes with part 0, the tail
+// with part P - 1).
+template <typename T>
+DS_DEV void sr_part(SrRow<T>& g, int p, int P) {
+  const int per = (g.nchunk + P - 1) / P;
+  g.c_lo = min(g.nchunk, p * per);
+  g.c_hi = min(g.nchunk, g.c_lo + per);
+  g.own_head = p == 0;
+  g.own_tail = p == P - 1;
 }
 
 // Calls f(raw value, index, chunk) for every element this thread holds (head elements with chunk
 // -1, tail elements with chunk nchunk), and fc(chunk) after each chunk, with every thread of the
 // block taking part (fc may use warp collectives). SR_U chunks are loaded at a time.
+// Exclusive prefix (thread order) of per-thread doubles and their total: staged in shared memory and
+// scanned by warp 0 alone (16 values per lane), so the narrow FP64 pipe sees a few hundred adds.
+__device__ __noinline__ double sr_prefix(double v, double* total, double* s_run) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  s_run[tid] = v;
+  __syncthreads();
+  if (tid < 32) {
+    constexpr int PER = SR_THREADS / 32;
+    double loc = 0.0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) loc += s_run[lane * PER + q];
+    double incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += nb;
+    }
+    double run = incl - loc;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const double x = s_run[lane * PER + q];
+      s_run[lane * PER + q] = run;
+      run += x;
+    }
+    if (lane == 31) s_run[SR_THREADS] = incl;
+  }
+  __syncthreads();
+  *total = s_run[SR_THREADS];
+  const double r = s_run[tid];
+  __syncthreads();                                        // s_run is reused by the next call
+  return r;
+}
+
 template <typename T, typename F, typename FC>
 DS_DEV void sr_pass(const SrRow<T>& g, F&& f, FC&& fc) {
   constexpr int EPV = 16 / sizeof(T);
   const int tid = threadIdx.x;
-  if (tid < g.head) f(ds_load_elem<T>(g.row + tid), int64_t(tid), -1);
+  if (g.own_head && tid < g.head) f(ds_load_elem<T>(g.row + tid), int64_t(tid), -1);
   const uint4* vp = reinterpret_cast<const uint4*>(g.row + g.head);
-  for (int c0 = 0; c0 < g.nchunk; c0 += SR_U) {
+  for (int c0 = g.c_lo; c0 < g.c_hi; c0 += SR_U) {
     uint4 buf[SR_U];
 #pragma unroll
     for (int u = 0; u < SR_U; ++u) {
       const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
-      if (c0 + u < g.nchunk && v < g.nvec) buf[u] = __ldg(vp + v);
+      if (c0 + u < g.c_hi && v < g.nvec) buf[u] = __ldg(vp + v);
     }
 #pragma unroll
     for (int u = 0; u < SR_U; ++u) {
-      if (c0 + u >= g.nchunk) break;
+      if (c0 + u >= g.c_hi) break;
       const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
       if (v < g.nvec) {
 #pragma unroll
@@ -98,7 +152,7 @@ DS_DEV void sr_pass(const SrRow<T>& g, F&& f, FC&& fc) {
       fc(c0 + u);
     }
   }
-  if (tid < g.ntail) f(ds_load_elem<T>(g.row + g.tail0 + tid), g.tail0 + tid, g.nchunk);
+  if (g.own_tail && tid < g.ntail) f(ds_load_elem<T>(g.row + g.tail0 + tid), g.tail0 + tid, g.nchunk);
 }
 
 // NUC: rows may need a top-p nucleus; SPQ: a sparse record is written. The common case (neither)
@@ -114,35 +168,64 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
   __shared__ uint32_t s_cnt;
   __shared__ int s_cellpick;
   __shared__ double s_tau, s_cut[2];
-
+  // exchange slots of the row's parts (a cluster of P blocks), one per part
+  __shared__ float s_xf[SR_MAXP];
+  __shared__ unsigned long long s_xu[SR_MAXP], s_xl[SR_MAXP];
+  __shared__ double s_xd[SR_MAXP];
+  __shared__ double s_run[SR_THREADS + 1];
+  cg::cluster_group cl = cg::this_cluster();
+  const int P = int(cl.num_blocks()), part = int(cl.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool greedy = !(a.T > 0.0f);
   const float Tz = greedy ? 1.0f : a.T;
   auto zof = [&](float raw) { return ds_temper(sp_xform<XFORM>(raw, a.mult, a.softcap), Tz); };
 
-  for (int64_t row_id = blockIdx.x; row_id < rows; row_id += gridDim.x) {
+  for (int64_t row_id = blockIdx.x / P; row_id < rows; row_id += gridDim.x / P) {
     const int64_t r = row_id / a.B, j = row_id % a.B;
-    if (a.n_draft && j > a.n_draft[r]) continue;          // the whole block skips the row
+    if (a.n_draft && j > a.n_draft[r]) continue;          // every part of the row skips it
     const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
-    const SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
+    SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
+    if (P > 1) sr_part(g, part, P);
     const int64_t qrow = row_id * a.q_row_mul + a.q_row_add;
     float* zr = (a.q_mode == 2 && a.write_z) ? a.q.z + qrow * a.q.ldz : nullptr;
-    const int ncells = g.nchunk * SR_WARPS;
+    const int ncells = (g.c_hi - g.c_lo) * SR_WARPS;      // this block's cells
 
     // ---- pass 1: maximum of z and the argmax key (lowest index on ties); the z row of a dense
     // record is written on the way ----
     float tmax = -INFINITY;
     unsigned long long best = 0;
-    const bool want_key = greedy || a.amax_out != nullptr;
-    sr_pass(g,
-            [&](float raw, int64_t i, int) {
-              const float z = zof(raw);
-              tmax = fmaxf(tmax, z);
-              if (want_key) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(z), uint32_t(i)));
-              if (zr) zr[i] = z;
-            },
-            [](int) {});
+    // the argmax key per element only when greedy; a sampled row finds its argmax (lowest index
+    // with z == zmax) in the kept-mass pass
+    const bool want_key = greedy;
+    if (!want_key && zr == nullptr) {
+      // the common case: the maximum only
+      sr_pass(g, [&](float raw, int64_t, int) { tmax = fmaxf(tmax, zof(raw)); }, [](int) {});
+    } else {
+      sr_pass(g,
+              [&](float raw, int64_t i, int) {
+                const float z = zof(raw);
+                tmax = fmaxf(tmax, z);
+                if (want_key) best = max(best, (unsigned long long)ds_key64(ds_canon_zero(z), uint32_t(i)));
+                if (zr) zr[i] = z;
+              },
+              [](int) {});
+    }
     if (want_key) best = rs::block_max_u64(best, bs);
+    if (P > 1) {
+      // the parts' maxima: every block posts into slot `part` of every block, then reads them
+      const float bt = rs::block_max(tmax, bs);
+      if (tid < P) {
+        *cl.map_shared_rank(&s_xf[part], tid) = bt;
+        *cl.map_shared_rank(&s_xu[part], tid) = best;
+      }
+      cl.sync();
+      tmax = -INFINITY;
+      best = 0;
+      for (int q = 0; q < P; ++q) {
+        tmax = fmaxf(tmax, s_xf[q]);
+        best = max(best, s_xu[q]);
+      }
+    }
 
     int64_t pick = -1;
     float zmax, wcut = 0.0f;
@@ -152,7 +235,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       zmax = ds_key64_val(best);
       wcut = 1.0f;
       icut = ds_key64_idx(best);
-      if (tid == 0) pick = icut;
+      if (tid == 0 && part == 0) pick = icut;
     } else {
       zmax = rs::block_max(tmax, bs);
       if (!(zmax > -INFINITY && zmax < INFINITY)) {
@@ -163,6 +246,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
           if (a.prev_out) a.prev_out[r] = -1;
         }
         __syncthreads();
+        if (P > 1) cl.sync();                              // every part takes this branch
         continue;
       }
       auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
@@ -171,7 +255,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       if (NUC && a.top_p < 1.0f) {
         rs::FF acc{0.0f, 0.0f};
         sr_pass(g, [&](float raw, int64_t, int) { rs::ff_add(acc, wof(raw)); }, [](int) {});
-        const double wall = rs::block_sum(rs::ff_value(acc), bs);
+        const double wall = rs::block_sum_ff(acc, bs);
         const double tp = double(a.top_p);
         for (int round = 0; round < 4; ++round) {
           const float tau = round == 0 ? ds_weight(-10.0f) : round == 1 ? ds_weight(-20.0f)
@@ -187,7 +271,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
                     }
                   },
                   [](int) {});
-          const double mass = rs::block_sum(rs::ff_value(m), bs);
+          const double mass = rs::block_sum_ff(m, bs);
           const double ncand = rs::block_sum(cnt, bs);
           if (round < 3 && !(mass / wall > tp + 1e-12)) continue;
           if (ncand <= double(SP_CAP)) {
@@ -236,7 +320,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
                         if ((unsigned long long)ds_key64(w, uint32_t(i)) >= cand) rs::ff_add(mm, w);
                       },
                       [](int) {});
-              const double mb = rs::block_sum(rs::ff_value(mm), bs);
+              const double mb = rs::block_sum_ff(mm, bs);
               if (mb / wall > tp) res = cand;
             }
             if (tid == 0) {
@@ -251,38 +335,82 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         icut = int64_t(s_cut[1]);
       }
 
-      // ---- pass: kept mass per cell (float pairs per thread, double per warp), head, tail and
-      // the last kept index ----
-      rs::FF m{0.0f, 0.0f}, mh{0.0f, 0.0f}, mt{0.0f, 0.0f};
-      unsigned long long lastk = 0;
-      sr_pass(g,
-              [&](float raw, int64_t i, int c) {
-                const float w = wof(raw);
-                if (sp_keep(w, i, wcut, icut)) {
-                  if (c < 0) rs::ff_add(mh, w);
-                  else if (c >= g.nchunk) rs::ff_add(mt, w);
-                  else rs::ff_add(m, w);
-                  lastk = max(lastk, (unsigned long long)(i + 1));
-                }
-              },
-              [&](int c) {
-                const double cw = ds_warp_sum(rs::ff_value(m));
-                if (lane == 0) s_cell[c * SR_WARPS + warp] = cw;
-                m = rs::FF{0.0f, 0.0f};
-              });
-      const double Hm = rs::block_sum(rs::ff_value(mh), bs);    // (also orders the cell writes)
-      const double Tm = rs::block_sum(rs::ff_value(mt), bs);
-      const int64_t last_kept = int64_t(rs::block_max_u64(lastk, bs)) - 1;
+      // ---- pass: kept mass per cell (float pairs per thread, double per warp), head and tail.
+      // Without a nucleus every positive weight is kept ----
+      auto keep = [&](float w, int64_t i) { return NUC ? sp_keep(w, i, wcut, icut) : (w > 0.0f); };
+      rs::FF mh{0.0f, 0.0f}, mt{0.0f, 0.0f};
+      const bool want_amax = a.amax_out != nullptr;
+      uint32_t amin = 0xFFFFFFFFu;                         // lowest index with z == zmax
+      if (g.own_head && tid < g.head) {
+        const float z = zof(ds_load_elem<T>(g.row + tid)), w = ds_weight(__fsub_rn(z, zmax));
+        if (keep(w, tid)) rs::ff_add(mh, w);
+        if (z == zmax) amin = min(amin, uint32_t(tid));
+      }
+      if (g.own_tail && tid < g.ntail) {
+        const float z = zof(ds_load_elem<T>(g.row + g.tail0 + tid)), w = ds_weight(__fsub_rn(z, zmax));
+        if (keep(w, g.tail0 + tid)) rs::ff_add(mt, w);
+        if (z == zmax) amin = min(amin, uint32_t(g.tail0 + tid));
+      }
+      {
+        const uint4* vp = reinterpret_cast<const uint4*>(g.row + g.head);
+        for (int cb = g.c_lo; cb < g.c_hi; cb += SR_U) {
+          uint4 buf[SR_U];
+#pragma unroll
+          for (int u = 0; u < SR_U; ++u) {
+            const int64_t v = int64_t(cb + u) * SR_THREADS + tid;
+            if (cb + u < g.c_hi && v < g.nvec) buf[u] = __ldg(vp + v);
+          }
+#pragma unroll
+          for (int u = 0; u < SR_U; ++u) {
+            if (cb + u >= g.c_hi) break;
+            const int64_t v = int64_t(cb + u) * SR_THREADS + tid;
+            rs::FF m{0.0f, 0.0f};
+            if (v < g.nvec) {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) {
+                const float z = zof(ds_vec_elem<T>(buf[u], e)), w = ds_weight(__fsub_rn(z, zmax));
+                if (keep(w, g.head + v * EPV + e)) rs::ff_add(m, w);
+                if (want_amax && z == zmax) amin = min(amin, uint32_t(g.head + v * EPV + e));
+              }
+            }
+            const rs::FF cw = rs::warp_ff_reduce(m);
+            if (lane == 0) s_cell[(cb + u - g.c_lo) * SR_WARPS + warp] = rs::ff_value(cw);
+          }
+        }
+      }
+      const double Hm = rs::block_sum_ff(mh, bs);              // (also orders the cell writes)
+      const double Tm = rs::block_sum_ff(mt, bs);
+      if (want_amax) {
+        // the row's argmax: the lowest index of weight 1 over the block, then over the parts
+        best = ~rs::block_max_u64(~(unsigned long long)amin, bs);   // minimum via max of the complement
+        if (P > 1) {
+          if (tid < P) *cl.map_shared_rank(&s_xu[part], tid) = best;
+          cl.sync();
+          for (int q = 0; q < P; ++q) best = min(best, s_xu[q]);
+        }
+      }
       // cells: each thread owns a contiguous run of cells; exclusive prefix over threads
       const int per = (ncells + SR_THREADS - 1) / SR_THREADS;
       const int c0 = tid * per, c1 = min(ncells, c0 + per);
       double mine = 0.0;
       for (int c = c0; c < c1; ++c) mine += s_cell[c];
       double ctot = 0.0;
-      const double before = rs::block_exclusive_scan(mine, &ctot, bs);
-      wkept = Hm + ctot + Tm;
+      const double before = sr_prefix(mine, &ctot, s_run);
+      // this part's mass, the parts before it and the row's total (one exchange when P > 1)
+      const double ptot = Hm + ctot + Tm;
+      double pbase = 0.0;
+      wkept = ptot;
+      if (P > 1) {
+        if (tid < P) *cl.map_shared_rank(&s_xd[part], tid) = ptot;
+        cl.sync();
+        wkept = 0.0;
+        for (int q = 0; q < P; ++q) {
+          if (q < part) pbase += s_xd[q];
+          wkept += s_xd[q];
+        }
+      }
 
-      if (a.probe_w) {
+      if (a.probe_w && part == 0) {
         const int64_t x = (a.probe_tgt && j < a.n_draft[r]) ? int64_t(a.probe_tgt[r * (a.B - 1) + j]) : -1;
         if (tid == 0) {
           float pw = 0.0f;
@@ -298,13 +426,18 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       if (!a.no_draw) {
         const double u = ds_uniform(a.seed[r], a.step[r], uint32_t(a.position >= 0 ? a.position : int32_t(j)),
                                     DS_PURPOSE_DRAFT);
-        const double target = u * wkept;
-        if (tid == 0) s_cellpick = -3;                        // -3 none, -1 head, -2 tail
+        const double gtarget = u * wkept;
+        // the part whose mass holds the target works in its own frame; past the total (rounding)
+        // the last part takes the last kept index
+        const bool mine_p = (gtarget >= pbase && gtarget < pbase + ptot) || (part == P - 1 && gtarget >= wkept);
+        const double target = gtarget - pbase;
+        if (tid == 0) s_cellpick = mine_p ? -3 : -5;          // -5 another part, -3 none, -1 head, -2 tail
         __syncthreads();
-        if (target < Hm) {
+        if (!mine_p) {
+        } else if (target < Hm) {
           if (tid == 0) s_cellpick = -1;
         } else if (target >= Hm + ctot) {
-          if (tid == 0) s_cellpick = (target < wkept) ? -2 : -4;   // -4: rounding left it past the end
+          if (tid == 0) s_cellpick = (target < ptot) ? -2 : -4;    // -4: rounding left it past the end
         } else {
           const double t_in = target - Hm;
           if (t_in >= before && t_in < before + mine) {
@@ -333,7 +466,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         if (cp == -1 || cp == -2) {
           // the few scalar head or tail elements, walked by one thread
           if (tid == 0) {
-            double run = (cp == -1) ? 0.0 : Hm + ctot;
+            double run = (cp == -1) ? 0.0 : Hm + ctot;        // in this part's frame, as `target`
             const int64_t i0 = (cp == -1) ? 0 : g.tail0, i1 = (cp == -1) ? g.head : a.V;
             int64_t lastmine = -1;
             for (int64_t i = i0; i < i1 && pick < 0; ++i) {
@@ -347,10 +480,15 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
             if (pick < 0) pick = lastmine;
           }
         } else if (cp == -4 || cp == -3) {
-          if (tid == 0) pick = last_kept;                     // rounding left the target at the very end
-        } else if (warp == cp % SR_WARPS) {
+          // rounding left the target at the very end: the last kept index of the row (this is the
+          // last part), found by a backward scan
+          if (tid == 0) {
+            for (int64_t i = a.V - 1; i >= 0 && pick < 0; --i)
+              if (keep(wof(ds_load_elem<T>(g.row + i)), i)) pick = i;
+          }
+        } else if (cp >= 0 && warp == cp % SR_WARPS) {
           // the crossing cell: its warp re-reads its 32 vectors and finds the lane, then the element
-          const int c = cp / SR_WARPS;
+          const int c = g.c_lo + cp / SR_WARPS;
           const double tau = s_tau;
           const int64_t v = int64_t(c) * SR_THREADS + tid;
           uint4 w4 = make_uint4(0, 0, 0, 0);
@@ -409,11 +547,11 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
                   if (lane == 0) s_cell[c * SR_WARPS + warp] = double(n);
                   kc = 0;
                 });
-        const double nh = rs::block_sum(double(kh), bs), nt = rs::block_sum(double(kt), bs);
+        const double nh = double(rs::block_count(kh, bs)), nt = double(rs::block_count(kt, bs));
         double cmine = 0.0;
         for (int c = c0; c < c1; ++c) cmine += s_cell[c];
         double cnt_tot = 0.0;
-        const double cbefore = rs::block_exclusive_scan(cmine, &cnt_tot, bs);
+        const double cbefore = sr_prefix(cmine, &cnt_tot, s_run);
         const double ntot = nh + cnt_tot + nt;
         if (ntot > double(a.q.cap)) {
           if (tid == 0) {
@@ -477,7 +615,8 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       }
     }
 
-    if (a.amax_out && tid == 0) a.amax_out[row_id] = int32_t(ds_key64_idx(best));
+    if (a.amax_out && tid == 0 && part == 0)
+      a.amax_out[row_id] = greedy ? int32_t(ds_key64_idx(best)) : int32_t(best);
 
     // ---- outputs (the thread that picked) ----
     if (pick >= 0) {
@@ -498,13 +637,14 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         a.q.p[qrow * a.q.cap] = 1.0f;
       }
     }
-    if (a.q_mode == 2 && tid == 0) {
+    if (a.q_mode == 2 && tid == 0 && part == 0) {
       a.q.zmax[qrow] = zmax;
       a.q.wsum[qrow] = greedy ? 1.0 : wkept;
       a.q.wcut[qrow] = wcut;
       a.q.icut[qrow] = int32_t(icut);
     }
     __syncthreads();                                       // the next row reuses the shared arrays
+    if (P > 1) cl.sync();                                  // ... and the other parts' slots
   }
 }
 
@@ -523,10 +663,33 @@ cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stre
     configured_dev = dev;
   }
   const int per_sm = (NUC || SPQ || XFORM) ? 1 : 2;
-  const int64_t grid = std::min<int64_t>(rows, int64_t(per_sm) * ds_num_sms());
-  if (grid <= 0) return cudaSuccess;
-  kern<<<unsigned(grid), SR_THREADS, smem, stream>>>(a, rows);
-  return cudaGetLastError();
+  const int64_t slots = int64_t(per_sm) * ds_num_sms();
+  if (rows <= 0) return cudaSuccess;
+  // few rows: split each row over P blocks of a cluster so that every SM streams (common case only)
+  int P = 1;
+  if (!NUC && !SPQ) {
+    const int64_t nchunk = (a.V * int64_t(sizeof(T)) / 16 + SR_THREADS) / SR_THREADS;
+    while (P < SR_MAXP && rows * (2 * P) <= slots && nchunk >= int64_t(4 * 2 * P)) P *= 2;
+  }
+  if (P == 1) {
+    const int64_t grid = std::min<int64_t>(rows, slots);
+    kern<<<unsigned(grid), SR_THREADS, smem, stream>>>(a, rows);
+    return cudaGetLastError();
+  }
+  const int64_t grid = std::min<int64_t>(rows, slots / P) * P;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(SR_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(P);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, rows);
 }
 
 template <typename T, bool XFORM>

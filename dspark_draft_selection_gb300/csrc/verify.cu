@@ -224,27 +224,26 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
     return rs::FF{sd, lo};
   };
   auto rho = [&](int64_t t, bool use_q) -> double { return rs::ff_value(rho_ff(t, use_q)); };
-  // sum of a float pair over a warp (float pairs throughout), as a double
-  auto warp_ff_sum = [](rs::FF v) -> double {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o), ol = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-      const float lo = __fadd_rn(v.lo, ol);
-      v.lo = 0.0f;
-      rs::ff_add(v, oh);
-      v.lo = __fadd_rn(v.lo, lo);
-    }
-    return rs::ff_value(v);
-  };
 
   const double u = ds_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
   bool use_q = resid;
   for (int attempt = 0; attempt < 2; ++attempt) {
     // per-(round, warp) sums in index order
-    for (int k = 0; k < nrounds; ++k) {
-      const int64_t t = int64_t(k) * VD_THREADS + tid;
-      const double v = warp_ff_sum((t < V) ? rho_ff(t, use_q) : rs::FF{0.0f, 0.0f});
-      if (lane == 0) s_rw[k * VD_WARPS + warp] = v;
+    // four rounds at a time: their masses are formed first (all loads in flight together), then
+    // summed per warp
+    for (int k0 = 0; k0 < nrounds; k0 += 4) {
+      rs::FF f[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t t = int64_t(k0 + u) * VD_THREADS + tid;
+        f[u] = (k0 + u < nrounds && t < V) ? rho_ff(t, use_q) : rs::FF{0.0f, 0.0f};
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (k0 + u >= nrounds) break;
+        const rs::FF v = rs::warp_ff_reduce(f[u]);
+        if (lane == 0) s_rw[(k0 + u) * VD_WARPS + warp] = rs::ff_value(v);
+      }
     }
     __syncthreads();
     // round totals and their running sums (sequential in one warp per 32 rounds)
