@@ -162,7 +162,10 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
     sample_row_kernel(const rs::SampleArgs a, int64_t rows) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(16) uint8_t dsm[];
-  double* s_cell = reinterpret_cast<double*>(dsm);                        // [SR_CELLS] per-cell sums
+  double* s_cell = reinterpret_cast<double*>(dsm);                        // [SR_CELLS] per-cell values
+  float2* s_cellf = reinterpret_cast<float2*>(dsm);                       // ... as float pairs
+  // per-cell counts of a sparse record, after the nucleus keys
+  uint32_t* s_cnt32 = reinterpret_cast<uint32_t*>(dsm + sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0));
   uint64_t* s_keys = reinterpret_cast<uint64_t*>(dsm + sizeof(double) * SR_CELLS);   // [SP_CAP]
   __shared__ rs::BlockScratch bs;
   __shared__ uint32_t s_cnt;
@@ -373,8 +376,8 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
                 if (want_amax && z == zmax) amin = min(amin, uint32_t(g.head + v * EPV + e));
               }
             }
-            const rs::FF cw = rs::warp_ff_reduce(m);
-            if (lane == 0) s_cell[(cb + u - g.c_lo) * SR_WARPS + warp] = rs::ff_value(cw);
+            const rs::FF cw = rs::warp_ff_reduce(m);              // kept as a float pair: the
+            if (lane == 0) s_cellf[(cb + u - g.c_lo) * SR_WARPS + warp] = make_float2(cw.hi, cw.lo);
           }
         }
       }
@@ -392,8 +395,17 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       // cells: each thread owns a contiguous run of cells; exclusive prefix over threads
       const int per = (ncells + SR_THREADS - 1) / SR_THREADS;
       const int c0 = tid * per, c1 = min(ncells, c0 + per);
-      double mine = 0.0;
-      for (int c = c0; c < c1; ++c) mine += s_cell[c];
+      // (FP64 pipe costs a warp instruction per use whatever the active lanes: one conversion
+      // per thread here, not one per warp and cell)
+      rs::FF mf{0.0f, 0.0f};
+      for (int c = c0; c < c1; ++c) {
+        const float2 cv = s_cellf[c];
+        const float lo = __fadd_rn(mf.lo, cv.y);
+        mf.lo = 0.0f;
+        rs::ff_add(mf, cv.x);
+        mf.lo = __fadd_rn(mf.lo, lo);
+      }
+      const double mine = rs::ff_value(mf);
       double ctot = 0.0;
       const double before = sr_prefix(mine, &ctot, s_run);
       // this part's mass, the parts before it and the row's total (one exchange when P > 1)
@@ -444,15 +456,16 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
             double acc = before;
             int found = -1;
             for (int c = c0; c < c1; ++c) {
-              if (found < 0 && t_in < acc + s_cell[c] && s_cell[c] > 0.0) {
+              const double cv = double(s_cellf[c].x) + double(s_cellf[c].y);
+              if (found < 0 && t_in < acc + cv && cv > 0.0) {
                 found = c;
                 s_tau = t_in - acc;
               }
-              acc += s_cell[c];
+              acc += cv;
             }
             if (found < 0) {                                  // rounding: the last cell with mass
               for (int c = c1 - 1; c >= c0; --c)
-                if (s_cell[c] > 0.0) {
+                if (double(s_cellf[c].x) + double(s_cellf[c].y) > 0.0) {
                   found = c;
                   s_tau = INFINITY;
                   break;
@@ -544,12 +557,12 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
                 },
                 [&](int c) {
                   const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, kc);
-                  if (lane == 0) s_cell[c * SR_WARPS + warp] = double(n);
+                  if (lane == 0) s_cnt32[c * SR_WARPS + warp] = n;
                   kc = 0;
                 });
         const double nh = double(rs::block_count(kh, bs)), nt = double(rs::block_count(kt, bs));
         double cmine = 0.0;
-        for (int c = c0; c < c1; ++c) cmine += s_cell[c];
+        for (int c = c0; c < c1; ++c) cmine += double(s_cnt32[c]);
         double cnt_tot = 0.0;
         const double cbefore = sr_prefix(cmine, &cnt_tot, s_run);
         const double ntot = nh + cnt_tot + nt;
@@ -563,8 +576,8 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
           // cell bases: each thread rewrites its own cells as exclusive prefixes
           double acc = nh + cbefore;
           for (int c = c0; c < c1; ++c) {
-            const double n = s_cell[c];
-            s_cell[c] = acc;
+            const double n = double(s_cnt32[c]);
+            s_cell[c] = acc;                                  // the cell's first output position
             acc += n;
           }
           __syncthreads();
@@ -652,7 +665,8 @@ template <typename T, bool XFORM, bool NUC, bool SPQ>
 cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
   auto kern = sample_row_kernel<T, XFORM, NUC, SPQ>;
   // the nucleus' candidate keys are only needed with NUC
-  const size_t smem = sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0);
+  const size_t smem = sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0) +
+                      (SPQ ? sizeof(uint32_t) * SR_CELLS : 0);
   static int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

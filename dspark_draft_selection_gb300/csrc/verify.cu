@@ -144,7 +144,7 @@ __global__ void verify_accept_kernel(const VerifyArgs a, int64_t R) {
 
 template <typename T>
 __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const VerifyArgs a) {
-  extern __shared__ __align__(16) double s_rw[];          // [rounds][VD_WARPS]
+  extern __shared__ __align__(16) float2 s_rwf[];         // [rounds][VD_WARPS] float pairs
   __shared__ double s_scan[VD_MAXROUNDS];
   __shared__ double s_wtot[VD_WARPS];
   __shared__ int32_t s_sid[VD_SPARSE_MAX];
@@ -241,16 +241,22 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (k0 + u >= nrounds) break;
-        const rs::FF v = rs::warp_ff_reduce(f[u]);
-        if (lane == 0) s_rw[(k0 + u) * VD_WARPS + warp] = rs::ff_value(v);
+        const rs::FF v = rs::warp_ff_reduce(f[u]);          // kept as a float pair (no FP64 here)
+        if (lane == 0) s_rwf[(k0 + u) * VD_WARPS + warp] = make_float2(v.hi, v.lo);
       }
     }
     __syncthreads();
-    // round totals and their running sums (sequential in one warp per 32 rounds)
+    // round totals in float pairs, one double per round, and their running sums
     for (int k = tid; k < nrounds; k += VD_THREADS) {
-      double sum = 0.0;
-      for (int w = 0; w < VD_WARPS; ++w) sum += s_rw[k * VD_WARPS + w];
-      s_scan[k] = sum;
+      rs::FF sum{0.0f, 0.0f};
+      for (int w = 0; w < VD_WARPS; ++w) {
+        const float2 c = s_rwf[k * VD_WARPS + w];
+        const float lo = __fadd_rn(sum.lo, c.y);
+        sum.lo = 0.0f;
+        rs::ff_add(sum, c.x);
+        sum.lo = __fadd_rn(sum.lo, lo);
+      }
+      s_scan[k] = rs::ff_value(sum);
     }
     __syncthreads();
     if (tid == 0) {
@@ -278,8 +284,9 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const Verify
       if (!(target < next)) continue;                  // the crossing is in a later round
       double acc = s_scan[k];
       for (int w = 0; w < VD_WARPS; ++w) {
-        const double nx = acc + s_rw[k * VD_WARPS + w];
-        if (target < nx && s_rw[k * VD_WARPS + w] > 0.0) {
+        const double cw = double(s_rwf[k * VD_WARPS + w].x) + double(s_rwf[k * VD_WARPS + w].y);
+        const double nx = acc + cw;
+        if (target < nx && cw > 0.0) {
           kr = k;
           kw = w;
           tau = target - acc;
