@@ -244,14 +244,15 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
               }
             }
           }
-          // sorted position i = lane + 32h: mass w / wall, running sums over positions 0..63
+          // sorted position i = lane + 32h: running weight sums over positions 0..63, compared
+          // with top_p * W (no division per candidate on the narrow FP64 pipe)
           double pw[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? double(ds_key64_val(x[h])) / wall : 0.0;
+          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? double(ds_key64_val(x[h])) : 0.0;
           const double inc0 = ch_warp_scan(pw[0]);
           const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
           const double inc1 = tot0 + ch_warp_scan(pw[1]);
-          const double tp = double(a.top_p);
+          const double tp = double(a.top_p) * wall;
           const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && inc0 > tp && pw[0] > 0.0);
           const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && inc1 > tp && pw[1] > 0.0);
           if (b0 | b1) {
