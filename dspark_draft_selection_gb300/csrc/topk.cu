@@ -8,27 +8,23 @@
 // draft vocabulary (target id i + d2t[i]). optimum-intel PR #2098 runs this selection with the
 // OpenVINO GPU plugin's radix TopK; this kernel is a different, exact design for sm_103a.
 //
-// Design: persistent CTAs (two per SM) each take whole rows, streaming a row in chunks of up to
-// 42 KB through a 2-stage shared-memory ring filled by bulk asynchronous copies (cp.async.bulk +
-// mbarrier transaction counts); the ring runs on across rows, so HBM keeps streaming while a
-// chunk is screened. The logits are read once and no other CTA is involved in a row.
-// Per row the CTA keeps the exact top-K' keys seen so far (64-bit keys: value, then lower index
-// first), sorted, in shared memory, and a bound B that K' elements already seen reach:
-//  1. Chunk 0: each warp takes the m-th largest of its lanes' maxima (m = ceil(K'/8), warp REDUX
-//     rounds); every lane maximum is a distinct element, so 8 warps x m >= K' elements are >= the
-//     minimum T over the warps. Elements >= T survive (a few K'); B = T.
-//  2. Later chunks: every element of the chunk comes after the K' elements behind B, so an equal
-//     value loses on the index and only values strictly above B can enter: one packed compare
-//     of each vector's maximum, survivors rare and never a flood of ties.
-//  3. Screening is one sweep without side effects that marks the vectors holding a survivor;
-//     the marked vectors are then taken apart by the whole warp (8-bit masks from packed
-//     compares, one survivor per lane per pass, one shared-memory atomic per pass).
-//  4. Once 2K' survivors have gathered (and at the row's end) they merge into the running list:
-//     a key's position is the number of keys above it in both lists; the list keeps its first
-//     K' entries and B rises to its K'-th value.
-//  5. A chunk whose survivors overflow the buffer (ties in chunk 0, or a rising row) is first cut
-//     to its own exact top-K' by a bisection over its keys in shared memory.
-// After the last chunk the list is the row's top-K', written in order with the d2t map.
+// Design: one CTA of 512 threads per row, persistent over rows (two CTAs per SM). Thread t owns
+// the row's 16-byte vectors t, t + 512, t + 1024, ..., so each batch of the CTA is one contiguous
+// stretch of the row and every load is coalesced. The logits go from HBM to registers once;
+// nothing is staged in shared memory and no barrier falls inside the stream.
+//  1. Stream: each thread loads its vectors in batches of 8 and keeps the keys (vector maximum,
+//     vector number) of its 4 largest vectors, sorted, with a branch-free min/max network.
+//  2. Bound: each warp pops its m largest tracked maxima (warp REDUX rounds). They are maxima of
+//     distinct vectors, so once the pops add up to K' there are K' distinct elements at or above
+//     T, the smallest warp's last pop, and every top-K' element is >= T.
+//  3. Gather: only a vector whose maximum reaches T can hold an element >= T. A thread whose
+//     fourth tracked maximum is below T knows all its other vectors are below T and re-reads only
+//     its tracked vectors that reach T (from L2); otherwise it re-reads all of its vectors.
+//     Elements >= T go to a shared list (about 2K' on Gaussian rows).
+//  4. Select: a listed key's rank is the number of listed keys above it (64-bit keys: value, then
+//     lower index first); the first K' ranks are written in order with the d2t map.
+//  5. A list that overflows its 2048 slots (ties at T, as in a constant row) is cut exactly by a
+//     bisection over the 64 key bits, counting the whole row once per bit.
 #include <type_traits>
 
 #include "dspark_common.cuh"
@@ -36,13 +32,13 @@
 
 namespace {
 
-constexpr int TK_THREADS = 256;
+constexpr int TK_THREADS = 512;
 constexpr int TK_WARPS = TK_THREADS / 32;
-constexpr int TK_STAGES = 2;
-constexpr int TK_STAGE_VEC = 2688;      // 16-byte vectors per chunk (42 KB)
-constexpr int TK_NEW_CAP = 1024;        // survivors of one chunk before the exact cut
+constexpr int TK_TRACK = 6;             // largest vectors remembered per thread
+constexpr int TK_CAP = 2048;            // listed keys
 constexpr int TK_KMAX = 64;
-constexpr int TK_ROUNDS = (TK_STAGE_VEC + TK_THREADS - 1) / TK_THREADS;   // vectors per lane per chunk
+constexpr int TK_POPS = 32;             // tracked maxima a warp offers to the bound
+constexpr int64_t TK_SHORT_V = int64_t(8) * TK_THREADS * 65536;   // rows a 16-bit vector number covers
 
 struct TopkArgs {
   const void* logits;
@@ -82,11 +78,10 @@ DS_DEV uint32_t tk_block_sum(uint32_t c, uint32_t* s_red) {
   return t;
 }
 
-// Geometry of one row: scalar head up to 16-byte alignment, vectors, scalar tail, chunks.
+// Geometry of one row: scalar head up to 16-byte alignment, vectors, scalar tail.
 struct TkRow {
   const void* row;
   int64_t head, nvec, tail0;
-  int nch;
 };
 
 template <typename T>
@@ -105,7 +100,6 @@ DS_DEV TkRow tk_row(const TopkArgs& a, uint32_t row_id) {
   if (g.head > a.V) g.head = a.V;
   g.nvec = (a.V - g.head) / EPV;
   g.tail0 = g.head + g.nvec * EPV;
-  g.nch = g.nvec > 0 ? int((g.nvec + TK_STAGE_VEC - 1) / TK_STAGE_VEC) : 1;
   return g;
 }
 
@@ -126,330 +120,301 @@ DS_DEV void tk_emit(const TopkArgs& a, uint32_t row_id, int rank, uint64_t k64) 
   a.cand_val[o] = ds_key64_val(k64);
 }
 
-// The chunk's own top-K' among the elements that pass the screen (x > thr when `strict`, else
-// x >= thr): the K'-th largest passing key by bisection over the 64 key bits (chunk read from
-// shared memory), then every passing key at or above it (exactly K' keys) into s_new[base...].
-// Only for a chunk whose survivors overflow the buffer. Returns base + the keys written.
+// Keys of tracked vectors: the order key of the vector's maximum (-0.0 folded onto +0.0) in the
+// high half, the thread's vector number in the low half; 0 marks an empty slot. Rows of bf16
+// without transform and at most TK_SHORT_V elements use 16 + 16 bits, other rows 32 + 32 bits.
+template <bool SHORT>
+struct TkKey {
+  using K = uint32_t;
+  static constexpr bool narrow = true;
+  static constexpr int VBITS = 16;
+  DS_DEV static K make(float vmax, uint32_t j) { return (ds_key32(ds_canon_zero(vmax)) & 0xFFFF0000u) | j; }
+  DS_DEV static uint32_t val(K k) { return k >> 16; }
+  DS_DEV static uint32_t num(K k) { return k & 0xFFFFu; }
+  DS_DEV static float to_float(uint32_t v) { return ds_key32_to_float((v << 16) | ((v & 0x8000u) ? 0u : 0xFFFFu)); }
+};
+template <>
+struct TkKey<false> {
+  using K = uint64_t;
+  static constexpr bool narrow = false;
+  static constexpr int VBITS = 32;
+  DS_DEV static K make(float vmax, uint32_t j) { return (uint64_t(ds_key32(ds_canon_zero(vmax))) << 32) | j; }
+  DS_DEV static uint32_t val(K k) { return uint32_t(k >> 32); }
+  DS_DEV static uint32_t num(K k) { return uint32_t(k); }
+  DS_DEV static float to_float(uint32_t v) { return ds_key32_to_float(v); }
+};
+
+// The largest (transformed) element of a 16-byte vector.
 template <typename T, bool XFORM>
-__device__ __noinline__ uint32_t tk_chunk_exact(const TopkArgs& a, const uint4* sv, int nv, int64_t e0,
-                                                int64_t iextra, float xextra, float thr, bool strict,
-                                                uint64_t* s_new, uint32_t base, uint32_t* s_red, uint32_t* s_n) {
+DS_DEV float tk_vec_max(const uint4& w, float mult, float softcap) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && !XFORM) {
+    const __nv_bfloat162 m2 = __hmax2(__hmax2(tk_b2(w.x), tk_b2(w.y)), __hmax2(tk_b2(w.z), tk_b2(w.w)));
+    return __bfloat162float(__hmax(m2.x, m2.y));
+  } else {
+    constexpr int EPV = 16 / sizeof(T);
+    float m = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < EPV; ++x) m = fmaxf(m, tk_xform<XFORM>(ds_vec_elem<T>(w, x), mult, softcap));
+    return m;
+  }
+}
+
+// Lists every element >= thr of the row's vector e, loaded as w (thr2: the bound as a bf16 pair).
+template <typename T, bool XFORM>
+DS_DEV void tk_take(const TopkArgs& a, const uint4& w, int64_t e, int64_t head, float thr,
+                    __nv_bfloat162 thr2, uint64_t* s_list, uint32_t* s_n) {
   constexpr int EPV = 16 / sizeof(T);
-  auto pass = [&](float x) { return strict ? (x > thr) : (x >= thr); };
+  const int64_t i0 = head + e * EPV;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && !XFORM) {
+    // bytes [e0 e1 e2 e3] and [e4 e5 e6 e7] (0x00 / 0xFF) from packed compares, then one bit each
+    const uint32_t c0 = __hge2_mask(tk_b2(w.x), thr2), c1 = __hge2_mask(tk_b2(w.y), thr2);
+    const uint32_t c2 = __hge2_mask(tk_b2(w.z), thr2), c3 = __hge2_mask(tk_b2(w.w), thr2);
+    const uint32_t w01 = __byte_perm(c0, c1, 0x6420), w23 = __byte_perm(c2, c3, 0x6420);
+    uint32_t f = (w01 & 0x08040201u) | (w23 & 0x80402010u);
+    f |= f >> 16;
+    f |= f >> 8;
+    uint32_t m8 = f & 0xFFu;
+    while (m8) {
+      const int x = __ffs(m8) - 1;
+      m8 &= m8 - 1u;
+      const uint32_t slot = atomicAdd(s_n, 1u);
+      if (slot < uint32_t(TK_CAP)) s_list[slot] = ds_key64(ds_canon_zero(ds_vec_elem<T>(w, x)), uint32_t(i0 + x));
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < EPV; ++x) {
+      const float v = tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap);
+      if (v >= thr) {
+        const uint32_t slot = atomicAdd(s_n, 1u);
+        if (slot < uint32_t(TK_CAP)) s_list[slot] = ds_key64(ds_canon_zero(v), uint32_t(i0 + x));
+      }
+    }
+  }
+}
+
+// The K'-th largest of the warps' pops (s_pop[w * TK_POPS + r], r < s_wcnt[w], m per warp at most)
+// by a bisection over the VBITS-bit value key, run by one warp: lane l holds the pops at flat
+// positions l, l + 32, ... of the 16 x m grid (NV >= ceil(16 m / 32)).
+template <int NV, int VBITS>
+DS_DEV uint32_t tk_kth_pop(const uint32_t* s_pop, const uint32_t* s_wcnt, int m, uint32_t Kp) {
+  const int lane = threadIdx.x & 31;
+  uint32_t pv[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int f = lane + 32 * k;
+    const int w = f / m, r = f - w * m;
+    pv[k] = (w < TK_WARPS && uint32_t(r) < s_wcnt[w]) ? s_pop[w * TK_POPS + r] : 0u;
+  }
+  uint32_t kth = 0;
+#pragma unroll 1
+  for (int b = VBITS - 1; b >= 0; --b) {
+    const uint32_t cand = kth | (1u << b);
+    uint32_t n = 0;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) n += pv[k] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xFFFFFFFFu, n) >= Kp) kth = cand;
+  }
+  return kth;
+}
+
+// The same for up to 32 pops per warp (short rows), kept out of line.
+template <int VBITS>
+__device__ __noinline__ uint32_t tk_kth_pop_wide(const uint32_t* s_pop, const uint32_t* s_wcnt, int m, uint32_t Kp) {
+  return tk_kth_pop<TK_POPS / 2, VBITS>(s_pop, s_wcnt, m, Kp);
+}
+
+// The row's exact top-K' keys into s_list[0..K'), for a row whose list overflowed: the K'-th
+// largest key by bisection over the 64 key bits (the whole row counted per bit, from global
+// memory), then every key at or above it. Returns K'.
+template <typename T, bool XFORM>
+__device__ __noinline__ uint32_t tk_row_exact(const TopkArgs& a, const uint4* rv, int nvt, int64_t head,
+                                              int64_t iextra, float xextra, uint64_t* s_list,
+                                              uint32_t* s_red, uint32_t* s_n) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int tid = threadIdx.x;
   uint64_t kres = 0;
   for (int b = 63; b >= 0; --b) {
     const uint64_t cand = kres | (1ull << b);
     uint32_t c = 0;
-    for (int e = threadIdx.x; e < nv; e += TK_THREADS) {
-      const uint4 w = sv[e];
+    for (int j = 0; j < nvt; ++j) {
+      const int64_t e = tid + int64_t(j) * TK_THREADS;
+      const uint4 w = __ldg(rv + e);
 #pragma unroll
       for (int x = 0; x < EPV; ++x) {
         const float v = ds_canon_zero(tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap));
-        c += (pass(v) && ds_key64(v, uint32_t(e0 + int64_t(e) * EPV + x)) >= cand) ? 1u : 0u;
+        c += ds_key64(v, uint32_t(head + e * EPV + x)) >= cand ? 1u : 0u;
       }
     }
-    if (iextra >= 0) {
-      const float v = ds_canon_zero(xextra);
-      c += (pass(v) && ds_key64(v, uint32_t(iextra)) >= cand) ? 1u : 0u;
-    }
+    if (iextra >= 0) c += ds_key64(ds_canon_zero(xextra), uint32_t(iextra)) >= cand ? 1u : 0u;
     if (tk_block_sum(c, s_red) >= uint32_t(a.Kp)) kres = cand;
   }
   __syncthreads();
-  if (threadIdx.x == 0) *s_n = base;
+  if (tid == 0) *s_n = 0;
   __syncthreads();
-  for (int e = threadIdx.x; e < nv; e += TK_THREADS) {
-    const uint4 w = sv[e];
+  for (int j = 0; j < nvt; ++j) {
+    const int64_t e = tid + int64_t(j) * TK_THREADS;
+    const uint4 w = __ldg(rv + e);
 #pragma unroll
     for (int x = 0; x < EPV; ++x) {
       const float v = ds_canon_zero(tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap));
-      const uint64_t k = ds_key64(v, uint32_t(e0 + int64_t(e) * EPV + x));
-      if (pass(v) && k >= kres) {
-        const uint32_t slot = atomicAdd(s_n, 1u);
-        if (slot < TK_NEW_CAP) s_new[slot] = k;
-      }
+      const uint64_t k = ds_key64(v, uint32_t(head + e * EPV + x));
+      if (k >= kres) s_list[atomicAdd(s_n, 1u)] = k;     // exactly K' keys pass
     }
   }
   if (iextra >= 0) {
-    const float v = ds_canon_zero(xextra);
-    const uint64_t k = ds_key64(v, uint32_t(iextra));
-    if (pass(v) && k >= kres) {
-      const uint32_t slot = atomicAdd(s_n, 1u);
-      if (slot < TK_NEW_CAP) s_new[slot] = k;
-    }
+    const uint64_t k = ds_key64(ds_canon_zero(xextra), uint32_t(iextra));
+    if (k >= kres) s_list[atomicAdd(s_n, 1u)] = k;
   }
   __syncthreads();
-  return min(*s_n, uint32_t(TK_NEW_CAP));
+  return *s_n;
 }
 
-template <typename T, bool XFORM>
+template <typename T, bool XFORM, bool SHORT>
 __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs a) {
+  using KK = TkKey<SHORT>;
+  using K = typename KK::K;
   constexpr int EPV = 16 / sizeof(T);
-  constexpr bool PACKED = std::is_same<T, __nv_bfloat16>::value && !XFORM;
-  constexpr int PRODUCER = TK_THREADS - 32;               // lane 0 of the last warp issues the copies
-  extern __shared__ __align__(128) uint8_t tk_dyn[];      // TK_STAGES x TK_STAGE_VEC x 16 bytes
-  __shared__ uint64_t s_full[TK_STAGES];
-  __shared__ uint64_t s_top[2][TK_KMAX];                  // running top-K' keys, sorted
-  __shared__ uint64_t s_new[TK_NEW_CAP];                  // survivors not yet merged
+  __shared__ uint64_t s_list[TK_CAP];
+  __shared__ uint64_t s_top[TK_KMAX];
   __shared__ uint32_t s_red[TK_WARPS];
-  __shared__ float s_wthr[TK_WARPS];
-  __shared__ uint32_t s_n;
+  __shared__ uint32_t s_pop[TK_WARPS * TK_POPS];
+  __shared__ uint32_t s_wcnt[TK_WARPS];
+  __shared__ uint32_t s_n, s_tv;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint4* stages = reinterpret_cast<const uint4*>(tk_dyn);
-
-  // producer: the CTA's (row, chunk) sequence, TK_STAGES items ahead of the consumer
-  int p_ri = 0, p_c = 0, issued = 0;
-  auto issue_next = [&]() {
-    const int64_t row_id = int64_t(blockIdx.x) + int64_t(p_ri) * gridDim.x;
-    if (row_id >= a.rows) return;
-    const TkRow g = tk_row<T>(a, uint32_t(row_id));
-    const int64_t v0 = int64_t(p_c) * TK_STAGE_VEC, v1 = min(g.nvec, v0 + TK_STAGE_VEC);
-    const uint32_t bytes = v1 > v0 ? uint32_t((v1 - v0) * 16) : 0u;
-    const int s = issued % TK_STAGES;
-    ds_mbar_arrive_expect_tx(&s_full[s], bytes);
-    if (bytes)
-      ds_bulk_g2s(tk_dyn + size_t(s) * TK_STAGE_VEC * 16,
-                  reinterpret_cast<const uint8_t*>(g.row) + g.head * int64_t(sizeof(T)) + v0 * 16, bytes, &s_full[s]);
-    ++issued;
-    if (++p_c == g.nch) {
-      p_c = 0;
-      ++p_ri;
-    }
-  };
-
-  if (tid == PRODUCER) {
-    for (int s = 0; s < TK_STAGES; ++s) ds_mbar_init(&s_full[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int s = 0; s < TK_STAGES; ++s) issue_next();
-  }
-  if (tid == 0) s_n = 0;
-  __syncthreads();
-
-  const int m = (a.Kp + TK_WARPS - 1) / TK_WARPS;
-  int n = 0;                                               // items consumed
   for (int64_t row_id = blockIdx.x; row_id < a.rows; row_id += gridDim.x) {
     const TkRow g = tk_row<T>(a, uint32_t(row_id));
     const T* row = reinterpret_cast<const T*>(g.row);
-    int cur = 0, ntop = 0;
-    float bound = -INFINITY;                               // every later element must beat it strictly
-    for (int c = 0; c < g.nch; ++c, ++n) {
-      const int s = n % TK_STAGES;
-      const int64_t v0 = int64_t(c) * TK_STAGE_VEC, v1 = min(g.nvec, v0 + TK_STAGE_VEC);
-      const int nv = v1 > v0 ? int(v1 - v0) : 0;
-      const int64_t e0 = g.head + v0 * EPV;                 // index of the chunk's first vector element
-      const uint4* sv = stages + size_t(s) * TK_STAGE_VEC;
+    const uint4* rv = reinterpret_cast<const uint4*>(row + g.head);
+    const int nvt = tid < g.nvec ? int((g.nvec - 1 - tid) / TK_THREADS) + 1 : 0;
 
-      // scalar head (chunk 0) and tail (last chunk) elements, loaded directly
-      int64_t iextra = -1;
-      if (c == 0 && tid < g.head) iextra = tid;
-      if (c == g.nch - 1 && tid >= 8 && tid - 8 < a.V - g.tail0) iextra = g.tail0 + (tid - 8);
-      const float xextra = iextra >= 0 ? tk_xform<XFORM>(ds_load_elem<T>(row + iextra), a.mult, a.softcap) : -INFINITY;
+    // scalar head and tail elements, one per thread
+    int64_t iextra = -1;
+    if (tid < g.head) iextra = tid;
+    else if (tid >= 8 && tid - 8 < a.V - g.tail0) iextra = g.tail0 + (tid - 8);
+    const float xextra = iextra >= 0 ? tk_xform<XFORM>(ds_load_elem<T>(row + iextra), a.mult, a.softcap) : -INFINITY;
 
-      bool ok = ds_mbar_wait(&s_full[s], uint32_t(n / TK_STAGES) & 1u, DS_WAIT_LIMIT);
-      ok = __syncthreads_and(ok) != 0;
-      if (!ok) {
-        // a copy never completed: report it, let the copies in flight land (bounded), stop
-        if (tid == PRODUCER) {
-          ds_set_error(a.status, DSPARK_ETIMEOUT);
-          for (int j = n; j < issued; ++j)
-            (void)ds_mbar_wait(&s_full[j % TK_STAGES], uint32_t(j / TK_STAGES) & 1u, DS_WAIT_LIMIT);
-        }
-        return;
-      }
-      const uint32_t nbase = s_n;                          // survivors of earlier chunks not merged yet
-
-      // ---- screen: one sweep without side effects marks the vectors holding a survivor (all
-      // loads in flight together), then the marked vectors are taken apart ----
-      float thr;
-      bool strict;
-      uint32_t hits = 0;
-      if (c == 0) {
-        // bound from the chunk itself: the m-th largest lane maximum of every warp
-        strict = false;
-        float tmax = xextra;
-        float vmax[TK_ROUNDS];
-        __nv_bfloat162 vmax2[TK_ROUNDS];
-        if constexpr (PACKED) {
-          __nv_bfloat162 acc = __float2bfloat162_rn(-INFINITY);
+    // ---- 1. stream: the 4 largest vectors of the thread ----
+    constexpr int TK_BATCH = KK::narrow ? 8 : 4;            // vectors in flight per thread
+    K t[TK_TRACK];
 #pragma unroll
-          for (int k = 0; k < TK_ROUNDS; ++k) {
-            const int e = tid + k * TK_THREADS;
-            vmax2[k] = __float2bfloat162_rn(-INFINITY);
-            if (e < nv) {
-              const uint4 w = sv[e];
-              vmax2[k] = __hmax2(__hmax2(tk_b2(w.x), tk_b2(w.y)), __hmax2(tk_b2(w.z), tk_b2(w.w)));
-              acc = __hmax2(acc, vmax2[k]);
-            }
-          }
-          tmax = fmaxf(tmax, fmaxf(__low2float(acc), __high2float(acc)));
-        } else {
+    for (int i = 0; i < TK_TRACK; ++i) t[i] = 0;
+    for (int j0 = 0; j0 < nvt; j0 += TK_BATCH) {
+      uint4 w[TK_BATCH];
 #pragma unroll
-          for (int k = 0; k < TK_ROUNDS; ++k) {
-            const int e = tid + k * TK_THREADS;
-            vmax[k] = -INFINITY;
-            if (e < nv) {
-              const uint4 w = sv[e];
+      for (int u = 0; u < TK_BATCH; ++u)
+        if (j0 + u < nvt) w[u] = __ldg(rv + (tid + int64_t(j0 + u) * TK_THREADS));
 #pragma unroll
-              for (int x = 0; x < EPV; ++x)
-                vmax[k] = fmaxf(vmax[k], tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap));
-              tmax = fmaxf(tmax, vmax[k]);
-            }
+      for (int u = 0; u < TK_BATCH; ++u) {
+        if (j0 + u < nvt) {
+          K x = KK::make(tk_vec_max<T, XFORM>(w[u], a.mult, a.softcap), uint32_t(j0 + u));
+#pragma unroll
+          for (int i = 0; i < TK_TRACK; ++i) {
+            const K hi = t[i] > x ? t[i] : x;
+            x = t[i] > x ? x : t[i];
+            t[i] = hi;
           }
         }
-        uint32_t key = ds_key32(ds_canon_zero(tmax)), kth = 0;
-#pragma unroll
-        for (int t = 0; t < (TK_KMAX + TK_WARPS - 1) / TK_WARPS; ++t) {
-          if (t < m) {
-            kth = __reduce_max_sync(0xFFFFFFFFu, key);
-            const unsigned who = __ballot_sync(0xFFFFFFFFu, key == kth);
-            if (lane == __ffs(who) - 1) key = 0;
-          }
-        }
-        if (lane == 0) s_wthr[warp] = (kth <= ds_key32(-INFINITY)) ? -INFINITY : ds_key32_to_float(kth);
-        __syncthreads();
-        thr = s_wthr[0];
-#pragma unroll
-        for (int w = 1; w < TK_WARPS; ++w) thr = fminf(thr, s_wthr[w]);
-        const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact for bf16 rows: an element value
-#pragma unroll
-        for (int k = 0; k < TK_ROUNDS; ++k) {
-          bool any;
-          if constexpr (PACKED) any = (tid + k * TK_THREADS < nv) && __hge2_mask(vmax2[k], thr2) != 0u;
-          else any = (tid + k * TK_THREADS < nv) && vmax[k] >= thr;
-          hits |= any ? (1u << k) : 0u;
-        }
-      } else {
-        // bound from the elements before the chunk: only values strictly above it can enter
-        strict = true;
-        thr = bound;
-        const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact for bf16 rows: an element value
-#pragma unroll
-        for (int k = 0; k < TK_ROUNDS; ++k) {
-          const int e = tid + k * TK_THREADS;
-          if (e < nv) {
-            const uint4 w = sv[e];
-            bool any;
-            if constexpr (PACKED) {
-              const __nv_bfloat162 mx = __hmax2(__hmax2(tk_b2(w.x), tk_b2(w.y)), __hmax2(tk_b2(w.z), tk_b2(w.w)));
-              any = __hgt2_mask(mx, thr2) != 0u;
-            } else {
-              float mx = -INFINITY;
-#pragma unroll
-              for (int x = 0; x < EPV; ++x) mx = fmaxf(mx, tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap));
-              any = mx > thr;
-            }
-            hits |= any ? (1u << k) : 0u;
-          }
-        }
-      }
-      // the marked vectors, one per lane at a time: 8-bit survivor masks drained by the whole warp
-      // (one survivor per lane per pass, one shared-memory atomic per pass)
-      {
-        const unsigned below = (1u << lane) - 1u;
-        const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);
-        while (__any_sync(0xFFFFFFFFu, hits != 0u)) {
-          uint32_t m8 = 0;
-          int e = 0;
-          if (hits) {
-            e = tid + (__ffs(hits) - 1) * TK_THREADS;
-            hits &= hits - 1u;
-            const uint4 w = sv[e];
-            if constexpr (PACKED) {
-              uint32_t c0, c1, c2, c3;
-              if (strict) {
-                c0 = __hgt2_mask(tk_b2(w.x), thr2), c1 = __hgt2_mask(tk_b2(w.y), thr2);
-                c2 = __hgt2_mask(tk_b2(w.z), thr2), c3 = __hgt2_mask(tk_b2(w.w), thr2);
-              } else {
-                c0 = __hge2_mask(tk_b2(w.x), thr2), c1 = __hge2_mask(tk_b2(w.y), thr2);
-                c2 = __hge2_mask(tk_b2(w.z), thr2), c3 = __hge2_mask(tk_b2(w.w), thr2);
-              }
-              // bytes [e0 e1 e2 e3] and [e4 e5 e6 e7] (0x00 / 0xFF), then one bit per element
-              const uint32_t w01 = __byte_perm(c0, c1, 0x6420), w23 = __byte_perm(c2, c3, 0x6420);
-              uint32_t f = (w01 & 0x08040201u) | (w23 & 0x80402010u);
-              f |= f >> 16;
-              f |= f >> 8;
-              m8 = f & 0xFFu;
-            } else {
-#pragma unroll
-              for (int x = 0; x < EPV; ++x) {
-                const float v = tk_xform<XFORM>(ds_vec_elem<T>(w, x), a.mult, a.softcap);
-                m8 |= (strict ? v > thr : v >= thr) ? (1u << x) : 0u;
-              }
-            }
-          }
-          while (true) {
-            const unsigned act = __ballot_sync(0xFFFFFFFFu, m8 != 0u);
-            if (act == 0u) break;
-            uint32_t slot = 0;
-            const int leader = __ffs(act) - 1;
-            if (lane == leader) slot = atomicAdd(&s_n, uint32_t(__popc(act)));
-            slot = __shfl_sync(0xFFFFFFFFu, slot, leader) + uint32_t(__popc(act & below));
-            if (m8 != 0u) {
-              const int x = __ffs(m8) - 1;
-              m8 &= m8 - 1u;
-              const float v = tk_xform<XFORM>(ds_load_elem<T>(reinterpret_cast<const T*>(sv + e) + x), a.mult, a.softcap);
-              if (slot < TK_NEW_CAP) s_new[slot] = ds_key64(ds_canon_zero(v), uint32_t(e0 + int64_t(e) * EPV + x));
-            }
-          }
-        }
-      }
-      if (iextra >= 0 && (strict ? xextra > thr : xextra >= thr)) {
-        const uint32_t slot = atomicAdd(&s_n, 1u);
-        if (slot < TK_NEW_CAP) s_new[slot] = ds_key64(ds_canon_zero(xextra), uint32_t(iextra));
-      }
-      if (c == 0) bound = thr;      // K' elements of chunk 0 are >= thr and precede every later one
-      __syncthreads();
-      uint32_t N = s_n;
-      if (N > uint32_t(TK_NEW_CAP))
-        N = tk_chunk_exact<T, XFORM>(a, sv, nv, e0, iextra, xextra, thr, strict, s_new, nbase, s_red, &s_n);
-      // the stage is free: refill it with the item TK_STAGES ahead
-      if (tid == PRODUCER) {
-        ds_fence_proxy_async_smem();
-        issue_next();
-      }
-
-      // ---- merge the survivors into the running list once enough have gathered (and at the end
-      // of the row): a key's position is the number of keys above it in both lists (binary
-      // search in the sorted list, a count over the new keys) ----
-      if (N >= uint32_t(2 * a.Kp) || c == g.nch - 1) {
-        const uint64_t* old = s_top[cur];
-        uint64_t* out = s_top[cur ^ 1];
-        const uint32_t nt = uint32_t(ntop);
-        for (uint32_t t = tid; t < N + nt; t += TK_THREADS) {
-          const bool is_new = t < N;
-          const uint64_t k = is_new ? s_new[t] : old[t - N];
-          uint32_t pos = 0;
-          if (is_new) {
-            uint32_t lo = 0, hi = nt;                      // first old key below k
-            while (lo < hi) {
-              const uint32_t mid = (lo + hi) >> 1;
-              if (old[mid] > k) lo = mid + 1;
-              else hi = mid;
-            }
-            pos = lo;
-          } else {
-            pos = t - N;
-          }
-          uint32_t u = 0;
-          for (; u + 8 <= N; u += 8) {
-            uint32_t cnt = 0;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) cnt += (s_new[u + r] > k) ? 1u : 0u;
-            pos += cnt;
-          }
-          for (; u < N; ++u) pos += (s_new[u] > k) ? 1u : 0u;
-          if (pos < uint32_t(a.Kp)) out[pos] = k;
-        }
-        __syncthreads();
-        cur ^= 1;
-        ntop = int(min(uint32_t(ntop) + N, uint32_t(a.Kp)));
-        if (ntop == a.Kp) bound = fmaxf(bound, ds_key64_val(s_top[cur][a.Kp - 1]));
-        if (tid == 0) s_n = 0;
       }
     }
+
+    // ---- 2. bound: each warp pops its m largest tracked maxima, m = ceil(2K' / warps holding
+    // vectors) (at most 32); T is the K'-th largest of all pops, found by one warp ----
+    const int64_t busy = g.nvec < TK_THREADS ? g.nvec : TK_THREADS;
+    const int aw = int((busy + 31) / 32);
+    const int m_pop = aw > 0 ? min(TK_POPS, (2 * a.Kp + aw - 1) / aw) : 0;
+    {
+      K c[TK_TRACK];
+#pragma unroll
+      for (int i = 0; i < TK_TRACK; ++i) c[i] = t[i];
+      uint32_t cnt = 0;
+      for (int r = 0; r < m_pop; ++r) {
+        const uint32_t head = KK::val(c[0]);
+        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, head);
+        if (top == 0u) break;                              // the warp's tracked vectors are used up
+        if (lane == 0) s_pop[warp * TK_POPS + r] = top;
+        ++cnt;
+        const unsigned who = __ballot_sync(0xFFFFFFFFu, head == top);
+        if (lane == __ffs(who) - 1) {
+#pragma unroll
+          for (int i = 0; i + 1 < TK_TRACK; ++i) c[i] = c[i + 1];
+          c[TK_TRACK - 1] = 0;
+        }
+      }
+      if (lane == 0) s_wcnt[warp] = cnt;
+    }
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t pops = 0, kth = 0;
+#pragma unroll
+      for (int w = 0; w < TK_WARPS; ++w) pops += s_wcnt[w];
+      if (pops >= uint32_t(a.Kp))                          // else no bound: every element is listed
+        kth = m_pop <= 8 ? tk_kth_pop<4, KK::VBITS>(s_pop, s_wcnt, m_pop, uint32_t(a.Kp))
+                         : tk_kth_pop_wide<KK::VBITS>(s_pop, s_wcnt, m_pop, uint32_t(a.Kp));
+      if (lane == 0) s_tv = kth;
+    }
+    __syncthreads();
+    const uint32_t tv = s_tv;
+    const float thr = tv == 0u ? -INFINITY : KK::to_float(tv);
+    const __nv_bfloat162 thr2 = __float2bfloat162_rn(thr);   // exact: thr is a bf16 value on packed rows
+
+    // ---- 3. gather the elements >= T ----
+    // a thread whose last tracked maximum is below T re-reads only its tracked vectors that reach
+    // T (usually none or one); the vectors of the other threads are re-read by their whole warp,
+    // one lane per vector
+    const bool full = KK::val(t[TK_TRACK - 1]) >= tv;
+    if (!full) {
+#pragma unroll
+      for (int i = 0; i < TK_TRACK; ++i) {
+        if (KK::val(t[i]) >= tv) {
+          const int64_t e = tid + int64_t(KK::num(t[i])) * TK_THREADS;
+          tk_take<T, XFORM>(a, __ldg(rv + e), e, g.head, thr, thr2, s_list, &s_n);
+        }
+      }
+    }
+    for (unsigned fm = __ballot_sync(0xFFFFFFFFu, full); fm != 0u; fm &= fm - 1u) {
+      const int src = __ffs(fm) - 1;
+      const int stid = (tid & ~31) + src;
+      const int snvt = __shfl_sync(0xFFFFFFFFu, nvt, src);
+      for (int j = lane; j < snvt; j += 32) {
+        const int64_t e = stid + int64_t(j) * TK_THREADS;
+        tk_take<T, XFORM>(a, __ldg(rv + e), e, g.head, thr, thr2, s_list, &s_n);
+      }
+    }
+    if (iextra >= 0 && xextra >= thr) {
+      const uint32_t slot = atomicAdd(&s_n, 1u);
+      if (slot < uint32_t(TK_CAP)) s_list[slot] = ds_key64(ds_canon_zero(xextra), uint32_t(iextra));
+    }
+    __syncthreads();
+    uint32_t N = s_n;
+    if (N > uint32_t(TK_CAP)) N = tk_row_exact<T, XFORM>(a, rv, nvt, g.head, iextra, xextra, s_list, s_red, &s_n);
+
+    // ---- 4. rank the listed keys: P threads share a key's count (P = 1, 2, 4 or 8) ----
+    {
+      uint32_t P = 1;
+      while (P < 8u && N * P * 2u <= uint32_t(TK_THREADS)) P *= 2u;
+      const uint32_t sub = tid & (P - 1u), per = uint32_t(TK_THREADS) / P;
+      for (uint32_t base = 0; base < N; base += per) {
+        if (base + uint32_t(warp * 32) / P >= N) continue;   // no key for this warp
+        const uint32_t q = base + tid / P;
+        const uint64_t k = q < N ? s_list[q] : ~0ull;
+        uint32_t pos = 0, u = sub;
+        for (; u + 7u * P < N; u += 8u * P) {
+          uint32_t cnt = 0;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) cnt += (s_list[u + r * P] > k) ? 1u : 0u;
+          pos += cnt;
+        }
+        for (; u < N; u += P) pos += (s_list[u] > k) ? 1u : 0u;
+        for (uint32_t o = 1; o < P; o <<= 1) pos += __shfl_xor_sync(0xFFFFFFFFu, pos, o);
+        if (q < N && sub == 0u && pos < uint32_t(a.Kp)) s_top[pos] = k;
+      }
+    }
+    __syncthreads();
     if (tid < a.Kp) {
-      if (tid < ntop) {
-        tk_emit(a, uint32_t(row_id), tid, s_top[cur][tid]);
+      if (uint32_t(tid) < N) {
+        tk_emit(a, uint32_t(row_id), tid, s_top[tid]);
       } else {                                             // unreachable: every row holds >= K' elements
         ds_set_error(a.status, DSPARK_EINVAL);
         const int64_t o = row_id * a.Kp + tid;
@@ -458,24 +423,15 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
         a.cand_val[o] = -INFINITY;
       }
     }
+    __syncthreads();                                       // the lists are rebuilt for the next row
   }
+  (void)EPV;
 }
 
-template <typename T, bool XFORM>
+template <typename T, bool XFORM, bool SHORT>
 cudaError_t tk_launch(const TopkArgs& a, cudaStream_t stream) {
-  auto kern = topk_row_kernel<T, XFORM>;
-  const size_t smem = size_t(TK_STAGES) * TK_STAGE_VEC * 16;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
   const int grid = int(std::min<int64_t>(a.rows, int64_t(2) * ds_num_sms()));
-  kern<<<unsigned(grid), TK_THREADS, smem, stream>>>(a);
+  topk_row_kernel<T, XFORM, SHORT><<<unsigned(grid), TK_THREADS, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -512,10 +468,13 @@ extern "C" dspark_status dspark_topk(const void* logits, dspark_dtype dtype, int
   a.status = dev_status;
   const bool xform = (mult != 1.0f) || (softcap > 0.0f);
   cudaError_t e;
-  if (dtype == DSPARK_BF16)
-    e = xform ? tk_launch<__nv_bfloat16, true>(a, stream) : tk_launch<__nv_bfloat16, false>(a, stream);
+  if (dtype == DSPARK_BF16 && !xform)
+    e = V_d <= TK_SHORT_V ? tk_launch<__nv_bfloat16, false, true>(a, stream)
+                          : tk_launch<__nv_bfloat16, false, false>(a, stream);
+  else if (dtype == DSPARK_BF16)
+    e = tk_launch<__nv_bfloat16, true, false>(a, stream);
   else
-    e = xform ? tk_launch<float, true>(a, stream) : tk_launch<float, false>(a, stream);
+    e = xform ? tk_launch<float, true, false>(a, stream) : tk_launch<float, false, false>(a, stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return DSPARK_ECUDA;
