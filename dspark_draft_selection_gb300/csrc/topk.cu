@@ -13,14 +13,14 @@
 // stretch of the row and every load is coalesced. The logits go from HBM to registers once;
 // nothing is staged in shared memory and no barrier falls inside the stream.
 //  1. Stream: each thread loads its vectors in batches of 8 and keeps the keys (vector maximum,
-//     vector number) of its 4 largest vectors, sorted, with a branch-free min/max network.
-//  2. Bound: each warp pops its m largest tracked maxima (warp REDUX rounds). They are maxima of
-//     distinct vectors, so once the pops add up to K' there are K' distinct elements at or above
-//     T, the smallest warp's last pop, and every top-K' element is >= T.
+//     vector number) of its 6 largest vectors, sorted, with a branch-free min/max network.
+//  2. Bound: each warp pops its m = ceil(2K'/16) largest tracked maxima (REDUX rounds) and one
+//     warp finds T, the K'-th largest pop, by a bisection over the value key. The pops are maxima
+//     of distinct vectors, so K' distinct elements are >= T and every top-K' element is >= T.
 //  3. Gather: only a vector whose maximum reaches T can hold an element >= T. A thread whose
-//     fourth tracked maximum is below T knows all its other vectors are below T and re-reads only
-//     its tracked vectors that reach T (from L2); otherwise it re-reads all of its vectors.
-//     Elements >= T go to a shared list (about 2K' on Gaussian rows).
+//     sixth tracked maximum is below T knows all its other vectors are below T and re-reads only
+//     its tracked vectors that reach T (from L2); otherwise its warp re-reads all of them.
+//     Elements >= T go to a shared list (about K' + 3 on Gaussian rows).
 //  4. Select: a listed key's rank is the number of listed keys above it (64-bit keys: value, then
 //     lower index first); the first K' ranks are written in order with the d2t map.
 //  5. A list that overflows its 2048 slots (ties at T, as in a constant row) is cut exactly by a
@@ -37,7 +37,7 @@ constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_TRACK = 6;             // largest vectors remembered per thread
 constexpr int TK_CAP = 2048;            // listed keys
 constexpr int TK_KMAX = 64;
-constexpr int TK_POPS = 32;             // tracked maxima a warp offers to the bound
+constexpr int TK_POPS = 16;             // tracked maxima a warp offers to the bound (at most)
 constexpr int64_t TK_SHORT_V = int64_t(8) * TK_THREADS * 65536;   // rows a 16-bit vector number covers
 
 struct TopkArgs {
@@ -193,8 +193,8 @@ DS_DEV void tk_take(const TopkArgs& a, const uint4& w, int64_t e, int64_t head, 
 }
 
 // The K'-th largest of the warps' pops (s_pop[w * TK_POPS + r], r < s_wcnt[w], m per warp at most)
-// by a bisection over the VBITS-bit value key, run by one warp: lane l holds the pops at flat
-// positions l, l + 32, ... of the 16 x m grid (NV >= ceil(16 m / 32)).
+// by a bisection over the VBITS-bit value key, two bits a round, run by one warp: lane l holds the
+// pops at flat positions l, l + 32, ... of the 16 x m grid (NV >= ceil(16 m / 32)).
 template <int NV, int VBITS>
 DS_DEV uint32_t tk_kth_pop(const uint32_t* s_pop, const uint32_t* s_wcnt, int m, uint32_t Kp) {
   const int lane = threadIdx.x & 31;
@@ -207,20 +207,21 @@ DS_DEV uint32_t tk_kth_pop(const uint32_t* s_pop, const uint32_t* s_wcnt, int m,
   }
   uint32_t kth = 0;
 #pragma unroll 1
-  for (int b = VBITS - 1; b >= 0; --b) {
-    const uint32_t cand = kth | (1u << b);
-    uint32_t n = 0;
+  for (int b = VBITS - 2; b >= 0; b -= 2) {               // two bits a round: three counts
+    const uint32_t c1 = kth | (1u << b), c2 = kth | (2u << b), c3 = kth | (3u << b);
+    uint32_t n1 = 0, n2 = 0, n3 = 0;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) n += pv[k] >= cand ? 1u : 0u;
-    if (__reduce_add_sync(0xFFFFFFFFu, n) >= Kp) kth = cand;
+    for (int k = 0; k < NV; ++k) {
+      n1 += pv[k] >= c1 ? 1u : 0u;
+      n2 += pv[k] >= c2 ? 1u : 0u;
+      n3 += pv[k] >= c3 ? 1u : 0u;
+    }
+    n1 = __reduce_add_sync(0xFFFFFFFFu, n1);
+    n2 = __reduce_add_sync(0xFFFFFFFFu, n2);
+    n3 = __reduce_add_sync(0xFFFFFFFFu, n3);
+    kth |= ((n1 >= Kp ? 1u : 0u) + (n2 >= Kp ? 1u : 0u) + (n3 >= Kp ? 1u : 0u)) << b;
   }
   return kth;
-}
-
-// The same for up to 32 pops per warp (short rows), kept out of line.
-template <int VBITS>
-__device__ __noinline__ uint32_t tk_kth_pop_wide(const uint32_t* s_pop, const uint32_t* s_wcnt, int m, uint32_t Kp) {
-  return tk_kth_pop<TK_POPS / 2, VBITS>(s_pop, s_wcnt, m, Kp);
 }
 
 // The row's exact top-K' keys into s_list[0..K'), for a row whose list overflowed: the K'-th
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
     else if (tid >= 8 && tid - 8 < a.V - g.tail0) iextra = g.tail0 + (tid - 8);
     const float xextra = iextra >= 0 ? tk_xform<XFORM>(ds_load_elem<T>(row + iextra), a.mult, a.softcap) : -INFINITY;
 
-    // ---- 1. stream: the 4 largest vectors of the thread ----
+    // ---- 1. stream: the six largest vectors of the thread ----
     constexpr int TK_BATCH = KK::narrow ? 8 : 4;            // vectors in flight per thread
     K t[TK_TRACK];
 #pragma unroll
@@ -319,7 +320,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
     }
 
     // ---- 2. bound: each warp pops its m largest tracked maxima, m = ceil(2K' / warps holding
-    // vectors) (at most 32); T is the K'-th largest of all pops, found by one warp ----
+    // vectors) (at most 16); T is the K'-th largest of all pops, found by one warp. Rows too short
+    // for K' pops (under 800 elements) list every element ----
     const int64_t busy = g.nvec < TK_THREADS ? g.nvec : TK_THREADS;
     const int aw = int((busy + 31) / 32);
     const int m_pop = aw > 0 ? min(TK_POPS, (2 * a.Kp + aw - 1) / aw) : 0;
@@ -330,12 +332,20 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
       uint32_t cnt = 0;
       for (int r = 0; r < m_pop; ++r) {
         const uint32_t head = KK::val(c[0]);
-        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, head);
+        uint32_t top;
+        int owner;
+        if constexpr (KK::narrow) {                        // value and lane in one 21-bit key
+          const uint32_t pk = __reduce_max_sync(0xFFFFFFFFu, (head << 5) | uint32_t(lane));
+          top = pk >> 5;
+          owner = int(pk & 31u);
+        } else {
+          top = __reduce_max_sync(0xFFFFFFFFu, head);
+          owner = __ffs(__ballot_sync(0xFFFFFFFFu, head == top)) - 1;
+        }
         if (top == 0u) break;                              // the warp's tracked vectors are used up
         if (lane == 0) s_pop[warp * TK_POPS + r] = top;
         ++cnt;
-        const unsigned who = __ballot_sync(0xFFFFFFFFu, head == top);
-        if (lane == __ffs(who) - 1) {
+        if (lane == owner) {
 #pragma unroll
           for (int i = 0; i + 1 < TK_TRACK; ++i) c[i] = c[i + 1];
           c[TK_TRACK - 1] = 0;
@@ -350,8 +360,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
 #pragma unroll
       for (int w = 0; w < TK_WARPS; ++w) pops += s_wcnt[w];
       if (pops >= uint32_t(a.Kp))                          // else no bound: every element is listed
-        kth = m_pop <= 8 ? tk_kth_pop<4, KK::VBITS>(s_pop, s_wcnt, m_pop, uint32_t(a.Kp))
-                         : tk_kth_pop_wide<KK::VBITS>(s_pop, s_wcnt, m_pop, uint32_t(a.Kp));
+        kth = tk_kth_pop<TK_POPS / 2, KK::VBITS>(s_pop, s_wcnt, m_pop, uint32_t(a.Kp));
       if (lane == 0) s_tv = kth;
     }
     __syncthreads();
