@@ -8,14 +8,18 @@
 // gathered by thresholds p_max e^-10, e^-20, e^-40, then all; exponents below -64 flushed); the
 // commit on double-precision multinomial sums; the commit on the double uniform.
 //
-// One block of 512 threads per row (persistent over rows, one block per SM), no clusters: the
-// row streams through the block in passes (16-byte loads, several chunks in flight per thread;
-// repeated passes mostly hit L2): the maximum of z = s / T (and the dense record's z row), the
-// nucleus when top-p < 1 (threshold rounds with the candidates sorted in shared memory; a
-// 64-step bisection over (weight, index) keys when they overflow), then the kept mass of every
-// cell of 32 vectors (float pairs per thread, double per warp). A block scan over the cells
-// locates the one whose running sum crosses u * W_kept; its warp re-reads those 32 vectors and
-// finds the lane, then the element.
+// One block of 512 threads per row, persistent over rows (two blocks per SM on the plain path,
+// one with a nucleus, a transform or a sparse record). When the rows are fewer than the blocks
+// that fit, each row is split into P = 2, 4 or 8 parts run by the blocks of one cluster, which
+// exchange their maxima and masses through distributed shared memory. The row streams through
+// the block in passes (16-byte loads, several chunks in flight per thread; repeated passes mostly
+// hit L2): the maximum of z = s / T (and the dense record's z row), the nucleus when top-p < 1
+// (threshold rounds with the candidates sorted in shared memory; a 64-step bisection over
+// (weight, index) keys when they overflow), then the kept mass of every cell of 32 vectors as a
+// float pair (2Sum), turned into double once per thread rather than once per cell, since the
+// FP64 pipe is costly per warp instruction. A block scan over the cells locates the one whose
+// running sum crosses u * W_kept; its warp re-reads those 32 vectors and finds the lane, then
+// the element.
 #include <cfloat>
 
 #include <cooperative_groups.h>
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
   __shared__ double s_tau, s_cut[2];
   // exchange slots of the row's parts (a cluster of P blocks), one per part
   __shared__ float s_xf[SR_MAXP];
-  __shared__ unsigned long long s_xu[SR_MAXP], s_xl[SR_MAXP];
+  __shared__ unsigned long long s_xu[SR_MAXP];
   __shared__ double s_xd[SR_MAXP];
   __shared__ double s_run[SR_THREADS + 1];
   cg::cluster_group cl = cg::this_cluster();
