@@ -159,13 +159,41 @@ DS_DEV uint64_t ds_warp_max_u64(uint64_t v) {
 }
 
 // ----------------------------------------------------------------------------------------
-// gate gamma = sigmoid(h . g) of one hidden row, whole block: float32 partial dots per thread,
-// summed in double; s_red holds one float per warp.
+// gate gamma = sigmoid(h . g) of one hidden row, whole block: float32 partial dots per thread
+// (16-byte loads, four pairs in flight, when both rows are 16-byte aligned), summed in double;
+// s_red holds one float per warp.
 // ----------------------------------------------------------------------------------------
 template <typename HT>
 DS_DEV float ds_block_gate(const HT* h, const HT* g, int H, float* s_red) {
+  constexpr int EPV = 16 / sizeof(HT);
+  constexpr int U = 4;
   float acc = 0.0f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) acc = __fmaf_rn(ds_load_elem<HT>(h + k), ds_load_elem<HT>(g + k), acc);
+  int k0 = 0;
+  if (((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(g)) & 15u) == 0) {
+    const int nv = H / EPV;
+    const uint4* hv = reinterpret_cast<const uint4*>(h);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    for (int v0 = threadIdx.x; v0 < nv; v0 += U * int(blockDim.x)) {
+      uint4 x[U], y[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * int(blockDim.x);
+        if (v < nv) {
+          x[u] = __ldg(hv + v);
+          y[u] = __ldg(gv + v);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (v0 + u * int(blockDim.x) < nv) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc = __fmaf_rn(ds_vec_elem<HT>(x[u], e), ds_vec_elem<HT>(y[u], e), acc);
+        }
+      }
+    }
+    k0 = nv * EPV;
+  }
+  for (int k = k0 + int(threadIdx.x); k < H; k += blockDim.x) acc = __fmaf_rn(ds_load_elem<HT>(h + k), ds_load_elem<HT>(g + k), acc);
   acc = ds_warp_sumf(acc);
   if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
   __syncthreads();
