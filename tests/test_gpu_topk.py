@@ -134,7 +134,7 @@ def test_full_size_configs(cfg):
 
 @pytest.mark.parametrize("dtype,V", [("bf16", 400000), ("f32", 200000)])
 def test_long_rows(dtype, V):
-    # many chunks per row: the running top-K' list carries across 19 and 38 chunks
+    # long rows: 98 vectors per thread, the tracked maxima and the bound span the whole row
     w = di.lattice_workload(25, R=1, B=3, V_d=V, K=64, rank=8, dtype=dtype, peak=8.0)
     got = run_topk(w["logits"], 3, 64)
     assert got[3] == 0
@@ -154,8 +154,8 @@ def test_long_rows_with_ties_and_constant_rows():
 
 
 def test_many_rows_per_block_with_flooded_rows():
-    # a batch of the Qwen3-4B shape, more rows than resident blocks; some rows flood the survivor
-    # buffer of their first chunk (constant, all -inf, few distinct values) and take the exact cut
+    # a batch of the Qwen3-4B shape in which some rows flood the candidate list with ties at the
+    # bound (constant, all -inf, few distinct values) and take the exact cut
     w = di.lattice_workload(26, R=32, B=7, V_d=151936, K=64, rank=8, peak=8.0)
     s = as_f32(w["logits"]).copy()
     rng = np.random.default_rng(7)
@@ -180,8 +180,9 @@ def test_small_k_and_single_part_rows_in_bulk():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_rising_falling_and_late_peak_rows(dtype):
-    # a rising row: every later chunk beats the running K'-th value everywhere (exact cut each
-    # chunk); a falling row: nothing after the first chunk enters; the peak in the scalar tail
+    # a rising row (the bound comes from the last batch of every thread), a falling row (from the
+    # first), the peak in the scalar tail, and a rising row with long runs of ties (the list
+    # overflows and takes the exact cut)
     V = 100003
     s = np.zeros((4, V), dtype=np.float32)
     s[0] = np.arange(V, dtype=np.float32) / 64.0
@@ -194,3 +195,22 @@ def test_rising_falling_and_late_peak_rows(dtype):
     got = run_topk(data, 4, 64)
     assert got[3] == 0
     assert_same(got, oracle_topk(as_f32(data), 64))
+
+
+@pytest.mark.parametrize("mult,cap", [(1.0, 0.0), (0.37, 0.0), (1.0, 30.0), (0.5, 30.0)])
+def test_no_head_argmax_fast_path(mult, cap):
+    # no Markov head: the output multiplier and soft cap, then the argmax of full-vocabulary rows,
+    # is the Top-K with K = 1 (one streaming pass; the bound is the row maximum)
+    w = di.lattice_workload(29, R=8, B=7, V_d=151936, K=64, rank=8, peak=8.0)
+    s = as_f32(w["logits"])
+    cd, ct, cv, st = run_topk(w["logits"], 7, 1, mult=mult, softcap=cap)
+    assert st == 0
+    cd, cv = cd.reshape(-1), cv.reshape(-1)
+    for i in range(s.shape[0]):
+        x = od.row_transform(s[i], mult, cap)
+        idx, val = od.topk_row(x, 1)
+        if cap == 0.0:
+            assert cd[i] == idx[0] and cv[i] == val[0], f"row {i}"
+        else:                                              # CUDA's tanhf against tanh in double
+            np.testing.assert_allclose(cv[i], val[0], rtol=4e-7, atol=0)
+            assert cd[i] == idx[0] or abs(x[cd[i]] - val[0]) <= 4e-7 * abs(val[0]), f"row {i}"
