@@ -8,10 +8,12 @@
 // (nucleus = shortest prefix of (probability desc, index asc) whose mass exceeds top_p), the
 // double-sum commit and the double-uniform commit; the candidate rank is the row index.
 //
-// One CTA of 256 threads per request. The K'xK' tile of position j + 1 streams into shared
-// memory (cp.async, double buffered) while position j is decided, so the lattice is read once
-// and its latency hides behind the recurrence. Max-sum uses all threads (4 threads per column b,
-// 16 predecessors each); the walks use warp 0 with the row after the previous choice.
+// One CTA of 256 threads per request. The unary scores and candidate ids, then the K'xK' tiles
+// of up to 16 positions at once, are requested together with 16-byte cp.async copies (the next
+// batch as soon as one is consumed), so the lattice is read once and its latency is paid once per
+// batch rather than once per position; odd K' or unaligned lattices take double-buffered tiles.
+// Max-sum uses all threads (4 threads per column b, 16 predecessors each); the walks use warp 0
+// with the row after the previous choice.
 #include "dspark_common.cuh"
 #include "host_common.h"
 
