@@ -177,3 +177,139 @@ def test_dense_walk_with_zero_table_samples_the_raw_rows():
     for j in range(5):
         tok, _ = sample_row(w["logits"][j], 0.9, 0.8, float(uniform(seed, step, j, 0)))
         assert dw["tokens"][j] == tok
+
+
+# ---- row transform: output multiplier, then soft cap ([G] block-sampler commit) ---------------
+
+def test_row_transform_multiplier_is_one_rounded_product():
+    # hand values: products by powers of two are exact; 0.1f * 3 rounds once
+    l = np.array([3.0, -2.5, F32(0.1), 0.0, -0.0], dtype=F32)
+    np.testing.assert_array_equal(od.row_transform(l, mult=0.5), np.array([1.5, -1.25, F32(0.1) / 2, 0.0, 0.0], F32))
+    assert od.row_transform(np.array([F32(0.1)]), mult=3.0)[0] == F32(0.30000001192092896)
+    # a float32 product is exact in double: one rounding of the exact product is the answer
+    rng = np.random.default_rng(21)
+    for mult in (0.75, 1.3, 23.0, 1e-3):
+        x = (rng.standard_normal(5000) * 4).astype(F32)
+        exact = x.astype(F64) * F64(F32(mult))
+        np.testing.assert_array_equal(od.row_transform(x, mult=mult), exact.astype(F32))
+    # identity when neither is set, and the input is not modified
+    x = np.array([1.0, 2.0], dtype=F32)
+    assert od.row_transform(x) is not x or np.array_equal(od.row_transform(x), x)
+    np.testing.assert_array_equal(od.row_transform(x), x)
+
+
+def test_row_transform_soft_cap_hand_values():
+    tanh1 = 0.7615941559557649                              # tanh(1)
+    s = od.row_transform(np.array([2.0, -2.0, 0.0, 1e6, -1e6], dtype=F32), softcap=2.0)
+    np.testing.assert_allclose(s[:2], [2 * tanh1, -2 * tanh1], rtol=2 ** -23)
+    assert s[2] == 0.0 and s[3] == F32(2.0) and s[4] == F32(-2.0)
+    # multiplier first, then the cap: 4 * 0.5 = 2 -> 2 tanh(1)
+    np.testing.assert_allclose(od.row_transform(np.array([4.0], F32), mult=0.5, softcap=2.0), [2 * tanh1],
+                               rtol=2 ** -23)
+    # the cap is 30 tanh(s / 30): s = 30 atanh(1/2) gives 15
+    x = F32(30.0 * math.atanh(0.5))
+    np.testing.assert_allclose(od.row_transform(np.array([x]), softcap=30.0), [15.0], rtol=2 ** -22)
+    # near zero the cap is the identity to first order
+    np.testing.assert_allclose(od.row_transform(np.array([1e-3], F32), softcap=30.0), [1e-3], rtol=1e-6)
+
+
+def test_soft_cap_is_monotone_and_keeps_the_top_k():
+    rng = np.random.default_rng(22)
+    for trial in range(200):
+        x = np.sort((rng.standard_normal(2000) * 6).astype(F32))
+        y = od.row_transform(x, mult=float(rng.choice([1.0, 0.8, 2.5])), softcap=float(rng.choice([5.0, 15.0, 30.0])))
+        assert np.all(np.diff(y.astype(F64)) >= 0)            # order preserving (ties possible when saturated)
+        perm = rng.permutation(2000)
+        xs, ys = x[perm], y[perm]
+        idx_x, _ = od.topk_row(xs, 64)
+        idx_y, vy = od.topk_row(ys, 64)
+        if np.unique(vy).shape[0] == 64 and ys[ys >= vy[-1]].shape[0] == 64:
+            assert list(idx_x) == list(idx_y)
+
+
+# ---- sampled walk ([G] block-sampler commit: a sampled request walks the lattice with its draft RNG) ----
+
+def test_chain_sample_low_temperature_is_the_greedy_walk():
+    rng = np.random.default_rng(23)
+    checked = 0
+    for trial in range(60):
+        B, K = 5, 16
+        u = (rng.standard_normal((B, K)) * 2).astype(F32)
+        A = rng.standard_normal((B, K, K)) * 2
+        rows_ok = True
+        walk, _ = od.chain_walk(u, A)
+        prev = None
+        for j in range(B):                                    # every row on the walk has a clear maximum
+            v = np.sort(od.walk_rows(u, A, prev, j).astype(F64))
+            rows_ok &= (v[-1] - v[-2]) > 0.05
+            prev = walk[j]
+        if not rows_ok:
+            continue
+        chain, _, recs = od.chain_sample(u, A, np.arange(B * K).reshape(B, K), 1e-4, 1.0, 77 + trial, 5)
+        assert list(chain) == list(walk)
+        assert all(r["kept"].shape[0] == 1 for r in recs)     # every other weight is flushed
+        checked += 1
+    assert checked >= 20
+
+
+def test_chain_sample_draws_follow_the_hand_row():
+    # one position, no transitions: the row is T log q for a hand q, so the draws follow q, and
+    # top-p 0.7 keeps {0, 1} (0.5 + 0.25 is the first prefix above 0.7), renormalised to {2/3, 1/3}
+    T = 0.8
+    q = np.array([0.5, 0.25, 0.125, 0.125])
+    u = (T * np.log(q)).astype(F32)[None, :]
+    A = np.zeros((1, 4, 4))
+    ids = np.array([[40, 41, 42, 43]])
+    from scipy import stats
+    for top_p, want in ((1.0, q), (0.7, np.array([2 / 3, 1 / 3, 0.0, 0.0]))):
+        n = 20000
+        counts = np.zeros(4)
+        for s in range(n):
+            chain, _, recs = od.chain_sample(u, A, ids, T, top_p, 1234, s)
+            counts[chain[0]] += 1
+        kept = want > 0
+        assert counts[~kept].sum() == 0
+        exp = want[kept] * n
+        stat = np.sum((counts[kept] - exp) ** 2 / exp)
+        assert stat < stats.chi2.ppf(0.999, kept.sum() - 1), stat
+        np.testing.assert_allclose(recs[0]["q"], want[kept], rtol=1e-6)
+        assert list(recs[0]["ids"]) == list(ids[0][kept])
+
+
+def test_chain_sample_uses_the_position_word_of_the_draft_stream():
+    # p = (1/2, 1/2) at every position: the index-order draw takes rank 1 exactly when u_j >= 1/2,
+    # u_j = U(seed, step, j, purpose 0)
+    from oracle.philox import uniform
+    B = 12
+    u = np.zeros((B, 2), dtype=F32)
+    A = np.zeros((B, 2, 2))
+    ids = np.tile(np.array([7, 9]), (B, 1))
+    varied = 0
+    for seed, step in ((1, 0), (2**40 + 3, 17), (99, 2**33 + 5)):
+        chain, score, _ = od.chain_sample(u, A, ids, 1.0, 1.0, seed, step)
+        want = [int(uniform(seed, step, j, 0) >= 0.5) for j in range(B)]
+        assert list(chain) == want
+        # the pin has teeth: the acceptance stream or the next position's word give other chains
+        assert want != [int(uniform(seed, step, j, 1) >= 0.5) for j in range(B)]
+        assert want != [int(uniform(seed, step, j + 1, 0) >= 0.5) for j in range(B)]
+        varied += len(set(want)) > 1
+    assert varied == 3
+
+
+def test_chain_sample_reads_the_row_after_the_token_before():
+    # A_j[a, b] = 50 exactly when b = a + 3 (mod K): the walk must step by +3 from the first draw
+    # (a transposed lattice would step by -3); with top-p 0.5 the record keeps only the drawn rank
+    rng = np.random.default_rng(24)
+    B, K = 6, 8
+    A = np.zeros((B, K, K))
+    for j in range(1, B):
+        for a in range(K):
+            A[j, a, (a + 3) % K] = 50.0
+    ids = rng.permutation(1000)[:B * K].reshape(B, K)
+    for trial in range(10):
+        u = (rng.standard_normal((B, K)) * 0.5).astype(F32)
+        chain, score, recs = od.chain_sample(u, A, ids, 1.0, 0.5, 5 + trial, 3)
+        for j in range(1, B):
+            assert chain[j] == (chain[j - 1] + 3) % K
+            assert list(recs[j]["ids"]) == [ids[j, chain[j]]]
+        assert abs(score - od.chain_score(u, A, chain)) < 1e-4

@@ -111,3 +111,41 @@ def test_flush_below_minus_64():
     s = np.array([0.0, -63.5, -64.5, -200.0], dtype=F32)
     _, _, w = softmax_weights(s, 1.0)
     assert w[0] == 1 and w[1] > 0 and w[2] == 0 and w[3] == 0
+
+
+def test_dense_q_is_the_distribution_drawn_from():
+    # [G] exact sampled speculative decoding: the record is the post-filter q each token was drawn
+    # from. Rebuilt from a dense record (z, zmax, W_kept, cut), q must equal sample_row's q on the
+    # kept set and vanish elsewhere, ties at the cut included.
+    from oracle.sampling import dense_q
+    rng = np.random.default_rng(31)
+    for trial in range(10000):
+        V = int(rng.integers(2, 64))
+        s = (rng.standard_normal(V) * float(rng.choice([0.5, 2.0, 8.0]))).astype(F32)
+        if trial % 2 == 0:
+            s = np.round(s)                                   # exact ties, also at the cut
+        T = float(rng.choice([0.5, 0.8, 1.0, 1.7]))
+        top_p = float(rng.choice([0.3, 0.5, 0.9, 0.95, 1.0]))
+        tok, rec = sample_row(s, T, top_p, float(rng.random()))
+        dq = dense_q(rec["z"], rec["zmax"], rec["wsum"], rec["w_cut"], rec["i_cut"], np.arange(V))
+        mask = np.zeros(V, dtype=bool)
+        mask[rec["kept"]] = True
+        assert np.all(dq[~mask] == 0.0)
+        assert np.array_equal(dq[mask].astype(F32), rec["q"])
+        assert dq[tok] > 0.0
+        assert abs(dq.sum() - 1.0) < 1e-12
+
+
+def test_dense_q_matches_draw_frequencies():
+    from oracle.sampling import dense_q
+    rng = np.random.default_rng(32)
+    s = np.round(rng.standard_normal(40) * 2).astype(F32)
+    n = 400000
+    _, rec = sample_row(s, 0.9, 0.8, 0.5)
+    u = uniform(3, np.arange(n, dtype=np.uint64), 0, 0)
+    tok, _ = draw_from_weights(rec["w"], rec["kept"], u)      # the draw sample_row makes, vectorised
+    counts = np.bincount(tok, minlength=40).astype(np.float64)
+    dq = dense_q(rec["z"], rec["zmax"], rec["wsum"], rec["w_cut"], rec["i_cut"], np.arange(40))
+    assert counts[dq == 0].sum() == 0
+    ok, stat = chi2_ok(counts, dq)
+    assert ok, stat
