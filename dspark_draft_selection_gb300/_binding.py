@@ -40,8 +40,8 @@ SIGNATURES = [
     ("dspark_dense_walk", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i64,
                                   c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_f32, c_f32, c_f32, c_f32, c_vp, c_vp, c_vp,
                                   c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
-    ("dspark_verify", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i64, c_f32, c_f32,
-                              c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    ("dspark_verify", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_f32,
+                              c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
 ]
 
 
@@ -292,8 +292,8 @@ def dspark_dense_walk(logits, B, prev, E, W, *, R=None, V_d=None, row_start=None
     return out + (status,)
 
 
-def dspark_verify(tgt_logits, B, draft_tgt, n_draft, q, *, V_q=None, R=None, row_start=None, temperature=1.0,
-                  top_p=1.0, vseed=None, step=None, out=None, ws=None, status=None, stream=None):
+def dspark_verify(tgt_logits, B, draft_tgt, n_draft, q, *, V_q=None, q_d2t=None, R=None, row_start=None,
+                  temperature=1.0, top_p=1.0, vseed=None, step=None, out=None, ws=None, status=None, stream=None):
     rows, ld = _rows(tgt_logits)
     V_t = tgt_logits.shape[1]
     R = draft_tgt.shape[0] if R is None else R
@@ -308,7 +308,8 @@ def dspark_verify(tgt_logits, B, draft_tgt, n_draft, q, *, V_q=None, R=None, row
     if V_q is None:
         V_q = q[0].shape[1] if (q is not None and len(q) == 5) else V_t
     _check(lib().dspark_verify(_p(tgt_logits), _dt(tgt_logits), R, B, V_t, ld, _p(row_start), _p(draft_tgt),
-                               _p(n_draft), ctypes.byref(qr) if qr is not None else None, V_q, temperature, top_p,
+                               _p(n_draft), ctypes.byref(qr) if qr is not None else None, V_q, _p(q_d2t),
+                               temperature, top_p,
                                _p(vseed), _p(step), _p(out[0]), _p(out[1]), _p(out[2]), wp, wn, _p(status),
                                _stream(stream)), "dspark_verify")
     return out + (status,)

@@ -1,6 +1,47 @@
-// api.cu - library-wide entry points: workspace sizes and status names.
+// api.cu - library-wide entry points (workspace sizes, status names) and the per-device host
+// caches every entry point shares.
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "dspark_common.cuh"
 #include "host_common.h"
+
+namespace {
+std::mutex ds_cache_mu;
+std::map<int, int> ds_sms_by_device;
+std::map<std::pair<int, const void*>, size_t> ds_smem_by_kernel;
+}  // namespace
+
+int ds_num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  std::lock_guard<std::mutex> lock(ds_cache_mu);
+  auto it = ds_sms_by_device.find(dev);
+  if (it != ds_sms_by_device.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return 148;                                   // not cached: asked again next time
+  }
+  ds_sms_by_device[dev] = n;
+  return n;
+}
+
+cudaError_t ds_ensure_smem(const void* func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(ds_cache_mu);
+  size_t& have = ds_smem_by_kernel[std::make_pair(dev, func)];
+  if (bytes <= have) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 // Per-op workspace layouts are defined next to their kernels; these sizes must cover them.
 extern "C" size_t dspark_internal_ws_sample(int64_t R, int32_t B, int64_t V);

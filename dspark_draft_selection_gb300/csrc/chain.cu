@@ -407,18 +407,12 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   const size_t smem = size_t(ns) * tile + ubytes;
   if (smem > kBudget + 16 * 1024) return DSPARK_EINVAL;
   if (ring) {
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-      DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-      configured = smem;
-    }
+    if (smem > 48 * 1024)
+      DS_CUDA_TRY(ds_ensure_smem(reinterpret_cast<const void*>(chain_kernel<true>), smem));
     chain_kernel<true><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
   } else {
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-      DS_CUDA_TRY(cudaFuncSetAttribute(chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-      configured = smem;
-    }
+    if (smem > 48 * 1024)
+      DS_CUDA_TRY(ds_ensure_smem(reinterpret_cast<const void*>(chain_kernel<false>), smem));
     chain_kernel<false><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
   }
   return ds_launch_status();

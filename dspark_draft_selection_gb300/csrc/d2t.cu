@@ -10,8 +10,6 @@
 // Two passes so that a range error always wins over a duplicate: the range pass, then (only if
 // the status word is still clear) a pass that sets one bit per target id in a workspace bitmap
 // and reports an id whose bit was already set.
-#include <mutex>
-
 #include "dspark_common.cuh"
 #include "host_common.h"
 
@@ -57,34 +55,26 @@ extern "C" dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64
 // Allocation-free variant. Some callers cannot hand the library a device workspace: runtimes that
 // allocate nothing once serving has started, or hosts whose device memory belongs to another
 // allocator. For them the duplicate bitmap is a static array in this library's device image,
-// sized for target vocabularies of up to D2T_NOALLOC_MAX_VT ids (128 KB). Its address is looked
-// up once per device, with that device current, on the first call made there. The bitmap is
-// cleared on the caller's stream at every call; calls that overlap on the GPU share it and race.
+// sized for target vocabularies of up to D2T_NOALLOC_MAX_VT ids (128 KB). Host code cannot use the
+// array's name as a device address, so every call asks the runtime for the array's address in the
+// context current at the call (a host-side query that allocates nothing; the first one on a
+// device loads the module there). The bitmap is cleared on the caller's stream at every call;
+// calls that overlap on the GPU share it and race.
 // ------------------------------------------------------------------------------------------------
 namespace {
 
 constexpr int64_t D2T_NOALLOC_MAX_VT = int64_t(1) << 20;
-constexpr int D2T_NOALLOC_MAX_DEVICES = 64;
 
 __device__ __align__(256) uint32_t d2t_noalloc_bitmap[D2T_NOALLOC_MAX_VT / 32];
 
-std::mutex d2t_noalloc_mu;
-uint32_t* d2t_noalloc_addr[D2T_NOALLOC_MAX_DEVICES] = {};
-
-// The bitmap's address on the current device (set-up on the first call there), or nullptr.
+// The bitmap's device address in the current context, or nullptr.
 uint32_t* d2t_noalloc_bitmap_ptr() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= D2T_NOALLOC_MAX_DEVICES) return nullptr;
-  std::lock_guard<std::mutex> lock(d2t_noalloc_mu);
-  if (d2t_noalloc_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, d2t_noalloc_bitmap) != cudaSuccess || ptr == nullptr) {
-      (void)cudaGetLastError();
-      return nullptr;
-    }
-    d2t_noalloc_addr[dev] = static_cast<uint32_t*>(ptr);
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, d2t_noalloc_bitmap) != cudaSuccess || ptr == nullptr) {
+    (void)cudaGetLastError();
+    return nullptr;
   }
-  return d2t_noalloc_addr[dev];
+  return static_cast<uint32_t*>(ptr);
 }
 
 }  // namespace

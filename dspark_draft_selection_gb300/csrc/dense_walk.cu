@@ -212,12 +212,8 @@ template <typename T, bool XFORM>
 cudaError_t dw_launch_gemm(const DwArgs& a, cudaStream_t stream) {
   auto kern = dense_walk_gemm_kernel<T, XFORM>;
   const size_t smem = size_t(a.rank / 64) * (DW_M + a.Npad) * 128 + 1024;
-  static size_t configured = 0;
-  if (smem > configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  const cudaError_t e = ds_ensure_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   const int per_sm = smem <= 110 * 1024 ? 2 : 1;
   const int64_t grid = std::min<int64_t>(a.ntiles, int64_t(ds_num_sms()) * per_sm);
   kern<<<unsigned(grid), DW_THREADS, smem, stream>>>(a);

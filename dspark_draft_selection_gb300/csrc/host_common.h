@@ -34,13 +34,10 @@ static inline bool ds_aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
 
-static inline int ds_num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-  }
-  return n;
-}
+// Streaming multiprocessors of the current device (cached per device; thread-safe).
+int ds_num_sms();
+
+// Raises `func`'s dynamic shared-memory limit on the current device to at least `bytes` (each
+// (device, kernel) pair is configured once; thread-safe). Kernel attributes are per device, so a
+// process driving several GPUs, or calling from several threads, configures each one it uses.
+cudaError_t ds_ensure_smem(const void* func, size_t bytes);

@@ -275,11 +275,7 @@ extern "C" dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int
                   ds_aligned(E, 16) && ds_aligned(W, 16);
   if (tc) {
     const size_t smem = std::max<size_t>(size_t(rank / 64) * (LT_M + LT_N) * 128, 64 * 65 * 4) + 1024;
-    static size_t configured = 0;
-    if (smem > configured) {
-      DS_CUDA_TRY(cudaFuncSetAttribute(lattice_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-      configured = smem;
-    }
+    DS_CUDA_TRY(ds_ensure_smem(reinterpret_cast<const void*>(lattice_tc_kernel), smem));
     lattice_tc_kernel<<<tiles, LT_THREADS, smem, stream>>>(a);
   } else if (table_dtype == DSPARK_BF16) {
     lattice_fma_kernel<__nv_bfloat16><<<tiles, 256, 0, stream>>>(a);

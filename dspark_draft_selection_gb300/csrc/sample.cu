@@ -189,7 +189,10 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
 
   for (int64_t row_id = blockIdx.x / P; row_id < rows; row_id += gridDim.x / P) {
     const int64_t r = row_id / a.B, j = row_id % a.B;
-    if (a.n_draft && j > a.n_draft[r]) continue;          // every part of the row skips it
+    if (a.n_draft) {                                      // every part of the row skips it
+      const int32_t nd = a.n_draft[r];                    // rows past n, and every row of a request
+      if (nd < 0 || nd > a.B - 1 || j > nd) continue;     // whose n is out of range, are not needed
+    }
     const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
     SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
     if (P > 1) sr_part(g, part, P);
@@ -671,15 +674,8 @@ cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stre
   // the nucleus' candidate keys are only needed with NUC
   const size_t smem = sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0) +
                       (SPQ ? sizeof(uint32_t) * SR_CELLS : 0);
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = ds_ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
   const int per_sm = (NUC || SPQ || XFORM) ? 1 : 2;
   const int64_t slots = int64_t(per_sm) * ds_num_sms();
   if (rows <= 0) return cudaSuccess;

@@ -5,35 +5,45 @@
 // position is checked against the target's post-filter p, accepted with probability min(1, p/q),
 // otherwise a sample of norm(max(0, p - q)) is emitted and the later candidates dropped;
 // accepted tokens report the target's log-probability; ids beyond a model's row have zero
-// probability; sums in double. Commit on the double uniform (acceptance test and draws).
-// Description > Fixes > Split validation windows: row j validates candidate j; row n is the
-// bonus row. This is the speculative sampling rule of Leviathan et al. (2023) and Chen et al.
-// (2023).
+// probability; q is recorded sparse over the kept tokens or dense, in target ids; sums in double.
+// Commit on the double uniform (acceptance test and draws). Description > Fixes > Split
+// validation windows: row j validates candidate j; row n is the bonus row. This is the
+// speculative sampling rule of Leviathan et al. (2023) and Chen et al. (2023).
 //
-// Three launches:
-//  1. the row sampler of sample.cu in statistics mode over every needed target row:
-//     the maximum, the top-p cut and the kept mass of p_j, the weight of the drafted token x_j,
-//     and the argmax (greedy requests). The target logits are read from HBM once here.
-//  2. verify_accept_kernel - one thread per request runs the sequential tests
-//     u_j < p_j(x_j) / q_j(x_j) and leaves at most one draw job (residual at j*, or bonus at n).
-//  3. verify_draw_kernel - one 1024-thread CTA per request with a job re-reads that one row
-//     (and the dense q row), forms rho = max(0, p - q) (or p) scaled by W_p * W_q so that no
-//     element needs a division (float pairs per element, double per warp), and finds the
-//     crossing of u * sum(rho) with per-(round, warp) sums and short scans.
+// Launches:
+//  0. pruned dense records only: the inverse map t2d over the target vocabulary (target id ->
+//     draft index of the record, -1 outside the draft vocabulary).
+//  1. the row sampler of sample.cu in statistics mode over every needed target row: the maximum,
+//     the top-p cut and the kept mass of p_j, the weight of the drafted token x_j, and the argmax
+//     (greedy requests). The target logits are read from HBM once here.
+//  2. verify_accept_kernel - one warp per request, one lane per window position: the tests
+//     u_j < p_j(x_j) / q_j(x_j) of different positions are independent, so every lane decides its
+//     own and the first failing position (a ballot) ends the window. Leaves at most one draw job
+//     per request: the residual at the first rejection, or the bonus draw at n.
+//  3. verify_mass_kernel - every draw row is split into parts of VM_PART ids spread over many
+//     CTAs; each forms rho = max(0, p - q) (p alone for the bonus draw) scaled by W_p * W_q, so no
+//     element needs a division, as float pairs, and writes the mass of every cell of VM_CELL
+//     consecutive ids.
+//  4. verify_pick_kernel - one CTA per job scans its cells in double, finds the cell whose running
+//     sum crosses u * sum(rho), re-evaluates that cell's ids and emits the token.
 #include "host_common.h"
 #include "rowsample.cuh"
 
 namespace {
 
-constexpr int VD_THREADS = 1024;
-constexpr int VD_WARPS = VD_THREADS / 32;
-constexpr int VD_MAXROUNDS = 256;        // rows up to 262,144 ids
-constexpr int VD_SPARSE_MAX = 1024;      // sparse q entries staged per draw
+constexpr int VM_THREADS = 512;            // residual-mass CTAs
+constexpr int VM_WARPS = VM_THREADS / 32;
+constexpr int VM_CELL = 256;               // ids per cell: one warp, eight consecutive ids a lane
+constexpr int VM_PART = 8192;              // ids per mass CTA (32 cells)
+constexpr int VM_CELLS_PER_PART = VM_PART / VM_CELL;
+constexpr int VP_THREADS = 512;            // pick CTAs
 
 enum : int32_t { JOB_NONE = 0, JOB_RESIDUAL = 1, JOB_BONUS = 2 };
+// proposal record forms
+enum : int { QF_NONE = 0, QF_SPARSE = 1, QF_DENSE = 2, QF_DENSE_PRUNED = 3 };
 
 struct VerifyWs {
-  float* zmax;       // [R * (B + 1)]
+  float* zmax;       // [R * (B + 1)] target row statistics
   double* wsum;
   float* wcut;
   int32_t* icut;
@@ -41,6 +51,8 @@ struct VerifyWs {
   int32_t* amax;
   int32_t* job_kind; // [R]
   int32_t* job_j;
+  float2* cells;     // [R, ncell] residual mass per cell (float pair)
+  int32_t* t2d;      // [V] record index of each target id (pruned dense records)
 };
 
 struct VerifyArgs {
@@ -51,7 +63,7 @@ struct VerifyArgs {
   const int32_t* draft_tgt;
   const int32_t* n_draft;
   dspark_qrecord q;
-  int q_dense;
+  int q_form;
   int64_t V_q;
   float T, top_p;
   const uint64_t* vseed;
@@ -60,6 +72,7 @@ struct VerifyArgs {
   int32_t* n_accepted;
   float* logprob;
   int32_t* status;
+  int64_t ncell;
   VerifyWs ws;
 };
 
@@ -67,277 +80,485 @@ DS_DEV bool vf_keep(float w, int64_t i, float wcut, int64_t icut) {
   return w > 0.0f && (w > wcut || (w == wcut && i <= icut));
 }
 
-// q_j(x) from the record (double); ids outside the record's width have probability zero
+// Record index of target id x for a dense record (-1: not in the record)
+DS_DEV int64_t vf_qindex(const VerifyArgs& a, int64_t x) {
+  if (x < 0) return -1;
+  if (a.q_form == QF_DENSE_PRUNED) return x < a.V ? int64_t(a.ws.t2d[x]) : -1;
+  return x < a.V_q ? x : -1;
+}
+
+// Kept weight of record index i of a dense record row
+DS_DEV float vf_wq(const VerifyArgs& a, int64_t qrow, int64_t i) {
+  if (i < 0) return 0.0f;
+  const float w = ds_weight(__fsub_rn(a.q.z[qrow * a.q.ldz + i], a.q.zmax[qrow]));
+  return vf_keep(w, i, a.q.wcut[qrow], a.q.icut[qrow]) ? w : 0.0f;
+}
+
+// q_j(x) from the record (double); ids outside the record have probability zero
 DS_DEV double vf_q(const VerifyArgs& a, int64_t qrow, int64_t x) {
   if (x < 0) return 0.0;
-  if (a.q_dense) {
-    if (x >= a.V_q) return 0.0;
-    const float w = ds_weight(__fsub_rn(a.q.z[qrow * a.q.ldz + x], a.q.zmax[qrow]));
-    return vf_keep(w, x, a.q.wcut[qrow], a.q.icut[qrow]) ? double(w) / a.q.wsum[qrow] : 0.0;
+  if (a.q_form == QF_SPARSE) {
+    const int n = a.q.n[qrow];
+    for (int k = 0; k < n && k < a.q.cap; ++k)
+      if (a.q.ids[qrow * a.q.cap + k] == x) return double(a.q.p[qrow * a.q.cap + k]);
+    return 0.0;
   }
-  const int n = a.q.n[qrow];
-  for (int k = 0; k < n && k < a.q.cap; ++k)
-    if (a.q.ids[qrow * a.q.cap + k] == x) return double(a.q.p[qrow * a.q.cap + k]);
-  return 0.0;
+  const float w = vf_wq(a, qrow, vf_qindex(a, x));
+  return w > 0.0f ? double(w) / a.q.wsum[qrow] : 0.0;
 }
 
-__global__ void verify_accept_kernel(const VerifyArgs a, int64_t R) {
-  const int64_t r = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-  if (r >= R) return;
-  const int B = a.B, n = a.n_draft[r];
-  const int64_t obase = r * (B + 1), rbase = r * (B + 1);
-  const bool greedy = !(a.T > 0.0f);
-  const uint64_t vseed = greedy ? 0 : a.vseed[r], step = greedy ? 0 : a.step[r];
-  int acc = 0;
-  int32_t kind = JOB_BONUS, jj = n;
-  for (int j = 0; j < n; ++j) {
-    const int64_t rid = rbase + j;
-    const int32_t x = a.draft_tgt[r * B + j];
-    const double lw = log(double(a.ws.probe_w[rid])) - log(a.ws.wsum[rid]);
-    if (greedy) {
-      if (x == a.ws.amax[rid]) {
-        a.out_tokens[obase + acc] = x;
-        a.logprob[obase + acc] = float(lw);
-        ++acc;
-        continue;
-      }
-      kind = JOB_RESIDUAL;
-      jj = j;
-      break;
-    }
-    const double qx = vf_q(a, r * B + j, x);
-    if (!(qx > 0.0)) {
-      ds_set_error(a.status, DSPARK_EPROPOSAL);
-      a.n_accepted[r] = -1;
-      for (int k = 0; k <= B; ++k) a.out_tokens[obase + k] = -1;
-      a.ws.job_kind[r] = JOB_NONE;
-      return;
-    }
-    const double px = double(a.ws.probe_w[rid]) / a.ws.wsum[rid];
-    const double ua = ds_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
-    if (ua < px / qx) {
-      a.out_tokens[obase + acc] = x;
-      a.logprob[obase + acc] = float(lw);
-      ++acc;
+__global__ void verify_t2d_kernel(const int64_t* d2t, int64_t V_d, int64_t V_t, int32_t* t2d, int32_t* status) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < V_d; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t t = i + d2t[i];
+    if (t < 0 || t >= V_t) {
+      ds_set_error(status, DSPARK_ERANGE);
       continue;
     }
-    kind = JOB_RESIDUAL;
-    jj = j;
-    break;
-  }
-  a.n_accepted[r] = acc;
-  for (int k = acc + 1; k <= B; ++k) {
-    a.out_tokens[obase + k] = -1;
-    a.logprob[obase + k] = 0.0f;
-  }
-  if (greedy) {
-    // the correction or bonus is the argmax of its row; it reports the temperature-1 log-prob
-    const int64_t rid = rbase + jj;
-    a.out_tokens[obase + acc] = a.ws.amax[rid];
-    a.logprob[obase + acc] = float(-log(a.ws.wsum[rid]));   // the argmax has weight 1
-    a.ws.job_kind[r] = JOB_NONE;
-  } else {
-    a.ws.job_kind[r] = kind;
-    a.ws.job_j[r] = jj;
+    t2d[t] = int32_t(i);
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(VD_THREADS, 1) verify_draw_kernel(const VerifyArgs a) {
-  extern __shared__ __align__(16) float2 s_rwf[];         // [rounds][VD_WARPS] float pairs
-  __shared__ double s_scan[VD_MAXROUNDS];
-  __shared__ double s_wtot[VD_WARPS];
-  __shared__ int32_t s_sid[VD_SPARSE_MAX];
-  __shared__ float s_sq[VD_SPARSE_MAX];
-  __shared__ int s_pick, s_round, s_warp;
-  __shared__ double s_tau;
+// One warp per request.
+__global__ void __launch_bounds__(128) verify_accept_kernel(const VerifyArgs a, int64_t R) {
+  const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;                                      // whole warps leave together
+  const int B = a.B, n = a.n_draft[r];
+  const int64_t obase = r * (B + 1), rbase = r * (B + 1);
+  if (n < 0 || n > B) {                                    // out of contract: an error, no indexing
+    if (lane == 0) {
+      ds_set_error(a.status, DSPARK_EINVAL);
+      a.n_accepted[r] = -1;
+      a.ws.job_kind[r] = JOB_NONE;
+    }
+    for (int k = lane; k <= B; k += 32) {
+      a.out_tokens[obase + k] = -1;
+      a.logprob[obase + k] = 0.0f;
+    }
+    return;
+  }
+  const bool greedy = !(a.T > 0.0f);
+  const uint64_t vseed = greedy ? 0 : a.vseed[r], step = greedy ? 0 : a.step[r];
+  int first = n;                                           // first position that is not accepted
+  bool first_zero_q = false;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    bool ev = false, zq = false;
+    if (j < n) {
+      const int64_t rid = rbase + j;
+      const int32_t x = a.draft_tgt[r * B + j];
+      if (greedy) {
+        ev = x != a.ws.amax[rid];
+      } else {
+        const double qx = vf_q(a, r * B + j, x);
+        zq = !(qx > 0.0);
+        if (!zq) {
+          const double px = double(a.ws.probe_w[rid]) / a.ws.wsum[rid];
+          const double ua = ds_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
+          ev = !(ua < px / qx);
+        }
+        ev = ev || zq;
+      }
+    }
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, ev);
+    if (bal) {
+      const int l = __ffs(bal) - 1;
+      first = j0 + l;
+      first_zero_q = __shfl_sync(0xFFFFFFFFu, zq, l);
+      break;
+    }
+  }
+  if (first_zero_q) {                                      // the proposal gave a drafted token q = 0
+    if (lane == 0) {
+      ds_set_error(a.status, DSPARK_EPROPOSAL);
+      a.n_accepted[r] = -1;
+      a.ws.job_kind[r] = JOB_NONE;
+    }
+    for (int k = lane; k <= B; k += 32) a.out_tokens[obase + k] = -1;
+    return;
+  }
+  const int acc = first;
+  for (int k = lane; k <= B; k += 32) {
+    if (k < acc) {
+      const int64_t rid = rbase + k;
+      a.out_tokens[obase + k] = a.draft_tgt[r * B + k];
+      a.logprob[obase + k] = float(log(double(a.ws.probe_w[rid])) - log(a.ws.wsum[rid]));
+    } else if (k > acc) {
+      a.out_tokens[obase + k] = -1;
+      a.logprob[obase + k] = 0.0f;
+    } else if (greedy) {
+      // the correction or bonus is the argmax of its row; it reports the temperature-1 log-prob
+      // (the argmax has weight 1)
+      const int64_t rid = rbase + acc;
+      a.out_tokens[obase + acc] = a.ws.amax[rid];
+      a.logprob[obase + acc] = float(-log(a.ws.wsum[rid]));
+    }
+  }
+  if (lane == 0) {
+    a.n_accepted[r] = acc;
+    a.ws.job_kind[r] = greedy ? JOB_NONE : (acc < n ? JOB_RESIDUAL : JOB_BONUS);
+    a.ws.job_j[r] = acc;
+  }
+}
 
+// ---- residual masses ---------------------------------------------------------------------------
+// Per job: the target row's statistics and the record row, so that rho'(t) = rho(t) * W_p * W_q
+// needs no division: max(0, w_p(t) W_q - w_q(t) W_p) for a dense q, max(0, w_p(t) - q(t) W_p) for a
+// sparse q, and w_p(t) when drawing from p. Each is a float pair (about 48 significant bits).
+template <typename T>
+struct VfJob {
+  const T* row;
+  float zmax, wcut;
+  int64_t icut;
+  double Wp;
+  float wp_hi, wp_lo, wq_hi, wq_lo;
+  int64_t qrow;
+  bool use_q;
+};
+
+template <typename T>
+DS_DEV VfJob<T> vf_job(const VerifyArgs& a, int64_t r, int j, bool use_q) {
+  VfJob<T> g;
+  const int64_t rid = r * (a.B + 1) + j;
+  const int64_t prow = a.row_start ? a.row_start[r] + j : rid;
+  g.row = reinterpret_cast<const T*>(a.logits) + prow * a.ld;
+  g.zmax = a.ws.zmax[rid];
+  g.wcut = a.ws.wcut[rid];
+  g.icut = a.ws.icut[rid];
+  g.Wp = a.ws.wsum[rid];
+  g.qrow = r * a.B + j;
+  g.use_q = use_q;
+  g.wp_hi = float(g.Wp);
+  g.wp_lo = float(g.Wp - double(g.wp_hi));
+  const double Wq = (use_q && a.q_form >= QF_DENSE) ? a.q.wsum[g.qrow] : 1.0;
+  g.wq_hi = float(Wq);
+  g.wq_lo = float(Wq - double(g.wq_hi));
+  return g;
+}
+
+DS_DEV rs::FF vf_ff_mul(float x, float dh, float dl) {     // x * (dh + dl) as a float pair
+  const float pr = __fmul_rn(x, dh);
+  return rs::FF{pr, __fadd_rn(__fmaf_rn(x, dh, -pr), __fmul_rn(x, dl))};
+}
+
+// rho' of one id from its target weight and its q term (a dense record's kept weight, or a sparse
+// record's probability)
+template <typename T>
+DS_DEV rs::FF vf_rho(const VerifyArgs& a, const VfJob<T>& g, float wp, float qterm) {
+  if (!g.use_q) return rs::FF{wp, 0.0f};
+  rs::FF av, bv;
+  if (a.q_form >= QF_DENSE) {
+    av = vf_ff_mul(wp, g.wq_hi, g.wq_lo);
+    bv = vf_ff_mul(qterm, g.wp_hi, g.wp_lo);
+  } else {
+    av = rs::FF{wp, 0.0f};
+    bv = vf_ff_mul(qterm, g.wp_hi, g.wp_lo);
+  }
+  // a - b with the rounding error of the leading difference kept (2Sum)
+  const float sd = __fsub_rn(av.hi, bv.hi);
+  const float bb = __fsub_rn(sd, av.hi);
+  const float err = __fadd_rn(__fsub_rn(av.hi, __fsub_rn(sd, bb)), __fsub_rn(-bv.hi, bb));
+  const float lo = __fadd_rn(err, __fsub_rn(av.lo, bv.lo));
+  if (!(__fadd_rn(sd, lo) > 0.0f)) return rs::FF{0.0f, 0.0f};
+  return rs::FF{sd, lo};
+}
+
+// Eight consecutive elements t..t+7 of a row (t % 8 == 0), zero past `n`; 16-byte loads when the
+// eight are whole and aligned.
+template <typename T>
+DS_DEV void vf_ld8(const T* p, int64_t t, int64_t n, float (&x)[8]) {
+  const T* q = p + t;
+  if (t + 8 <= n && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q));
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = ds_vec_elem<T>(v, e);
+    } else {
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(q)), v1 = __ldg(reinterpret_cast<const uint4*>(q) + 1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[e] = ds_vec_elem<T>(v0, e);
+        x[e + 4] = ds_vec_elem<T>(v1, e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (t + e < n) ? ds_load_elem<T>(q + e) : 0.0f;
+  }
+}
+
+DS_DEV void vf_ld8_i32(const int32_t* p, int64_t t, int64_t n, int32_t (&x)[8]) {
+  const int32_t* q = p + t;
+  if (t + 8 <= n && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+    const int4 v0 = __ldg(reinterpret_cast<const int4*>(q)), v1 = __ldg(reinterpret_cast<const int4*>(q) + 1);
+    x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+    x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (t + e < n) ? __ldg(q + e) : -1;
+  }
+}
+
+// rho' of the eight ids t..t+7 (zero past V). s_q: a sparse record's q by id, indexed from s_q0.
+template <typename T, int QF>
+DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const float* s_q, int64_t s_q0,
+                    rs::FF (&out)[8]) {
+  float x[8];
+  vf_ld8<T>(g.row, t, a.V, x);
+  float qt[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) qt[e] = 0.0f;
+  if (g.use_q) {
+    if constexpr (QF == QF_SPARSE) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qt[e] = (t + e < a.V) ? s_q[t + e - s_q0] : 0.0f;
+    } else if constexpr (QF == QF_DENSE) {
+      float zq[8];
+      vf_ld8<float>(a.q.z + g.qrow * a.q.ldz, t, a.V_q, zq);
+      const float zm = a.q.zmax[g.qrow], wc = a.q.wcut[g.qrow];
+      const int64_t ic = a.q.icut[g.qrow];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (t + e < a.V_q) {
+          const float w = ds_weight(__fsub_rn(zq[e], zm));
+          qt[e] = vf_keep(w, t + e, wc, ic) ? w : 0.0f;
+        }
+      }
+    } else if constexpr (QF == QF_DENSE_PRUNED) {
+      int32_t ii[8];
+      vf_ld8_i32(a.ws.t2d, t, a.V, ii);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qt[e] = vf_wq(a, g.qrow, ii[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float wp = 0.0f;
+    if (t + e < a.V) {
+      wp = ds_weight(__fsub_rn(ds_temper(x[e], a.T), g.zmax));
+      if (!vf_keep(wp, t + e, g.wcut, g.icut)) wp = 0.0f;
+    }
+    out[e] = vf_rho<T>(a, g, wp, qt[e]);
+  }
+}
+
+DS_DEV void vf_ff_acc(rs::FF& m, const rs::FF& v) {
+  const float lo = __fadd_rn(m.lo, v.lo);
+  m.lo = 0.0f;
+  rs::ff_add(m, v.hi);
+  m.lo = __fadd_rn(m.lo, lo);
+}
+
+// Stages a sparse record's q for ids [lo, lo + len) into s_q (zero elsewhere); whole block.
+DS_DEV void vf_stage_sparse(const VerifyArgs& a, int64_t qrow, int64_t lo, int len, float* s_q) {
+  for (int i = threadIdx.x; i < len; i += blockDim.x) s_q[i] = 0.0f;
+  __syncthreads();
+  const int n = min(a.q.n[qrow], a.q.cap);
+  for (int k = threadIdx.x; k < n; k += blockDim.x) {
+    const int64_t id = a.q.ids[qrow * a.q.cap + k];
+    if (id >= lo && id < lo + len) s_q[id - lo] = a.q.p[qrow * a.q.cap + k];
+  }
+  __syncthreads();
+}
+
+template <typename T, int QF>
+__global__ void __launch_bounds__(VM_THREADS) verify_mass_kernel(const VerifyArgs a) {
+  __shared__ float s_q[QF == QF_SPARSE ? VM_PART : 1];
+  const int64_t r = blockIdx.y;
+  const int32_t kind = a.ws.job_kind[r];
+  if (kind == JOB_NONE) return;
+  const int64_t t0 = int64_t(blockIdx.x) * VM_PART;
+  if (t0 >= a.V) return;
+  const VfJob<T> g = vf_job<T>(a, r, a.ws.job_j[r], kind == JOB_RESIDUAL);
+  if (QF == QF_SPARSE && g.use_q) vf_stage_sparse(a, g.qrow, t0, VM_PART, s_q);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int PER = VM_CELLS_PER_PART / VM_WARPS;       // cells per warp, loads issued together
+  rs::FF v[PER][8];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int64_t t = t0 + int64_t(warp + k * VM_WARPS) * VM_CELL + lane * 8;
+    if (t < a.V) vf_rho8<T, QF>(a, g, t, s_q, t0, v[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int64_t c = t0 / VM_CELL + warp + k * VM_WARPS;
+    if (c * VM_CELL >= a.V) break;                          // warp-uniform
+    const int64_t t = c * VM_CELL + lane * 8;
+    rs::FF m{0.0f, 0.0f};
+    if (t < a.V) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vf_ff_acc(m, v[k][e]);
+    }
+    const rs::FF cw = rs::warp_ff_reduce(m);
+    if (lane == 0) a.ws.cells[r * a.ncell + c] = make_float2(cw.hi, cw.lo);
+  }
+}
+
+template <typename T, int QF>
+__global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArgs a) {
+  __shared__ double s_run[VP_THREADS + 1];
+  __shared__ float s_q[QF == QF_SPARSE ? VM_CELL : 1];
+  __shared__ int64_t s_cell;
+  __shared__ double s_tau;
+  __shared__ int64_t s_pick;
   const int64_t r = blockIdx.x;
   const int32_t kind = a.ws.job_kind[r];
   if (kind == JOB_NONE) return;
-  const int B = a.B, j = a.ws.job_j[r];
+  const int j = a.ws.job_j[r];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t rid = r * (B + 1) + j;
-  const int64_t prow = a.row_start ? a.row_start[r] + j : rid;
-  const T* row = reinterpret_cast<const T*>(a.logits) + prow * a.ld;
-  const float zmax = a.ws.zmax[rid], wcut = a.ws.wcut[rid];
-  const int64_t icut = a.ws.icut[rid];
-  const double wsum = a.ws.wsum[rid];
-  const int64_t qrow = r * B + j;
-  const bool resid = kind == JOB_RESIDUAL;
-  const int64_t V = a.V;
-  const int nrounds = int((V + VD_THREADS - 1) / VD_THREADS);
+  constexpr int WARPS = VP_THREADS / 32;
+  const int64_t ncell = a.ncell;
+  float2* cells = a.ws.cells + r * ncell;
+  VfJob<T> g = vf_job<T>(a, r, j, kind == JOB_RESIDUAL);
 
-  // sparse q of this position, staged (ids are looked up by scan; the record holds few entries)
-  int ns = 0;
-  if (resid && !a.q_dense) {
-    ns = min(a.q.n[qrow], min(a.q.cap, VD_SPARSE_MAX));
-    for (int k = tid; k < ns; k += VD_THREADS) {
-      s_sid[k] = a.q.ids[qrow * a.q.cap + k];
-      s_sq[k] = a.q.p[qrow * a.q.cap + k];
-    }
-    __syncthreads();
-  }
-  auto pval = [&](int64_t t, float* wout) -> double {
-    const float z = ds_temper(ds_load_elem<T>(row + t), a.T);
-    const float w = ds_weight(__fsub_rn(z, zmax));
-    if (wout) *wout = w;
-    return vf_keep(w, t, wcut, icut) ? double(w) / wsum : 0.0;
-  };
-  // Residual masses scaled by W_p * W_q, so that no element needs a division (the draw only
-  // needs the masses up to a common factor): rho'(t) = max(0, w_p(t) W_q - w_q(t) W_p) for a
-  // dense q, max(0, w_p(t) - q(t) W_p) for a sparse q, and w_p(t) when drawing from p. Each is a
-  // float pair (about 48 bits); the double pipe only sees per-warp sums.
-  const double Wq = (resid && a.q_dense) ? a.q.wsum[qrow] : 1.0;
-  const float wp_hi = float(wsum), wp_lo = float(wsum - double(float(wsum)));
-  const float wq_hi = float(Wq), wq_lo = float(Wq - double(float(Wq)));
-  auto ff_mul = [](float x, float dh, float dl) {        // x * (dh + dl) as a float pair
-    const float pr = __fmul_rn(x, dh);
-    return rs::FF{pr, __fadd_rn(__fmaf_rn(x, dh, -pr), __fmul_rn(x, dl))};
-  };
-  auto rho_ff = [&](int64_t t, bool use_q) -> rs::FF {
-    float wp = ds_weight(__fsub_rn(ds_temper(ds_load_elem<T>(row + t), a.T), zmax));
-    if (!vf_keep(wp, t, wcut, icut)) wp = 0.0f;
-    if (!use_q) return rs::FF{wp, 0.0f};
-    rs::FF av, bv;
-    if (a.q_dense) {
-      float wq = 0.0f;
-      if (t < a.V_q) {
-        wq = ds_weight(__fsub_rn(a.q.z[qrow * a.q.ldz + t], a.q.zmax[qrow]));
-        if (!vf_keep(wq, t, a.q.wcut[qrow], a.q.icut[qrow])) wq = 0.0f;
-      }
-      av = ff_mul(wp, wq_hi, wq_lo);
-      bv = ff_mul(wq, wp_hi, wp_lo);
-    } else {
-      float q = 0.0f;
-      for (int k = 0; k < ns; ++k)
-        if (s_sid[k] == t) q = s_sq[k];
-      av = rs::FF{wp, 0.0f};
-      bv = ff_mul(q, wp_hi, wp_lo);
-    }
-    // a - b with the rounding error of the leading difference kept (2Sum)
-    const float sd = __fsub_rn(av.hi, bv.hi);
-    const float bb = __fsub_rn(sd, av.hi);
-    const float err = __fadd_rn(__fsub_rn(av.hi, __fsub_rn(sd, bb)), __fsub_rn(-bv.hi, bb));
-    const float lo = __fadd_rn(err, __fsub_rn(av.lo, bv.lo));
-    if (!(__fadd_rn(sd, lo) > 0.0f)) return rs::FF{0.0f, 0.0f};
-    return rs::FF{sd, lo};
-  };
-  auto rho = [&](int64_t t, bool use_q) -> double { return rs::ff_value(rho_ff(t, use_q)); };
-
-  const double u = ds_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
-  bool use_q = resid;
+  // this thread's contiguous run of cells: its mass, the mass before it, the row's total
+  const int64_t per = (ncell + VP_THREADS - 1) / VP_THREADS;
+  const int64_t c0 = min(ncell, tid * per), c1 = min(ncell, c0 + per);
+  double mine = 0.0, before = 0.0, total = 0.0;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // per-(round, warp) sums in index order
-    // four rounds at a time: their masses are formed first (all loads in flight together), then
-    // summed per warp
-    for (int k0 = 0; k0 < nrounds; k0 += 4) {
-      rs::FF f[4];
+    rs::FF mf{0.0f, 0.0f};
+    for (int64_t c = c0; c < c1; ++c) {
+      const float2 cv = cells[c];
+      vf_ff_acc(mf, rs::FF{cv.x, cv.y});
+    }
+    mine = rs::ff_value(mf);
+    // exclusive prefix over threads (staged, scanned by warp 0)
+    s_run[tid] = mine;
+    __syncthreads();
+    if (tid < 32) {
+      constexpr int PT = VP_THREADS / 32;
+      double loc = 0.0;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t t = int64_t(k0 + u) * VD_THREADS + tid;
-        f[u] = (k0 + u < nrounds && t < V) ? rho_ff(t, use_q) : rs::FF{0.0f, 0.0f};
-      }
+      for (int q = 0; q < PT; ++q) loc += s_run[lane * PT + q];
+      double incl = loc;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (k0 + u >= nrounds) break;
-        const rs::FF v = rs::warp_ff_reduce(f[u]);          // kept as a float pair (no FP64 here)
-        if (lane == 0) s_rwf[(k0 + u) * VD_WARPS + warp] = make_float2(v.hi, v.lo);
+      for (int o = 1; o < 32; o <<= 1) {
+        const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += nb;
       }
+      double run = incl - loc;
+#pragma unroll
+      for (int q = 0; q < PT; ++q) {
+        const double x = s_run[lane * PT + q];
+        s_run[lane * PT + q] = run;
+        run += x;
+      }
+      if (lane == 31) s_run[VP_THREADS] = incl;
     }
     __syncthreads();
-    // round totals in float pairs, one double per round, and their running sums
-    for (int k = tid; k < nrounds; k += VD_THREADS) {
-      rs::FF sum{0.0f, 0.0f};
-      for (int w = 0; w < VD_WARPS; ++w) {
-        const float2 c = s_rwf[k * VD_WARPS + w];
-        const float lo = __fadd_rn(sum.lo, c.y);
-        sum.lo = 0.0f;
-        rs::ff_add(sum, c.x);
-        sum.lo = __fadd_rn(sum.lo, lo);
-      }
-      s_scan[k] = rs::ff_value(sum);
-    }
+    before = s_run[tid];
+    total = s_run[VP_THREADS];
     __syncthreads();
-    if (tid == 0) {
-      double accum = 0.0;
-      for (int k = 0; k < nrounds; ++k) {
-        const double nx = accum + s_scan[k];
-        s_scan[k] = accum;                 // exclusive prefix
-        accum = nx;
-      }
-      s_wtot[0] = accum;
-    }
-    __syncthreads();
-    const double total = s_wtot[0];
     if (total > 0.0 || attempt == 1) break;
-    use_q = false;                         // the residual has no mass (rounding): draw from p
-    __syncthreads();
+    // the residual has no mass (possible only through rounding): draw from p, whose cells this CTA
+    // recomputes over the whole row (rare)
+    g.use_q = false;
+    for (int64_t c = warp; c < ncell; c += WARPS) {
+      const int64_t t = c * VM_CELL + lane * 8;
+      rs::FF v[8];
+      rs::FF m{0.0f, 0.0f};
+      if (t < a.V) {
+        vf_rho8<T, QF>(a, g, t, s_q, 0, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vf_ff_acc(m, v[e]);
+      }
+      const rs::FF cw = rs::warp_ff_reduce(m);
+      if (lane == 0) cells[c] = make_float2(cw.hi, cw.lo);
+    }
+    __syncthreads();                                       // global writes are visible block-wide
   }
-  const double total = s_wtot[0];
+
+  // the crossing cell: the first whose running sum exceeds u * total
+  const double u = ds_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
   const double target = u * total;
   if (tid == 0) {
-    int kr = -1, kw = -1;
-    double tau = 0.0;
-    for (int k = 0; k < nrounds && kr < 0; ++k) {
-      const double next = (k + 1 < nrounds) ? s_scan[k + 1] : total;
-      if (!(target < next)) continue;                  // the crossing is in a later round
-      double acc = s_scan[k];
-      for (int w = 0; w < VD_WARPS; ++w) {
-        const double cw = double(s_rwf[k * VD_WARPS + w].x) + double(s_rwf[k * VD_WARPS + w].y);
-        const double nx = acc + cw;
-        if (target < nx && cw > 0.0) {
-          kr = k;
-          kw = w;
-          tau = target - acc;
-          break;
-        }
-        acc = nx;
-      }
-    }
-    s_round = kr;
-    s_warp = kw;
-    s_tau = tau;
+    s_cell = -1;
     s_pick = -1;
   }
   __syncthreads();
-  if (s_round >= 0 && warp == s_warp) {
-    const int64_t t = int64_t(s_round) * VD_THREADS + tid;
-    const double v = (t < V) ? rho(t, use_q) : 0.0;
-    double incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double nn = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += nn;
+  if (mine > 0.0 && target >= before && target < before + mine) {
+    double acc = before;
+    for (int64_t c = c0; c < c1; ++c) {
+      const double cv = double(cells[c].x) + double(cells[c].y);
+      if (cv > 0.0 && target < acc + cv) {
+        s_cell = c;
+        s_tau = target - acc;
+        break;
+      }
+      acc += cv;
     }
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, v > 0.0 && incl > s_tau);
-    const unsigned pos = __ballot_sync(0xFFFFFFFFu, v > 0.0);
-    if (lane == 0) s_pick = hit ? int(s_round * VD_THREADS + warp * 32 + __ffs(hit) - 1)
-                               : (pos ? int(s_round * VD_THREADS + warp * 32 + 31 - __clz(int(pos))) : -1);
+  }
+  __syncthreads();
+  if (tid == 0 && s_cell < 0) {                            // rounding: the last cell with mass
+    for (int64_t c = ncell - 1; c >= 0; --c)
+      if (double(cells[c].x) + double(cells[c].y) > 0.0) {
+        s_cell = c;
+        s_tau = INFINITY;
+        break;
+      }
+  }
+  __syncthreads();
+  const int64_t cell = s_cell;
+  if (cell >= 0) {
+    if (QF == QF_SPARSE && g.use_q) vf_stage_sparse(a, g.qrow, cell * VM_CELL, VM_CELL, s_q);
+    if (warp == 0) {
+      const int64_t t = cell * VM_CELL + lane * 8;
+      const double tau = s_tau;
+      rs::FF v[8];
+      double rv[8], ls = 0.0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = rs::FF{0.0f, 0.0f};
+      if (t < a.V) vf_rho8<T, QF>(a, g, t, s_q, cell * VM_CELL, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        rv[e] = rs::ff_value(v[e]);
+        ls += rv[e];
+      }
+      double incl = ls;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      const double ex = incl - ls;
+      const unsigned withm = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+      const int lastl = withm ? 31 - __clz(int(withm)) : -1;
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, ls > 0.0 && tau >= ex && tau < incl);
+      const int hl = hit ? __ffs(hit) - 1 : lastl;
+      if (lane == hl) {
+        double run = ex;
+        int64_t pick = -1, last = -1;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (pick < 0 && rv[e] > 0.0) {
+            run += rv[e];
+            last = t + e;
+            if (run > tau) pick = t + e;
+          }
+        }
+        s_pick = pick >= 0 ? pick : last;
+      }
+    }
   }
   __syncthreads();
   if (tid == 0) {
-    int64_t pick = s_pick;
-    if (pick < 0) {
-      // the target fell past the last boundary by rounding: the last id with positive mass
-      for (int64_t t = V - 1; t >= 0; --t)
-        if (rho(t, use_q) > 0.0) {
-          pick = t;
-          break;
-        }
-    }
+    const int64_t pick = s_pick;
     const int acc = a.n_accepted[r];
     float w = 0.0f;
-    if (pick >= 0) pval(pick, &w);
-    a.out_tokens[r * (B + 1) + acc] = int32_t(pick);
-    a.logprob[r * (B + 1) + acc] = float(log(double(w)) - log(wsum));
+    if (pick >= 0) {
+      const float x = ds_load_elem<T>(g.row + pick);
+      w = ds_weight(__fsub_rn(ds_temper(x, a.T), g.zmax));
+    }
+    a.out_tokens[r * (a.B + 1) + acc] = int32_t(pick);
+    a.logprob[r * (a.B + 1) + acc] = float(log(double(w)) - log(g.Wp));
   }
 }
 
 size_t vf_align(size_t x) { return (x + 255) & ~size_t(255); }
 
-VerifyWs vf_layout(void* base, int64_t R, int32_t B, size_t* total) {
+VerifyWs vf_layout(void* base, int64_t R, int32_t B, int64_t V, size_t* total) {
   const size_t rows = size_t(R) * (B + 1);
+  const size_t ncell = size_t((V + VM_CELL - 1) / VM_CELL);
   uint8_t* p = reinterpret_cast<uint8_t*>(base);
   size_t off = 0;
   VerifyWs w = {};
@@ -354,44 +575,67 @@ VerifyWs vf_layout(void* base, int64_t R, int32_t B, size_t* total) {
   w.amax = reinterpret_cast<int32_t*>(take(rows * 4));
   w.job_kind = reinterpret_cast<int32_t*>(take(size_t(R) * 4));
   w.job_j = reinterpret_cast<int32_t*>(take(size_t(R) * 4));
+  w.cells = reinterpret_cast<float2*>(take(size_t(R) * ncell * sizeof(float2)));
+  w.t2d = reinterpret_cast<int32_t*>(take(size_t(V) * 4));
   *total = off;
   return w;
+}
+
+template <typename T, int QF>
+cudaError_t vf_launch_draws(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
+  const dim3 mgrid(unsigned((a.V + VM_PART - 1) / VM_PART), unsigned(R));
+  verify_mass_kernel<T, QF><<<mgrid, VM_THREADS, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  verify_pick_kernel<T, QF><<<unsigned(R), VP_THREADS, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t vf_launch_draws_any(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
+  switch (a.q_form) {
+    case QF_SPARSE: return vf_launch_draws<T, QF_SPARSE>(a, R, stream);
+    case QF_DENSE: return vf_launch_draws<T, QF_DENSE>(a, R, stream);
+    default: return vf_launch_draws<T, QF_DENSE_PRUNED>(a, R, stream);
+  }
 }
 
 }  // namespace
 
 extern "C" size_t dspark_internal_ws_verify(int64_t R, int32_t B, int64_t V) {
-  (void)V;
   size_t total = 0;
-  vf_layout(nullptr, R, B, &total);
+  vf_layout(nullptr, R, B, V, &total);
   return total;
 }
 
 extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_t,
                                        int64_t ld, const int64_t* row_start, const int32_t* draft_tgt,
                                        const int32_t* n_draft, const dspark_qrecord* q, int64_t V_q,
-                                       float temperature, float top_p, const uint64_t* vseed, const uint64_t* step,
-                                       int32_t* out_tokens, int32_t* n_accepted, float* logprob, void* ws,
-                                       size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
+                                       const int64_t* q_d2t, float temperature, float top_p, const uint64_t* vseed,
+                                       const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted, float* logprob,
+                                       void* ws, size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
   DS_REQUIRE(ds_dtype_ok(dtype) && R >= 0 && B >= 1 && B <= 100 && V_t >= 1 && ld >= V_t);
-  DS_REQUIRE(V_t <= int64_t(VD_MAXROUNDS) * VD_THREADS && R * (B + 1) <= 0x7FFFFFFF);
+  DS_REQUIRE(V_t <= 0x7FFFFFFF && R * (B + 1) <= 0x7FFFFFFF);
   DS_REQUIRE(tgt_logits && draft_tgt && n_draft && out_tokens && n_accepted && logprob && dev_status);
   DS_REQUIRE(ds_aligned(tgt_logits, ds_dtype_size(dtype)));
   DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f);
   const bool greedy = !(temperature > 0.0f);
-  int q_dense = 0;
+  int q_form = QF_NONE;
   if (!greedy) {
     DS_REQUIRE(vseed && step && q);
     if (q->z) {
-      DS_REQUIRE(q->zmax && q->wsum && q->wcut && q->icut && q->ldz >= V_q && V_q >= 1);
-      q_dense = 1;
+      DS_REQUIRE(q->zmax && q->wsum && q->wcut && q->icut && q->ldz >= V_q && V_q >= 1 && V_q <= 0x7FFFFFFF);
+      q_form = q_d2t ? QF_DENSE_PRUNED : QF_DENSE;
     } else {
-      DS_REQUIRE(q->ids && q->p && q->n && q->cap >= 1);
+      DS_REQUIRE(q->ids && q->p && q->n && q->cap >= 1 && !q_d2t);
+      q_form = QF_SPARSE;
     }
   }
+  const int C = rs::cluster_size_for(V_t, ds_dtype_size(dtype));
+  DS_REQUIRE(C > 0);
   if (R == 0) return DSPARK_OK;
   size_t need = 0;
-  vf_layout(nullptr, R, B, &need);
+  vf_layout(nullptr, R, B, V_t, &need);
   if (!ws || ws_bytes < need || !ds_aligned(ws, 256)) return DSPARK_EWORKSPACE;
   VerifyArgs a = {};
   a.logits = tgt_logits;
@@ -402,7 +646,7 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   a.draft_tgt = draft_tgt;
   a.n_draft = n_draft;
   if (q) a.q = *q;
-  a.q_dense = q_dense;
+  a.q_form = q_form;
   a.V_q = V_q;
   a.T = temperature;
   a.top_p = top_p;
@@ -412,7 +656,16 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   a.n_accepted = n_accepted;
   a.logprob = logprob;
   a.status = dev_status;
-  a.ws = vf_layout(ws, R, B, &need);
+  a.ncell = (V_t + VM_CELL - 1) / VM_CELL;
+  a.ws = vf_layout(ws, R, B, V_t, &need);
+
+  // 0. inverse map of a pruned dense record
+  if (q_form == QF_DENSE_PRUNED) {
+    DS_CUDA_TRY(cudaMemsetAsync(a.ws.t2d, 0xFF, size_t(V_t) * sizeof(int32_t), stream));
+    const unsigned blocks = unsigned(std::min<int64_t>(ds_ceil_div(V_q, 256), int64_t(ds_num_sms()) * 8));
+    verify_t2d_kernel<<<blocks, 256, 0, stream>>>(q_d2t, V_q, V_t, a.ws.t2d, dev_status);
+    DS_CUDA_TRY(cudaGetLastError());
+  }
 
   // 1. statistics of every needed target row
   rs::SampleArgs sa = {};
@@ -422,8 +675,7 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.row_start = row_start;
   sa.row_mul = 1;
   sa.B = B + 1;
-  sa.C = rs::cluster_size_for(V_t, ds_dtype_size(dtype));
-  DS_REQUIRE(sa.C > 0);
+  sa.C = C;
   sa.mult = 1.0f;
   sa.softcap = 0.0f;
   sa.T = greedy ? 1.0f : temperature;
@@ -444,26 +696,15 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.amax_out = greedy ? a.ws.amax : nullptr;
   DS_CUDA_TRY(rs::sample_rows(sa, R * (B + 1), dtype == DSPARK_BF16, 0, stream));
 
-  // 2. sequential acceptance tests, one thread per request
-  verify_accept_kernel<<<unsigned((R + 127) / 128), 128, 0, stream>>>(a, R);
+  // 2. acceptance tests, one warp per request
+  verify_accept_kernel<<<unsigned((R * 32 + 127) / 128), 128, 0, stream>>>(a, R);
   DS_CUDA_TRY(cudaGetLastError());
 
-  // 3. residual or bonus draws
+  // 3-4. residual or bonus draws
   if (!greedy) {
-    const int nrounds = int((V_t + VD_THREADS - 1) / VD_THREADS);
-    const size_t smem = size_t(nrounds) * VD_WARPS * sizeof(double);
-    static size_t configured[2] = {0, 0};
-    const int di = dtype == DSPARK_BF16 ? 0 : 1;
-    if (smem > configured[di]) {
-      if (di == 0)
-        DS_CUDA_TRY(cudaFuncSetAttribute(verify_draw_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-      else
-        DS_CUDA_TRY(cudaFuncSetAttribute(verify_draw_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-      configured[di] = smem;
-    }
-    if (di == 0) verify_draw_kernel<__nv_bfloat16><<<unsigned(R), VD_THREADS, smem, stream>>>(a);
-    else verify_draw_kernel<float><<<unsigned(R), VD_THREADS, smem, stream>>>(a);
-    DS_CUDA_TRY(cudaGetLastError());
+    const cudaError_t e = dtype == DSPARK_BF16 ? vf_launch_draws_any<__nv_bfloat16>(a, R, stream)
+                                               : vf_launch_draws_any<float>(a, R, stream);
+    DS_CUDA_TRY(e);
   }
   return DSPARK_OK;
 }

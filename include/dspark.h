@@ -136,9 +136,10 @@ dspark_status dspark_d2t_check(const int64_t* d2t, int64_t V_d, int64_t V_t,
  * counterpart: this is a library convenience, not part of the method.
  * The duplicate bitmap is a static 128 KB array in the library's device image, so V_t is
  * limited to 1,048,576 target ids; a larger V_t returns DSPARK_EINVAL before any launch.
- * The first call on a device (with that device current) looks up the array's address; make
- * that first call before any stream capture. Every call clears the bitmap on `stream` before
- * use. Calls that overlap on the GPU share the bitmap and race: serialise them (one stream, or
+ * Every call looks up the array's address in the context current at the call (so a device
+ * reset or another context is followed); the first call on a device also loads the library's
+ * device code there, so make that first call before any stream capture. Every call clears the
+ * bitmap on `stream` before use. Calls that overlap on the GPU share the bitmap and race: serialise them (one stream, or
  * events). d2t: device pointer to V_d int64 offsets; *dev_status as for dspark_d2t_check.
  */
 dspark_status dspark_d2t_check_noalloc(const int64_t* d2t, int64_t V_d, int64_t V_t,
@@ -253,31 +254,38 @@ dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtype, int64_t 
 
 /*
  * Rejection-sampling verification [G: commit on exact sampled speculative decoding -
- * accept with probability min(1, p/q), otherwise emit a sample of norm(max(0, p - q)) and
+ * accept with probability min(1, p/q), otherwise emit a draw from norm(max(0, p - q)) and
  * drop the later candidates; accepted tokens report the target's log-probability; ids
- * beyond a model's row have zero probability; Fixes > split validation windows - row j
- * validates candidate j, row n is the bonus row].
+ * beyond a model's row have zero probability; q is recorded in target ids, sparse or dense;
+ * Fixes > split validation windows - row j validates candidate j, row n is the bonus row].
  * tgt_logits: [rows, ld] of `dtype`; request r owns rows row_start[r] + j, j <= B (B + 1
  * rows; row_start NULL means r * (B + 1)). draft_tgt [R, B] int32 target ids, n_draft [R]
- * int32 (0..B). q: the proposal record of the drafted tokens, one record row per (r, j)
- * at r * B + j: sparse (ids in target space) or dense over draft indices with the
- * identity map (V_q = its width; ids >= V_q have q = 0). Ignored when temperature <= 0.
+ * int32 in 0..B; a request whose n is outside 0..B gets n_accepted = -1 and every
+ * out_tokens entry -1, with DSPARK_EINVAL on *dev_status (nothing of it is indexed).
+ * q: the proposal record of the drafted tokens, one record row per (r, j) at r * B + j:
+ *   sparse - ids in target space, any number of entries up to cap per row;
+ *   dense  - over record indices i < V_q (the record's width). With q_d2t == NULL index i
+ *            is target id i (ids >= V_q have q = 0); with q_d2t (int64 [V_q], one-to-one)
+ *            index i is target id i + q_d2t[i] (a pruned draft vocabulary), and target ids
+ *            outside its image have q = 0. q_d2t must be NULL for a sparse record.
+ * q is ignored when temperature <= 0.
  * p_j is the post-filter target distribution at (temperature, top_p). For j < n: accept
  * iff U(vseed[r], step[r], j, 1) < p_j(x_j)/q_j(x_j) (double); first rejection: emit a
  * draw from norm(max(0, p_j - q_j)) with U(..., j, 2) and stop; all accepted: bonus draw
  * from p_n with U(..., n, 2). temperature <= 0: accept iff x_j == argmax p_j, emit argmax.
  * Outputs: out_tokens [R, B+1] (accepted tokens then the correction or bonus; -1 after),
- * n_accepted [R] (-1 with DSPARK_EPROPOSAL when q(x_j) = 0), logprob [R, B+1] float32
- * (log p_j of each emitted token; greedy reports the temperature-1 log-probability).
+ * n_accepted [R] (-1 with DSPARK_EPROPOSAL when the first position that is not accepted has
+ * q(x_j) = 0), logprob [R, B+1] float32 (log p_j of each emitted token; greedy reports the
+ * temperature-1 log-probability).
  * ws: dspark_workspace_size(DSPARK_OP_VERIFY, R, B, V_t, 0).
  */
 dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B,
                             int64_t V_t, int64_t ld, const int64_t* row_start,
                             const int32_t* draft_tgt, const int32_t* n_draft,
-                            const dspark_qrecord* q, int64_t V_q, float temperature,
-                            float top_p, const uint64_t* vseed, const uint64_t* step,
-                            int32_t* out_tokens, int32_t* n_accepted, float* logprob,
-                            void* ws, size_t ws_bytes, int32_t* dev_status,
+                            const dspark_qrecord* q, int64_t V_q, const int64_t* q_d2t,
+                            float temperature, float top_p, const uint64_t* vseed,
+                            const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted,
+                            float* logprob, void* ws, size_t ws_bytes, int32_t* dev_status,
                             dspark_stream_t stream);
 
 #ifdef __cplusplus

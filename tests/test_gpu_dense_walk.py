@@ -95,5 +95,12 @@ def test_dense_walk_without_record_and_many_requests():
 
 
 def test_dense_walk_full_size_config():
-    w = di.config5(R=8)
-    assert check(w, w["temperature"], w["top_p"], reqs=[0, 3, 7]) <= 1
+    # the benchmarked shape: 64 requests (MMA N = 64), 15 positions, V = 151,936; requests from the
+    # first and the last 32-column epilogue chunks
+    w = di.config5()
+    assert check(w, w["temperature"], w["top_p"], reqs=[0, 17, 31, 32, 48, 63]) <= 1
+
+
+def test_dense_walk_full_size_greedy():
+    w = di.config5()
+    assert check(w, 0.0, 1.0, reqs=[5, 40, 63], record=False) <= 1

@@ -170,6 +170,29 @@ def test_chain_sample_pruned_config_full_size():
             assert qn[r, j] == n and np.array_equal(qp[r, j, :n], rec["q"])
         # every drafted token is in the draft vocabulary's image
         assert np.all(np.isin(got["chain_tgt"][r], w["subset"]))
+    # the full-size pruned lattice against the oracle (rows gathered from the 248,100-row tables)
+    for r in (0, 7, 15):
+        check_lattice_rows(w, got, r)
+
+
+def check_lattice_rows(w, got, r):
+    """Lattice values of request r against the oracle, gathering only the table rows it uses."""
+    B = w["B"]
+    ct = got["cand_tgt"][r]
+    ids = np.unique(np.concatenate([ct.ravel(), [int(w["prev"][r])]]))
+    pos = {int(t): k for k, t in enumerate(ids)}
+    E = as_f32(w["E"][ids]).astype(np.float64)
+    W = as_f32(w["W"][ids]).astype(np.float64)
+    loc = np.vectorize(lambda t: pos[int(t)])(ct)
+    ref = od.lattice_request(loc, pos[int(w["prev"][r])], E, W, [1.0] * B)
+    absdot = np.zeros_like(ref)
+    absdot[0, 0] = np.abs(E[pos[int(w["prev"][r])]]) @ np.abs(W[loc[0]]).T
+    for j in range(1, B):
+        absdot[j] = np.abs(E[loc[j - 1]]) @ np.abs(W[loc[j]]).T
+    bound = 1.01 * E.shape[1] * 2.0 ** -24 * absdot + 1e-6 * absdot
+    err = np.abs(got["trans"][r] - ref)
+    assert np.all(err <= bound), r
+    assert np.all(err <= 1e-3 * np.abs(ref) + 1e-5 * np.abs(ref).max())
 
 
 def test_gated_config_lattice_sampled_rows():
