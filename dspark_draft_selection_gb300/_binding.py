@@ -33,6 +33,9 @@ SIGNATURES = [
                             c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_lattice_score", c_i32, [c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
                                      c_i32, c_i32, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    ("dspark_lattice_chain", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
+                                     c_i32, c_i32, c_i64, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    ("dspark_test_set_first_wait_polls", None, [ctypes.c_uint32]),
     ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_vp, c_vp, c_vp,
                                     c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_sample", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_i64, c_f32, c_f32, c_f32, c_f32,
@@ -221,6 +224,34 @@ def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature
                                      ctypes.byref(q) if q is not None else None, _p(status), _stream(stream)),
            "dspark_chain_select")
     return out + qt + (status,)
+
+
+def dspark_lattice_chain(cand_val, cand_tgt, prev, E, W, mode="maxsum", *, hidden=None, g=None, row_start=None,
+                         trans=None, gate=None, out=None, status=None, stream=None):
+    """Lattice + greedy chain (max-sum or walk) in one call; trans/gate are written only if given."""
+    R, B, K = cand_tgt.shape
+    V_t, rank = E.shape
+    dev = cand_tgt.device
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if out is None:
+        out = (torch.empty((R, B), dtype=torch.int32, device=dev), torch.empty((R, B), dtype=torch.int32, device=dev),
+               torch.empty((R,), dtype=torch.float32, device=dev))
+    status = new_status(dev) if status is None else status
+    if hidden is not None:
+        _, ldh = _rows(hidden)
+        H, hdt = hidden.shape[1], _dt(hidden)
+    else:
+        ldh, H, hdt = 0, 0, DSPARK_BF16
+    _check(lib().dspark_lattice_chain(_p(cand_val), _p(cand_tgt), _p(prev), R, B, K, _p(E), _p(W), _dt(E), V_t, rank,
+                                      _p(hidden), _p(g), hdt, H, ldh, _p(row_start), m, _p(trans), _p(gate),
+                                      _p(out[0]), _p(out[1]), _p(out[2]), _p(status), _stream(stream)),
+           "dspark_lattice_chain")
+    return out + (status,)
+
+
+def dspark_test_set_first_wait_polls(polls: int) -> None:
+    """Test hook: poll limit of the first tensor-core completion wait (0xFFFFFFFF: default)."""
+    lib().dspark_test_set_first_wait_polls(polls)
 
 
 def dense_record(rows: int, V: int, device="cuda"):

@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 
   const int r = blockIdx.x, K = a.K, B = a.B, t = threadIdx.x;
   const int KK = K * K;
+  ds_pdl_trigger();
+  ds_pdl_wait();                                   // the lattice and candidates come from before
   const int KKp = (KK + 3) & ~3;
   const int NS = RING ? a.ns : 2;
   float* s_tile0 = ch_dyn;
@@ -409,11 +411,11 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   if (ring) {
     if (smem > 48 * 1024)
       DS_CUDA_TRY(ds_ensure_smem(reinterpret_cast<const void*>(chain_kernel<true>), smem));
-    chain_kernel<true><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
+    DS_CUDA_TRY(ds_launch(chain_kernel<true>, dim3(unsigned(R)), dim3(CH_THREADS), smem, stream, a));
   } else {
     if (smem > 48 * 1024)
       DS_CUDA_TRY(ds_ensure_smem(reinterpret_cast<const void*>(chain_kernel<false>), smem));
-    chain_kernel<false><<<unsigned(R), CH_THREADS, smem, stream>>>(a);
+    DS_CUDA_TRY(ds_launch(chain_kernel<false>, dim3(unsigned(R)), dim3(CH_THREADS), smem, stream, a));
   }
   return ds_launch_status();
 }

@@ -40,6 +40,7 @@ struct DwArgs {
   float* z;
   int64_t ldz, z_row_mul, z_row_add;
   int32_t* status;
+  uint32_t first_wait;       // polls of the first MMA-completion wait of a tile
 };
 
 template <bool XFORM>
@@ -158,10 +159,10 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
       ds_umma_commit(&s_bar);
     }
     __syncwarp();
-    bool ok = ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);
+    bool ok = ds_mbar_wait(&s_bar, phase, a.first_wait);
     if (!ok) {
       ds_set_error(a.status, DSPARK_ETIMEOUT);
-      ok = ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);   // let in-flight MMAs drain
+      (void)ds_mbar_wait(&s_bar, phase, DS_WAIT_LIMIT);  // let in-flight MMAs drain; the CTA stops
     }
     ok = __syncthreads_and(ok) != 0;                     // one verdict for the whole CTA
     alive = ok;
@@ -295,6 +296,7 @@ extern "C" dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtyp
     a.softcap = softcap;
     a.Tz = temperature > 0.0f ? temperature : 1.0f;
     a.status = dev_status;
+    a.first_wait = g_ds_first_wait_polls.load(std::memory_order_relaxed);
     if (record) {
       a.z = q->z + c0 * B * q->ldz;
       a.ldz = q->ldz;

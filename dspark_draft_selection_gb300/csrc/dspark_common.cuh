@@ -22,6 +22,17 @@ DS_DEV void ds_set_error(int32_t* status, int32_t code) {
 }
 
 // ----------------------------------------------------------------------------------------
+// programmatic dependent launch: every library kernel lets the next kernel on its stream launch
+// as soon as all of its own CTAs are running (trigger), and waits for the previous kernel to
+// complete, with its memory visible, before it reads any buffer a library call writes and before
+// it writes anything (wait). Before the wait a kernel reads only the caller's model inputs
+// (logits, hidden states, head tables, d2t, row starts). Without a programmatic launch both are
+// no-ops.
+// ----------------------------------------------------------------------------------------
+DS_DEV void ds_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DS_DEV void ds_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------------------
 // element access
 // ----------------------------------------------------------------------------------------
 DS_DEV float ds_bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
@@ -126,6 +137,56 @@ DS_DEV float ds_weight(float d) {
   p = __fmaf_rn(p, f, 1.0f);
   const int ni = int(n);                           // -93 <= n <= 0: 2^n is a normal float
   return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+// ---- packed float32 pairs (sm_100 family f32x2): each lane is one IEEE round-to-nearest
+// operation, so a packed evaluation gives the same bits as two scalar ones ----
+DS_DEV uint64_t ds_f2(float lo, float hi) {
+  return (uint64_t(__float_as_uint(hi)) << 32) | uint64_t(__float_as_uint(lo));
+}
+DS_DEV float ds_f2lo(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+DS_DEV float ds_f2hi(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+DS_DEV uint64_t ds_fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+DS_DEV uint64_t ds_mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+DS_DEV uint64_t ds_add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+DS_DEV uint64_t ds_sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ds_weight of two exponents at once, with the same bits: rint(t) is taken by adding and removing
+// 1.5 * 2^23 (round to nearest, ties to even, for |t| < 2^22), and 2^n * P(f) by adding n to the
+// exponent field of P(f) (P(f) in [0.70, 1.42] and n >= -93, so the result is a normal float);
+// the integer n sits in the low mantissa bits of t + 1.5 * 2^23, so (bits << 23) is n << 23.
+DS_DEV float2 ds_weight2(float d0, float d1) {
+  const uint64_t M = ds_f2(12582912.0f, 12582912.0f);
+  const uint64_t t = ds_mul2(ds_f2(d0, d1), ds_f2(0x1.715476p+0f, 0x1.715476p+0f));
+  const uint64_t tm = ds_add2(t, M);
+  const uint64_t f = ds_sub2(t, ds_sub2(tm, M));
+  uint64_t p = ds_f2(0x1.ffcbfcp-17f, 0x1.ffcbfcp-17f);
+  p = ds_fma2(p, f, ds_f2(0x1.430912p-13f, 0x1.430912p-13f));
+  p = ds_fma2(p, f, ds_f2(0x1.5d87fep-10f, 0x1.5d87fep-10f));
+  p = ds_fma2(p, f, ds_f2(0x1.3b2ab6p-7f, 0x1.3b2ab6p-7f));
+  p = ds_fma2(p, f, ds_f2(0x1.c6b08ep-5f, 0x1.c6b08ep-5f));
+  p = ds_fma2(p, f, ds_f2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
+  p = ds_fma2(p, f, ds_f2(0x1.62e430p-1f, 0x1.62e430p-1f));
+  p = ds_fma2(p, f, ds_f2(1.0f, 1.0f));
+  const uint32_t w0 = uint32_t(p) + (uint32_t(tm) << 23);
+  const uint32_t w1 = uint32_t(p >> 32) + (uint32_t(tm >> 32) << 23);
+  return make_float2((d0 >= -64.0f) ? __uint_as_float(w0) : 0.0f, (d1 >= -64.0f) ? __uint_as_float(w1) : 0.0f);
 }
 
 // z = s / T in float32 (the identity for T == 1)
@@ -269,6 +330,32 @@ DS_DEV void ds_bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, ui
       "l"(gmem_src), "r"(bytes), "r"(ds_smem_addr(bar))
       : "memory");
 }
+
+// --- thread-block clusters ---
+// Address of the same shared-memory location in CTA `rank` of the cluster (shared::cluster window).
+DS_DEV uint32_t ds_mapa(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// Bulk copy from this CTA's shared memory to another CTA's shared memory in the cluster
+// (16-byte aligned, size a multiple of 16), completing `bytes` on the destination's mbarrier.
+DS_DEV void ds_bulk_s2s_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes, uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+
+// Waits until this thread's bulk copies have finished reading their sources.
+DS_DEV void ds_bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Makes an mbarrier initialisation visible to the other CTAs of the cluster.
+DS_DEV void ds_fence_mbar_init_cluster() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
 DS_DEV void ds_fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -28,6 +28,34 @@ DS_DEV void ff_add(FF& a, float b) {
   a.lo = __fadd_rn(a.lo, err);
 }
 DS_DEV double ff_value(const FF& a) { return double(a.hi) + double(a.lo); }
+DS_DEV void ff_acc(FF& m, const FF& v) {   // m += v for float pairs
+  const float lo = __fadd_rn(m.lo, v.lo);
+  m.lo = 0.0f;
+  ff_add(m, v.hi);
+  m.lo = __fadd_rn(m.lo, lo);
+}
+
+// Two float-pair accumulators in packed float32 registers (lanes of the f32x2 operations): the
+// same 2Sum steps as ff_add on two independent sums at once.
+struct FF2 {
+  uint64_t hi, lo;
+};
+DS_DEV void ff2_add(FF2& a, uint64_t b) {
+  const uint64_t s = ds_add2(a.hi, b);
+  const uint64_t bb = ds_sub2(s, a.hi);
+  const uint64_t err = ds_add2(ds_sub2(a.hi, ds_sub2(s, bb)), ds_sub2(b, bb));
+  a.hi = s;
+  a.lo = ds_add2(a.lo, err);
+}
+// The two lanes folded into one float pair.
+DS_DEV FF ff2_fold(const FF2& a) {
+  FF r{ds_f2lo(a.hi), ds_f2lo(a.lo)};
+  const float lo = __fadd_rn(r.lo, ds_f2hi(a.lo));
+  r.lo = 0.0f;
+  ff_add(r, ds_f2hi(a.hi));
+  r.lo = __fadd_rn(r.lo, lo);
+  return r;
+}
 
 // Sum of a float pair over a warp in float pairs (FP32 shuffles and 2Sum only; every lane gets
 // it). The GPU's FP64 pipe is narrow, so callers convert the result once per warp, not per lane.

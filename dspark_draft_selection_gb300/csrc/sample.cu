@@ -14,8 +14,8 @@
 // exchange their maxima and masses through distributed shared memory. The row streams through
 // the block in passes (16-byte loads, several chunks in flight per thread; repeated passes mostly
 // hit L2): the maximum of z = s / T (and the dense record's z row), the nucleus when top-p < 1
-// (threshold rounds with the candidates sorted in shared memory; a 64-step bisection over
-// (weight, index) keys when they overflow), then the kept mass of every cell of 32 vectors as a
+// (a radix select on the weight bits by mass, then the few weights of the crossing digit sorted in
+// shared memory), then the kept mass of every cell of 32 vectors as a
 // float pair (2Sum), turned into double once per thread rather than once per cell, since the
 // FP64 pipe is costly per warp instruction. A block scan over the cells locates the one whose
 // running sum crosses u * W_kept; its warp re-reads those 32 vectors and finds the lane, then
@@ -31,7 +31,7 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int SP_CAP = 4096;   // nucleus candidates sorted in the leader CTA
+constexpr int SP_CAP = 1024;   // nucleus candidates sorted at the cut
 
 
 
@@ -57,6 +57,8 @@ constexpr int SR_U = 4;                      // chunks loaded together by a thre
 constexpr int SR_MAXCHUNK = 128;             // rows of up to 128 x 512 vectors
 constexpr int SR_CELLS = SR_MAXCHUNK * SR_WARPS;
 constexpr int SR_MAXP = 8;                   // parts (cluster blocks) per row
+// nucleus scratch: candidate keys, then 16 digit accumulators (float pair + count) per thread
+constexpr size_t SP_NUC_BYTES = sizeof(uint64_t) * SP_CAP + size_t(16) * SR_THREADS * (sizeof(float2) + sizeof(uint32_t));
 
 template <typename T>
 struct SrRow {
@@ -168,13 +170,18 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
   extern __shared__ __align__(16) uint8_t dsm[];
   double* s_cell = reinterpret_cast<double*>(dsm);                        // [SR_CELLS] per-cell values
   float2* s_cellf = reinterpret_cast<float2*>(dsm);                       // ... as float pairs
-  // per-cell counts of a sparse record, after the nucleus keys
-  uint32_t* s_cnt32 = reinterpret_cast<uint32_t*>(dsm + sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0));
+  // nucleus scratch after the cells: candidate keys [SP_CAP], then per-thread digit masses and
+  // counts; per-cell counts of a sparse record after that
   uint64_t* s_keys = reinterpret_cast<uint64_t*>(dsm + sizeof(double) * SR_CELLS);   // [SP_CAP]
+  uint8_t* s_nuc = dsm + sizeof(double) * SR_CELLS + sizeof(uint64_t) * SP_CAP;
+  uint32_t* s_cnt32 = reinterpret_cast<uint32_t*>(dsm + sizeof(double) * SR_CELLS + (NUC ? SP_NUC_BYTES : 0));
   __shared__ rs::BlockScratch bs;
   __shared__ uint32_t s_cnt;
   __shared__ int s_cellpick;
   __shared__ double s_tau, s_cut[2];
+  __shared__ double s_digm[16];
+  __shared__ uint32_t s_digc[16];
+  __shared__ int s_cutk;
   // exchange slots of the row's parts (a cluster of P blocks), one per part
   __shared__ float s_xf[SR_MAXP];
   __shared__ unsigned long long s_xu[SR_MAXP];
@@ -261,84 +268,151 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       }
       auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
 
-      // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order ----
+      // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order. A radix
+      // select on the weight bits by mass: each pass sorts the weights that match the digits fixed
+      // so far into 16 digit buckets (per-thread float-pair masses and counts in shared memory, so
+      // the sums are deterministic), and the digit where the mass from the top crosses top_p * W
+      // is fixed. Once that digit holds at most SP_CAP weights they are sorted by (weight desc,
+      // index asc) and cut by a block scan. Only more than SP_CAP equal weights at the cut (a
+      // flat row) fall back to a bisection over (weight, index) keys ----
       if (NUC && a.top_p < 1.0f) {
-        rs::FF acc{0.0f, 0.0f};
-        sr_pass(g, [&](float raw, int64_t, int) { rs::ff_add(acc, wof(raw)); }, [](int) {});
-        const double wall = rs::block_sum_ff(acc, bs);
-        const double tp = double(a.top_p);
-        for (int round = 0; round < 4; ++round) {
-          const float tau = round == 0 ? ds_weight(-10.0f) : round == 1 ? ds_weight(-20.0f)
-                          : round == 2 ? ds_weight(-40.0f) : FLT_MIN;
-          rs::FF m{0.0f, 0.0f};
-          double cnt = 0.0;
+        float2* s_accm = reinterpret_cast<float2*>(s_nuc);                    // [16][SR_THREADS]
+        uint32_t* s_accc = reinterpret_cast<uint32_t*>(s_accm + 16 * SR_THREADS);
+        uint32_t prefix = 0, pmask = 0, dcount = 0;
+        double above = 0.0, target = 0.0;
+        int shift = 30;                                // weights <= 1: bit 30 and up are zero
+        bool first = true;
+        while (true) {
+          const int width = min(4, shift);
+          shift -= width;
+          const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+          for (int d = 0; d < 16; ++d) {
+            s_accm[d * SR_THREADS + tid] = make_float2(0.0f, 0.0f);
+            s_accc[d * SR_THREADS + tid] = 0u;
+          }
           sr_pass(g,
                   [&](float raw, int64_t, int) {
                     const float w = wof(raw);
-                    if (w >= tau) {
-                      rs::ff_add(m, w);
-                      cnt += 1.0;
+                    const uint32_t kb = __float_as_uint(w);
+                    if (w > 0.0f && (kb & pmask) == prefix) {
+                      const int o = int((kb >> shift) & dmask) * SR_THREADS + tid;
+                      const float2 m = s_accm[o];
+                      rs::FF f{m.x, m.y};
+                      rs::ff_add(f, w);
+                      s_accm[o] = make_float2(f.hi, f.lo);
+                      s_accc[o] += 1u;
                     }
                   },
                   [](int) {});
-          const double mass = rs::block_sum_ff(m, bs);
-          const double ncand = rs::block_sum(cnt, bs);
-          if (round < 3 && !(mass / wall > tp + 1e-12)) continue;
-          if (ncand <= double(SP_CAP)) {
-            // the candidates (a prefix of the sorted order), sorted, walked in order
-            if (tid == 0) s_cnt = 0;
-            __syncthreads();
+          __syncthreads();
+          {                                            // digit `warp`'s mass and count
+            rs::FF f{0.0f, 0.0f};
+            uint32_t c = 0;
+            for (int k = lane; k < SR_THREADS; k += 32) {
+              const float2 m = s_accm[warp * SR_THREADS + k];
+              const float lo = __fadd_rn(f.lo, m.y);
+              f.lo = 0.0f;
+              rs::ff_add(f, m.x);
+              f.lo = __fadd_rn(f.lo, lo);
+              c += s_accc[warp * SR_THREADS + k];
+            }
+            f = rs::warp_ff_reduce(f);
+            c = __reduce_add_sync(0xFFFFFFFFu, c);
+            if (lane == 0) {
+              s_digm[warp] = rs::ff_value(f);
+              s_digc[warp] = c;
+            }
+          }
+          __syncthreads();
+          if (first) {                                 // the first pass sees every positive weight
+            double W = 0.0;
+            for (int d = 0; d < 16; ++d) W += s_digm[d];
+            target = double(a.top_p) * W;
+            first = false;
+          }
+          // the digit where the running mass from the top first exceeds the target (rounding can
+          // leave it unreached: then the lowest non-empty digit)
+          int dsel = -1;
+          double run = above;
+          for (int d = int(dmask); d >= 0; --d) {
+            if (s_digc[d] == 0u) continue;
+            if (run + s_digm[d] > target) {
+              dsel = d;
+              break;
+            }
+            run += s_digm[d];
+          }
+          if (dsel < 0) {
+            run = above;
+            for (int d = int(dmask); d >= 0; --d) {
+              if (s_digc[d] == 0u) continue;
+              dsel = d;
+              run += s_digm[d];
+            }
+            run -= s_digm[dsel];
+          }
+          above = run;
+          prefix |= uint32_t(dsel) << shift;
+          pmask |= dmask << shift;
+          dcount = s_digc[dsel];
+          __syncthreads();                             // digit totals are rewritten next pass
+          if (dcount <= uint32_t(SP_CAP) || shift == 0) break;
+        }
+        if (dcount <= uint32_t(SP_CAP)) {
+          // the weights of the selected digit, sorted, and the first whose running mass crosses
+          if (tid == 0) s_cnt = 0;
+          __syncthreads();
+          sr_pass(g,
+                  [&](float raw, int64_t i, int) {
+                    const float w = wof(raw);
+                    if (w > 0.0f && (__float_as_uint(w) & pmask) == prefix) {
+                      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+                      if (slot < uint32_t(SP_CAP)) s_keys[slot] = ds_key64(w, uint32_t(i));
+                    }
+                  },
+                  [](int) {});
+          __syncthreads();
+          const int n = int(min(s_cnt, uint32_t(SP_CAP)));
+          int n2 = 1;
+          while (n2 < n) n2 <<= 1;
+          for (int i = n + tid; i < n2; i += SR_THREADS) s_keys[i] = 0;
+          if (tid == 0) s_cutk = n - 1;                // rounding: the last one
+          __syncthreads();
+          ds_block_sort_desc(s_keys, n2);
+          const int k0 = 2 * tid;
+          const double w0 = k0 < n ? double(ds_key64_val(s_keys[k0])) : 0.0;
+          const double w1 = k0 + 1 < n ? double(ds_key64_val(s_keys[k0 + 1])) : 0.0;
+          double tot = 0.0;
+          const double before = above + rs::block_exclusive_scan(w0 + w1, &tot, bs);
+          if (k0 < n && before + w0 > target) atomicMin(&s_cutk, k0);
+          else if (k0 + 1 < n && before + w0 + w1 > target) atomicMin(&s_cutk, k0 + 1);
+          __syncthreads();
+          if (tid == 0) {
+            const uint64_t kc = s_keys[max(s_cutk, 0)];
+            s_cut[0] = double(ds_key64_val(kc));
+            s_cut[1] = double(ds_key64_idx(kc));
+          }
+        } else {
+          // more than SP_CAP equal weights at the cut: the largest (weight, index) key whose upper
+          // set has mass above the target, by bisection over the 64 key bits
+          unsigned long long res = 0;
+          for (int b = 63; b >= 0; --b) {
+            const unsigned long long cand = res | (1ull << b);
+            rs::FF mm{0.0f, 0.0f};
             sr_pass(g,
                     [&](float raw, int64_t i, int) {
                       const float w = wof(raw);
-                      if (w >= tau) {
-                        const uint32_t slot = atomicAdd(&s_cnt, 1u);
-                        if (slot < SP_CAP) s_keys[slot] = ds_key64(w, uint32_t(i));
-                      }
+                      if ((unsigned long long)ds_key64(w, uint32_t(i)) >= cand) rs::ff_add(mm, w);
                     },
                     [](int) {});
-            __syncthreads();
-            const int n = int(min(s_cnt, uint32_t(SP_CAP)));
-            int n2 = 1;
-            while (n2 < n) n2 <<= 1;
-            for (int i = n + tid; i < n2; i += SR_THREADS) s_keys[i] = 0;
-            __syncthreads();
-            ds_block_sort_desc(s_keys, n2);
-            if (tid == 0) {
-              double cum = 0.0;
-              s_cut[0] = 0.0;
-              s_cut[1] = -1.0;
-              for (int k = 0; k < n; ++k) {
-                const float w = ds_key64_val(s_keys[k]);
-                cum += double(w) / wall;
-                if (cum > tp) {
-                  s_cut[0] = double(w);
-                  s_cut[1] = double(ds_key64_idx(s_keys[k]));
-                  break;
-                }
-              }
-            }
-          } else {
-            // bisection for the largest (weight, index) key whose upper set has mass > top_p
-            unsigned long long res = 0;
-            for (int b = 63; b >= 0; --b) {
-              const unsigned long long cand = res | (1ull << b);
-              rs::FF mm{0.0f, 0.0f};
-              sr_pass(g,
-                      [&](float raw, int64_t i, int) {
-                        const float w = wof(raw);
-                        if ((unsigned long long)ds_key64(w, uint32_t(i)) >= cand) rs::ff_add(mm, w);
-                      },
-                      [](int) {});
-              const double mb = rs::block_sum_ff(mm, bs);
-              if (mb / wall > tp) res = cand;
-            }
-            if (tid == 0) {
-              s_cut[0] = double(ds_key64_val(res));
-              s_cut[1] = double(ds_key64_idx(res));
-            }
+            const double mb = rs::block_sum_ff(mm, bs);
+            if (mb > target) res = cand;
           }
-          break;
+          if (tid == 0) {
+            s_cut[0] = double(ds_key64_val(res));
+            s_cut[1] = double(ds_key64_idx(res));
+          }
         }
         __syncthreads();
         wcut = float(s_cut[0]);
@@ -672,7 +746,7 @@ template <typename T, bool XFORM, bool NUC, bool SPQ>
 cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
   auto kern = sample_row_kernel<T, XFORM, NUC, SPQ>;
   // the nucleus' candidate keys are only needed with NUC
-  const size_t smem = sizeof(double) * SR_CELLS + (NUC ? sizeof(uint64_t) * SP_CAP : 0) +
+  const size_t smem = sizeof(double) * SR_CELLS + (NUC ? SP_NUC_BYTES : 0) +
                       (SPQ ? sizeof(uint32_t) * SR_CELLS : 0);
   const cudaError_t e = ds_ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

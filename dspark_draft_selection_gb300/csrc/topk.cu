@@ -12,8 +12,9 @@
 // the row's 16-byte vectors t, t + 512, t + 1024, ..., so each batch of the CTA is one contiguous
 // stretch of the row and every load is coalesced. The logits go from HBM to registers once;
 // nothing is staged in shared memory and no barrier falls inside the stream.
-//  1. Stream: each thread loads its vectors in batches of 8 and keeps the keys (vector maximum,
-//     vector number) of its 6 largest vectors, sorted, with a branch-free min/max network.
+//  1. Stream: each thread loads its vectors in two alternating half-batches of 4 (one in flight
+//     while the other is folded in) and keeps the keys (vector maximum, vector number) of its 6
+//     largest vectors, sorted, with a branch-free min/max network.
 //  2. Bound: each warp pops its m = ceil(2K'/16) largest tracked maxima (REDUX rounds) and one
 //     warp finds T, the K'-th largest pop, by a bisection over the value key. The pops are maxima
 //     of distinct vectors, so K' distinct elements are >= T and every top-K' element is >= T.
@@ -25,6 +26,8 @@
 //     lower index first); the first K' ranks are written in order with the d2t map.
 //  5. A list that overflows its 2048 slots (ties at T, as in a constant row) is cut exactly by a
 //     bisection over the 64 key bits, counting the whole row once per bit.
+// Launched with programmatic dependent launch: the stream of the logits may overlap the previous
+// kernel on the stream; the candidates are written only after that kernel has completed.
 #include <type_traits>
 
 #include "dspark_common.cuh"
@@ -283,6 +286,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
   __shared__ uint32_t s_n, s_tv;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  ds_pdl_trigger();
+  bool waited = false;                                     // the previous kernel's completion
   for (int64_t row_id = blockIdx.x; row_id < a.rows; row_id += gridDim.x) {
     const TkRow g = tk_row<T>(a, uint32_t(row_id));
     const T* row = reinterpret_cast<const T*>(g.row);
@@ -295,18 +300,21 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
     else if (tid >= 8 && tid - 8 < a.V - g.tail0) iextra = g.tail0 + (tid - 8);
     const float xextra = iextra >= 0 ? tk_xform<XFORM>(ds_load_elem<T>(row + iextra), a.mult, a.softcap) : -INFINITY;
 
-    // ---- 1. stream: the six largest vectors of the thread ----
-    constexpr int TK_BATCH = KK::narrow ? 8 : 4;            // vectors in flight per thread
+    // ---- 1. stream: the six largest vectors of the thread. Two half-batches alternate, so one is
+    // always in flight while the other is folded into the tracked keys ----
+    constexpr int TK_HALF = KK::narrow ? 4 : 2;             // vectors per half-batch
     K t[TK_TRACK];
 #pragma unroll
     for (int i = 0; i < TK_TRACK; ++i) t[i] = 0;
-    for (int j0 = 0; j0 < nvt; j0 += TK_BATCH) {
-      uint4 w[TK_BATCH];
+    uint4 wa[TK_HALF], wb[TK_HALF];
+    auto load = [&](uint4 (&w)[TK_HALF], int j0) {
 #pragma unroll
-      for (int u = 0; u < TK_BATCH; ++u)
+      for (int u = 0; u < TK_HALF; ++u)
         if (j0 + u < nvt) w[u] = __ldg(rv + (tid + int64_t(j0 + u) * TK_THREADS));
+    };
+    auto fold = [&](const uint4 (&w)[TK_HALF], int j0) {
 #pragma unroll
-      for (int u = 0; u < TK_BATCH; ++u) {
+      for (int u = 0; u < TK_HALF; ++u) {
         if (j0 + u < nvt) {
           K x = KK::make(tk_vec_max<T, XFORM>(w[u], a.mult, a.softcap), uint32_t(j0 + u));
 #pragma unroll
@@ -317,6 +325,14 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
           }
         }
       }
+    };
+    load(wa, 0);
+    load(wb, TK_HALF);
+    for (int j0 = 0; j0 < nvt; j0 += 2 * TK_HALF) {
+      fold(wa, j0);
+      load(wa, j0 + 2 * TK_HALF);
+      fold(wb, j0 + TK_HALF);
+      load(wb, j0 + 3 * TK_HALF);
     }
 
     // ---- 2. bound: each warp pops its m largest tracked maxima, m = ceil(2K' / warps holding
@@ -421,6 +437,10 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
       }
     }
     __syncthreads();
+    if (!waited) {                                         // the logits were read before it; the
+      ds_pdl_wait();                                       // outputs are written after it
+      waited = true;
+    }
     if (tid < a.Kp) {
       if (uint32_t(tid) < N) {
         tk_emit(a, uint32_t(row_id), tid, s_top[tid]);
@@ -440,8 +460,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2) topk_row_kernel(const TopkArgs 
 template <typename T, bool XFORM, bool SHORT>
 cudaError_t tk_launch(const TopkArgs& a, cudaStream_t stream) {
   const int grid = int(std::min<int64_t>(a.rows, int64_t(2) * ds_num_sms()));
-  topk_row_kernel<T, XFORM, SHORT><<<unsigned(grid), TK_THREADS, 0, stream>>>(a);
-  return cudaGetLastError();
+  return ds_launch(topk_row_kernel<T, XFORM, SHORT>, dim3(unsigned(grid)), dim3(TK_THREADS), 0, stream, a);
 }
 
 }  // namespace

@@ -13,9 +13,10 @@
 // Launches:
 //  0. pruned dense records only: the inverse map t2d over the target vocabulary (target id ->
 //     draft index of the record, -1 outside the draft vocabulary).
-//  1. the row sampler of sample.cu in statistics mode over every needed target row: the maximum,
-//     the top-p cut and the kept mass of p_j, the weight of the drafted token x_j, and the argmax
-//     (greedy requests). The target logits are read from HBM once here.
+//  1. statistics of every needed target row: the maximum, the top-p cut and the kept mass of p_j,
+//     the weight of the drafted token x_j, and the argmax (greedy requests) - verify_stats_kernel
+//     when there is no nucleus, else the row sampler of sample.cu in statistics mode. The target
+//     logits are read from HBM once here.
 //  2. verify_accept_kernel - one warp per request, one lane per window position: the tests
 //     u_j < p_j(x_j) / q_j(x_j) of different positions are independent, so every lane decides its
 //     own and the first failing position (a ballot) ends the window. Leaves at most one draw job
@@ -118,10 +119,150 @@ __global__ void verify_t2d_kernel(const int64_t* d2t, int64_t V_d, int64_t V_t, 
   }
 }
 
+// ---- statistics of the target rows (no nucleus: top_p >= 1, or greedy) --------------------------
+// One CTA per row at a time, persistent over rows, several CTAs per SM. Pass 1 takes the row's
+// maximum over the raw 16-byte vectors (the maximum of z = s / T is fl(max s / T) for T > 0);
+// pass 2 (the row again, mostly from L2) sums the weights of z - zmax with the packed weight
+// function into two float pairs per thread, and finds the argmax of greedy rows. The probed
+// drafted token's weight is evaluated once.
+constexpr int VS_THREADS = 256;
+constexpr int VS_WARPS = VS_THREADS / 32;
+constexpr int VS_PER_SM = 3;
+
+template <typename T>
+DS_DEV float vs_vec_max(const uint4& v) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    return fmaxf(__low2float(m), __high2float(m));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(const VerifyArgs a, int64_t rows) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int BATCH = 8;
+  __shared__ float s_f[VS_WARPS];
+  __shared__ double s_d[VS_WARPS];
+  __shared__ uint32_t s_u[VS_WARPS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool greedy = !(a.T > 0.0f);
+  const float Tz = greedy ? 1.0f : a.T;
+  ds_pdl_trigger();
+  ds_pdl_wait();                                   // drafted tokens and counts may come from before
+  for (int64_t rid = blockIdx.x; rid < rows; rid += gridDim.x) {
+    const int64_t r = rid / (a.B + 1);
+    const int j = int(rid - r * (a.B + 1));
+    const int32_t n = a.n_draft[r];
+    if (n < 0 || n > a.B || j > n) continue;       // not needed (or an error the accept kernel reports)
+    const int64_t prow = a.row_start ? a.row_start[r] + j : rid;
+    const T* row = reinterpret_cast<const T*>(a.logits) + prow * a.ld;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    int64_t head = int64_t(((16u - (addr & 15u)) & 15u) / sizeof(T));
+    if (head > a.V) head = a.V;
+    const int64_t nvec = (a.V - head) / EPV, tail0 = head + nvec * EPV;
+    const uint4* rv = reinterpret_cast<const uint4*>(row + head);
+    // pass 1: the maximum of the raw values
+    float mx = -INFINITY;
+    if (tid < head) mx = ds_load_elem<T>(row + tid);
+    if (tid < a.V - tail0) mx = fmaxf(mx, ds_load_elem<T>(row + tail0 + tid));
+    for (int64_t v0 = tid; v0 < nvec; v0 += int64_t(BATCH) * VS_THREADS) {
+      uint4 w[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u)
+        if (v0 + u * VS_THREADS < nvec) w[u] = __ldg(rv + v0 + u * VS_THREADS);
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u)
+        if (v0 + u * VS_THREADS < nvec) mx = fmaxf(mx, vs_vec_max<T>(w[u]));
+    }
+    mx = ds_warp_max(mx);
+    if (lane == 0) s_f[warp] = mx;
+    __syncthreads();
+    float rmax = s_f[0];
+#pragma unroll
+    for (int k = 1; k < VS_WARPS; ++k) rmax = fmaxf(rmax, s_f[k]);
+    const float zmax = ds_temper(rmax, Tz);
+    if (!(zmax > -INFINITY && zmax < INFINITY)) {
+      if (tid == 0) ds_set_error(a.status, DSPARK_ENONFINITE);
+      __syncthreads();
+      continue;
+    }
+    // pass 2: the sum of the weights (two float pairs per thread) and the argmax of greedy rows
+    rs::FF2 acc{0, 0};
+    rs::FF sc{0.0f, 0.0f};
+    uint32_t amin = 0xFFFFFFFFu;
+    auto scalar = [&](int64_t i) {
+      const float z = ds_temper(ds_load_elem<T>(row + i), Tz);
+      rs::ff_add(sc, ds_weight(__fsub_rn(z, zmax)));
+      if (greedy && z == zmax) amin = min(amin, uint32_t(i));
+    };
+    if (tid < head) scalar(tid);
+    if (tid < a.V - tail0) scalar(tail0 + tid);
+    for (int64_t v0 = tid; v0 < nvec; v0 += int64_t(4) * VS_THREADS) {
+      uint4 w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * VS_THREADS < nvec) w[u] = __ldg(rv + v0 + u * VS_THREADS);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t v = v0 + u * VS_THREADS;
+        if (v < nvec) {
+#pragma unroll
+          for (int e = 0; e < EPV; e += 2) {
+            const float z0 = ds_temper(ds_vec_elem<T>(w[u], e), Tz), z1 = ds_temper(ds_vec_elem<T>(w[u], e + 1), Tz);
+            const float2 w2 = ds_weight2(__fsub_rn(z0, zmax), __fsub_rn(z1, zmax));
+            rs::ff2_add(acc, ds_f2(w2.x, w2.y));
+            if (greedy) {
+              const uint32_t i0 = uint32_t(head + v * EPV + e);
+              if (z0 == zmax) amin = min(amin, i0);
+              if (z1 == zmax) amin = min(amin, i0 + 1);
+            }
+          }
+        }
+      }
+    }
+    rs::FF f = rs::ff2_fold(acc);
+    rs::ff_acc(f, sc);
+    f = rs::warp_ff_reduce(f);
+    amin = __reduce_min_sync(0xFFFFFFFFu, amin);
+    if (lane == 0) {
+      s_d[warp] = rs::ff_value(f);
+      s_u[warp] = amin;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      double W = 0.0;
+      uint32_t am = 0xFFFFFFFFu;
+      for (int k = 0; k < VS_WARPS; ++k) {
+        W += s_d[k];
+        am = min(am, s_u[k]);
+      }
+      a.ws.zmax[rid] = zmax;
+      a.ws.wsum[rid] = W;
+      a.ws.wcut[rid] = 0.0f;
+      a.ws.icut[rid] = -1;
+      if (greedy) a.ws.amax[rid] = int32_t(am);
+      float pw = 0.0f;
+      if (j < n) {
+        const int64_t x = a.draft_tgt[r * a.B + j];
+        if (x >= 0 && x < a.V) pw = ds_weight(__fsub_rn(ds_temper(ds_load_elem<T>(row + x), Tz), zmax));
+      }
+      a.ws.probe_w[rid] = pw;
+    }
+    __syncthreads();                                 // the reduction slots are reused by the next row
+  }
+}
+
 // One warp per request.
 __global__ void __launch_bounds__(128) verify_accept_kernel(const VerifyArgs a, int64_t R) {
   const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  ds_pdl_trigger();
+  ds_pdl_wait();
   if (r >= R) return;                                      // whole warps leave together
   const int B = a.B, n = a.n_draft[r];
   const int64_t obase = r * (B + 1), rbase = r * (B + 1);
@@ -318,11 +459,10 @@ DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const flo
       const float zm = a.q.zmax[g.qrow], wc = a.q.wcut[g.qrow];
       const int64_t ic = a.q.icut[g.qrow];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (t + e < a.V_q) {
-          const float w = ds_weight(__fsub_rn(zq[e], zm));
-          qt[e] = vf_keep(w, t + e, wc, ic) ? w : 0.0f;
-        }
+      for (int e = 0; e < 8; e += 2) {
+        const float2 w2 = ds_weight2(__fsub_rn(zq[e], zm), __fsub_rn(zq[e + 1], zm));
+        if (t + e < a.V_q) qt[e] = vf_keep(w2.x, t + e, wc, ic) ? w2.x : 0.0f;
+        if (t + e + 1 < a.V_q) qt[e + 1] = vf_keep(w2.y, t + e + 1, wc, ic) ? w2.y : 0.0f;
       }
     } else if constexpr (QF == QF_DENSE_PRUNED) {
       int32_t ii[8];
@@ -332,13 +472,13 @@ DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const flo
     }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float wp = 0.0f;
-    if (t + e < a.V) {
-      wp = ds_weight(__fsub_rn(ds_temper(x[e], a.T), g.zmax));
-      if (!vf_keep(wp, t + e, g.wcut, g.icut)) wp = 0.0f;
-    }
-    out[e] = vf_rho<T>(a, g, wp, qt[e]);
+  for (int e = 0; e < 8; e += 2) {
+    const float2 w2 = ds_weight2(__fsub_rn(ds_temper(x[e], a.T), g.zmax), __fsub_rn(ds_temper(x[e + 1], a.T), g.zmax));
+    float wp0 = w2.x, wp1 = w2.y;
+    if (!(t + e < a.V) || !vf_keep(wp0, t + e, g.wcut, g.icut)) wp0 = 0.0f;
+    if (!(t + e + 1 < a.V) || !vf_keep(wp1, t + e + 1, g.wcut, g.icut)) wp1 = 0.0f;
+    out[e] = vf_rho<T>(a, g, wp0, qt[e]);
+    out[e + 1] = vf_rho<T>(a, g, wp1, qt[e + 1]);
   }
 }
 
@@ -364,6 +504,8 @@ DS_DEV void vf_stage_sparse(const VerifyArgs& a, int64_t qrow, int64_t lo, int l
 template <typename T, int QF>
 __global__ void __launch_bounds__(VM_THREADS) verify_mass_kernel(const VerifyArgs a) {
   __shared__ float s_q[QF == QF_SPARSE ? VM_PART : 1];
+  ds_pdl_trigger();
+  ds_pdl_wait();
   const int64_t r = blockIdx.y;
   const int32_t kind = a.ws.job_kind[r];
   if (kind == JOB_NONE) return;
@@ -401,6 +543,8 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
   __shared__ int64_t s_cell;
   __shared__ double s_tau;
   __shared__ int64_t s_pick;
+  ds_pdl_trigger();
+  ds_pdl_wait();
   const int64_t r = blockIdx.x;
   const int32_t kind = a.ws.job_kind[r];
   if (kind == JOB_NONE) return;
@@ -584,11 +728,9 @@ VerifyWs vf_layout(void* base, int64_t R, int32_t B, int64_t V, size_t* total) {
 template <typename T, int QF>
 cudaError_t vf_launch_draws(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
   const dim3 mgrid(unsigned((a.V + VM_PART - 1) / VM_PART), unsigned(R));
-  verify_mass_kernel<T, QF><<<mgrid, VM_THREADS, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = ds_launch(verify_mass_kernel<T, QF>, mgrid, dim3(VM_THREADS), 0, stream, a);
   if (e != cudaSuccess) return e;
-  verify_pick_kernel<T, QF><<<unsigned(R), VP_THREADS, 0, stream>>>(a);
-  return cudaGetLastError();
+  return ds_launch(verify_pick_kernel<T, QF>, dim3(unsigned(R)), dim3(VP_THREADS), 0, stream, a);
 }
 
 template <typename T>
@@ -668,6 +810,15 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   }
 
   // 1. statistics of every needed target row
+  if (greedy || !(top_p < 1.0f)) {
+    const int64_t grid = std::min<int64_t>(R * (B + 1), int64_t(ds_num_sms()) * VS_PER_SM);
+    if (dtype == DSPARK_BF16)
+      DS_CUDA_TRY(ds_launch(verify_stats_kernel<__nv_bfloat16>, dim3(unsigned(grid)), dim3(VS_THREADS), 0, stream, a,
+                            R * (B + 1)));
+    else
+      DS_CUDA_TRY(ds_launch(verify_stats_kernel<float>, dim3(unsigned(grid)), dim3(VS_THREADS), 0, stream, a,
+                            R * (B + 1)));
+  } else {
   rs::SampleArgs sa = {};
   sa.rows = tgt_logits;
   sa.V = V_t;
@@ -695,10 +846,10 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.probe_w = a.ws.probe_w;
   sa.amax_out = greedy ? a.ws.amax : nullptr;
   DS_CUDA_TRY(rs::sample_rows(sa, R * (B + 1), dtype == DSPARK_BF16, 0, stream));
+  }
 
   // 2. acceptance tests, one warp per request
-  verify_accept_kernel<<<unsigned((R * 32 + 127) / 128), 128, 0, stream>>>(a, R);
-  DS_CUDA_TRY(cudaGetLastError());
+  DS_CUDA_TRY(ds_launch(verify_accept_kernel, dim3(unsigned((R * 32 + 127) / 128)), dim3(128), 0, stream, a, R));
 
   // 3-4. residual or bonus draws
   if (!greedy) {

@@ -212,6 +212,23 @@ dspark_status dspark_chain_select(const float* cand_val, const float* trans,
                                   dspark_stream_t stream);
 
 /*
+ * Lattice and greedy chain in one call [G: Change > Markov heads, block-sampler commit; E:
+ * DFlash v2 packed Top-K lattice]: the same results as dspark_lattice_score followed by
+ * dspark_chain_select with mode DSPARK_MAXSUM or DSPARK_WALK (arguments as there). For bf16
+ * tables with rank % 64 == 0, rank <= 512 and B <= 8 it is one launch: the B tiles of a
+ * request are one thread-block cluster and the chain is decided on chip, so trans and gate
+ * may be NULL (not written). Otherwise it runs the two calls and trans must not be NULL.
+ */
+dspark_status dspark_lattice_chain(const float* cand_val, const int32_t* cand_tgt, const int32_t* prev,
+                                   int64_t R, int32_t B, int32_t K, const void* E, const void* W,
+                                   dspark_dtype table_dtype, int64_t V_t, int32_t rank,
+                                   const void* hidden, const void* g, dspark_dtype hidden_dtype,
+                                   int32_t H, int64_t ldh, const int64_t* row_start,
+                                   dspark_chain_mode mode, float* trans, float* gate,
+                                   int32_t* chain_rank, int32_t* chain_tgt, float* score,
+                                   int32_t* dev_status, dspark_stream_t stream);
+
+/*
  * Full-row multinomial drafting without a head [G: Change > Sampled drafting; commits on
  * the thresholded top-p filter, double sums and the double uniform]. Rows as in
  * dspark_topk (transform included). Per block row (r, j): z = s / T, weights, top-p
@@ -287,6 +304,16 @@ dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t 
                             const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted,
                             float* logprob, void* ws, size_t ws_bytes, int32_t* dev_status,
                             dspark_stream_t stream);
+
+/*
+ * Failure-detection test hook (not part of the method): sets the poll limit of the first wait
+ * for a tile's tensor-core MMAs in dspark_lattice_score, dspark_lattice_chain and
+ * dspark_dense_walk, process-wide, for later calls (0xFFFFFFFF restores the default, about 6.7e7
+ * polls). A wait that runs out sets DSPARK_ETIMEOUT on *dev_status and the CTA writes no
+ * results; it then waits for its MMAs in flight with the full limit before releasing tensor
+ * memory, so a limit of 0 makes the timeout path run without leaving work on the GPU.
+ */
+void dspark_test_set_first_wait_polls(uint32_t polls);
 
 #ifdef __cplusplus
 }

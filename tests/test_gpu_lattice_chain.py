@@ -205,3 +205,55 @@ def test_gated_config_lattice_sampled_rows():
         err = np.abs(got["trans"][r] - ref)
         assert np.all(err <= 1e-3 * np.abs(ref) + 1e-5 * np.abs(ref).max())
         check_maxsum(got, r, got["cand_val"][r], got["trans"][r].astype(np.float64), w["B"])
+
+
+def _two_call(ds, cv, ct, prev, E, W, mode, hidden=None, g=None):
+    trans, gate, st = ds.dspark_lattice_score(ct, prev, E, W, hidden=hidden, g=g)
+    rank_, tgt, score, st2 = ds.dspark_chain_select(cv, trans, ct, mode)
+    torch.cuda.synchronize()
+    assert ds.read_status(st) == 0 and ds.read_status(st2) == 0
+    return trans, gate, rank_, tgt, score
+
+
+@pytest.mark.parametrize("cfg,mode", [(2, "maxsum"), (2, "walk"), (4, "maxsum"), (1, "maxsum")])
+def test_lattice_chain_fused_equals_two_calls(cfg, mode):
+    # one cluster per request decides the chain on chip: same float32 operations as the two calls
+    import dspark_draft_selection_gb300 as ds
+    w = di.CONFIGS[cfg]()
+    cd, ct, cv, st = ds.dspark_topk(dev(w["logits"]), w["B"], w["K"])
+    hid = dev(w["hidden"]) if w["hidden"] is not None else None
+    g = dev(w["g"]) if hid is not None else None
+    prev, E, W = dev(w["prev"]), dev(w["E"]), dev(w["W"])
+    trans, gate, rank_, tgt, score = _two_call(ds, cv, ct, prev, E, W, mode, hid, g)
+    t2 = torch.full_like(trans, float("nan"))
+    g2 = torch.full_like(gate, float("nan"))
+    r2, tg2, sc2, st2 = ds.dspark_lattice_chain(cv, ct, prev, E, W, mode, hidden=hid, g=g, trans=t2, gate=g2)
+    pairs = [(rank_, r2), (tgt, tg2), (score, sc2), (trans, t2), (gate, g2)]
+    if w["table_dtype"] == "bf16":                      # one launch: the lattice need not be kept
+        r3, tg3, sc3, st3 = ds.dspark_lattice_chain(cv, ct, prev, E, W, mode, hidden=hid, g=g)
+        pairs += [(rank_, r3), (tgt, tg3), (score, sc3)]
+    else:                                               # float32 tables: two launches need the lattice
+        with pytest.raises(ds.DsparkError):
+            ds.dspark_lattice_chain(cv, ct, prev, E, W, mode)
+    torch.cuda.synchronize()
+    assert ds.read_status(st2) == 0
+    for a, b in pairs:
+        assert torch.equal(a, b)
+
+
+def test_lattice_chain_strong_head_and_long_block_fallback():
+    import dspark_draft_selection_gb300 as ds
+    for B in (8, 15):                                    # 8: the largest cluster; 15: two launches
+        w = di.lattice_workload(44 + B, R=6, B=B, V_d=4096, K=64, rank=64, head_sigma=0.35)
+        cd, ct, cv, st = ds.dspark_topk(dev(w["logits"]), B, 64)
+        prev, E, W = dev(w["prev"]), dev(w["E"]), dev(w["W"])
+        for mode in ("maxsum", "walk"):
+            trans, gate, rank_, tgt, score = _two_call(ds, cv, ct, prev, E, W, mode)
+            t2 = torch.empty_like(trans)
+            r2, tg2, sc2, st2 = ds.dspark_lattice_chain(cv, ct, prev, E, W, mode, trans=t2)
+            torch.cuda.synchronize()
+            assert ds.read_status(st2) == 0
+            assert torch.equal(rank_, r2) and torch.equal(tgt, tg2) and torch.equal(score, sc2)
+            assert torch.equal(trans, t2)
+    with pytest.raises(ds.DsparkError):                  # two launches need the lattice in memory
+        ds.dspark_lattice_chain(cv, ct, prev, E, W, "maxsum")
