@@ -13,6 +13,9 @@
 
 #define DS_DEV __device__ __forceinline__
 
+// Wall-clock bound of one mbarrier wait (2 s): far above any wait of a working kernel.
+#define DS_WAIT_NS 2000000000ull
+
 // ----------------------------------------------------------------------------------------
 // status
 // ----------------------------------------------------------------------------------------
@@ -191,6 +194,12 @@ DS_DEV float2 ds_weight2(float d0, float d1) {
 
 // z = s / T in float32 (the identity for T == 1)
 DS_DEV float ds_temper(float s, float T) { return (T == 1.0f) ? s : __fdiv_rn(s, T); }
+// the same with the T == 1 case decided at compile time (no division is evaluated for it)
+template <bool TONE>
+DS_DEV float ds_temper_t(float s, float T) {
+  if constexpr (TONE) return s;
+  else return __fdiv_rn(s, T);
+}
 
 // ----------------------------------------------------------------------------------------
 // warp helpers
@@ -298,9 +307,17 @@ DS_DEV void ds_mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
-// Waits for phase `parity` of an mbarrier to complete; gives up after `limit` polls.
+DS_DEV uint64_t ds_globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of an mbarrier to complete; gives up after `limit` polls or about
+// DS_WAIT_NS nanoseconds, whichever comes first (a poll may suspend the thread for a while).
 DS_DEV bool ds_mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   const uint32_t a = ds_smem_addr(bar);
+  uint64_t t0 = 0;
   for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
@@ -311,6 +328,36 @@ DS_DEV bool ds_mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
         : "r"(a), "r"(parity)
         : "memory");
     if (done) return true;
+    if ((i & 63u) == 63u) {
+      const uint64_t t = ds_globaltimer();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > DS_WAIT_NS) return false;
+    }
+  }
+  return false;
+}
+
+// ds_mbar_wait that also gives up as soon as *abort becomes nonzero (another role of the CTA
+// stopped).
+DS_DEV bool ds_mbar_wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t limit, const int* abort) {
+  const uint32_t a = ds_smem_addr(bar);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 63u) == 63u) {
+      if (*reinterpret_cast<const volatile int*>(abort)) return false;
+      const uint64_t t = ds_globaltimer();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > DS_WAIT_NS) return false;
+    }
   }
   return false;
 }
@@ -472,6 +519,41 @@ DS_DEV void ds_cp_async16(void* smem_dst, const void* gmem_src) {
                "l"(gmem_src)
                : "memory");
 }
+// 2-D tiled TMA load of box (x = inner coordinate in elements, y = row) into shared memory,
+// completing its bytes on an mbarrier, with an L2 cache policy. x * element size must be a
+// multiple of 16 bytes; rows outside the tensor read as zero.
+DS_DEV void ds_tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(ds_smem_addr(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(ds_smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// An L2 policy that keeps lines (evict last), for data read again by later launches.
+DS_DEV uint64_t ds_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+DS_DEV void ds_cp_async16_hint(void* smem_dst, const void* gmem_src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(ds_smem_addr(smem_dst)),
+               "l"(gmem_src), "l"(pol)
+               : "memory");
+}
+// Arrive on an mbarrier once this thread's earlier cp.async copies have landed (counted in its
+// expected arrivals).
+DS_DEV void ds_cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ds_smem_addr(bar)) : "memory");
+}
+DS_DEV void ds_mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ds_smem_addr(bar)) : "memory");
+}
+// Named barrier over `count` threads (a multiple of 32).
+DS_DEV void ds_named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 DS_DEV void ds_cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }

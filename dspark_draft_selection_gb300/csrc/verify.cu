@@ -16,17 +16,17 @@
 //  1. statistics of every needed target row: the maximum, the top-p cut and the kept mass of p_j,
 //     the weight of the drafted token x_j, and the argmax (greedy requests) - verify_stats_kernel
 //     when there is no nucleus, else the row sampler of sample.cu in statistics mode. The target
-//     logits are read from HBM once here.
-//  2. verify_accept_kernel - one warp per request, one lane per window position: the tests
-//     u_j < p_j(x_j) / q_j(x_j) of different positions are independent, so every lane decides its
-//     own and the first failing position (a ballot) ends the window. Leaves at most one draw job
-//     per request: the residual at the first rejection, or the bonus draw at n.
-//  3. verify_mass_kernel - every draw row is split into parts of VM_PART ids spread over many
-//     CTAs; each forms rho = max(0, p - q) (p alone for the bonus draw) scaled by W_p * W_q, so no
-//     element needs a division, as float pairs, and writes the mass of every cell of VM_CELL
-//     consecutive ids.
-//  4. verify_pick_kernel - one CTA per job scans its cells in double, finds the cell whose running
-//     sum crosses u * sum(rho), re-evaluates that cell's ids and emits the token.
+//     logits are read from HBM once here. The acceptance tests of a request run once its rows are
+//     done (in the statistics kernel, by the CTA that finishes the last of them; after the row
+//     sampler, in verify_accept_kernel): one warp, one lane per window position - the tests
+//     u_j < p_j(x_j) / q_j(x_j) of different positions are independent, and the first failing
+//     position (a ballot) ends the window. They leave at most one draw: the residual at the first
+//     rejection, or the bonus draw at n (greedy requests need none).
+//  2. verify_draw_kernel - one CTA per part of VM_PART ids of a request's draw row forms
+//     rho = max(0, p - q) (p alone for the bonus draw) scaled by W_p * W_q, so no element needs a
+//     division, as float pairs, and writes the mass of every cell of VM_CELL consecutive ids; the
+//     part that finishes last scans all cells in double, finds the cell whose running sum crosses
+//     u * sum(rho), re-evaluates that cell's ids and emits the token.
 #include "host_common.h"
 #include "rowsample.cuh"
 
@@ -35,9 +35,8 @@ namespace {
 constexpr int VM_THREADS = 512;            // residual-mass CTAs
 constexpr int VM_WARPS = VM_THREADS / 32;
 constexpr int VM_CELL = 256;               // ids per cell: one warp, eight consecutive ids a lane
-constexpr int VM_PART = 8192;              // ids per mass CTA (32 cells)
-constexpr int VM_CELLS_PER_PART = VM_PART / VM_CELL;
-constexpr int VP_THREADS = 512;            // pick CTAs
+constexpr int VM_PART = 32768;             // ids per draw CTA (128 cells) for dense records
+constexpr int VM_PART_SPARSE = 8192;       // ... for sparse records (staged in shared memory by id)
 
 enum : int32_t { JOB_NONE = 0, JOB_RESIDUAL = 1, JOB_BONUS = 2 };
 // proposal record forms
@@ -50,8 +49,10 @@ struct VerifyWs {
   int32_t* icut;
   float* probe_w;
   int32_t* amax;
-  int32_t* job_kind; // [R]
+  int32_t* job_kind; // [R] the draw job of each request (from the acceptance tests)
   int32_t* job_j;
+  int32_t* tk_stats; // [R] rows of a request whose statistics are done
+  int32_t* tk_draw;  // [R] parts of a request's draw row that are done
   float2* cells;     // [R, ncell] residual mass per cell (float pair)
   int32_t* t2d;      // [V] record index of each target id (pruned dense records)
 };
@@ -119,6 +120,102 @@ __global__ void verify_t2d_kernel(const int64_t* d2t, int64_t V_d, int64_t V_t, 
   }
 }
 
+// The acceptance tests of request r by one warp, one lane per window position: the tests of
+// different positions are independent, so every lane decides its own and the first position that is
+// not accepted (a ballot) ends the window. With `write`, the accepted tokens, their log-probabilities
+// and n_accepted are written (and the greedy correction or bonus). Returns the draw job through
+// *kind / *jj: none (greedy, an error, or a proposal error), the residual at the first rejection, or
+// the bonus draw at n.
+DS_DEV void vf_accept_warp(const VerifyArgs& a, int64_t r, bool write, int* kind, int* jj) {
+  const int lane = threadIdx.x & 31;
+  const int B = a.B, n = a.n_draft[r];
+  const int64_t obase = r * (B + 1), rbase = r * (B + 1);
+  if (n < 0 || n > B) {                                    // out of contract: an error, no indexing
+    if (write) {
+      if (lane == 0) {
+        ds_set_error(a.status, DSPARK_EINVAL);
+        a.n_accepted[r] = -1;
+        a.ws.job_kind[r] = JOB_NONE;
+      }
+      for (int k = lane; k <= B; k += 32) {
+        a.out_tokens[obase + k] = -1;
+        a.logprob[obase + k] = 0.0f;
+      }
+    }
+    *kind = JOB_NONE;
+    return;
+  }
+  const bool greedy = !(a.T > 0.0f);
+  const uint64_t vseed = greedy ? 0 : a.vseed[r], step = greedy ? 0 : a.step[r];
+  int first = n;                                           // first position that is not accepted
+  bool first_zero_q = false;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    bool ev = false, zq = false;
+    if (j < n) {
+      const int64_t rid = rbase + j;
+      const int32_t x = a.draft_tgt[r * B + j];
+      if (greedy) {
+        ev = x != a.ws.amax[rid];
+      } else {
+        const double qx = vf_q(a, r * B + j, x);
+        zq = !(qx > 0.0);
+        if (!zq) {
+          const double px = double(a.ws.probe_w[rid]) / a.ws.wsum[rid];
+          const double ua = ds_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
+          ev = !(ua < px / qx);
+        }
+        ev = ev || zq;
+      }
+    }
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, ev);
+    if (bal) {
+      const int l = __ffs(bal) - 1;
+      first = j0 + l;
+      first_zero_q = __shfl_sync(0xFFFFFFFFu, zq, l);
+      break;
+    }
+  }
+  if (first_zero_q) {                                      // the proposal gave a drafted token q = 0
+    if (write) {
+      if (lane == 0) {
+        ds_set_error(a.status, DSPARK_EPROPOSAL);
+        a.n_accepted[r] = -1;
+        a.ws.job_kind[r] = JOB_NONE;
+      }
+      for (int k = lane; k <= B; k += 32) a.out_tokens[obase + k] = -1;
+    }
+    *kind = JOB_NONE;
+    return;
+  }
+  const int acc = first;
+  if (write) {
+    for (int k = lane; k <= B; k += 32) {
+      if (k < acc) {
+        const int64_t rid = rbase + k;
+        a.out_tokens[obase + k] = a.draft_tgt[r * B + k];
+        a.logprob[obase + k] = float(log(double(a.ws.probe_w[rid])) - log(a.ws.wsum[rid]));
+      } else if (k > acc) {
+        a.out_tokens[obase + k] = -1;
+        a.logprob[obase + k] = 0.0f;
+      } else if (greedy) {
+        // the correction or bonus is the argmax of its row; it reports the temperature-1 log-prob
+        // (the argmax has weight 1)
+        const int64_t rid = rbase + acc;
+        a.out_tokens[obase + acc] = a.ws.amax[rid];
+        a.logprob[obase + acc] = float(-log(a.ws.wsum[rid]));
+      }
+    }
+    if (lane == 0) a.n_accepted[r] = acc;
+  }
+  *kind = greedy ? JOB_NONE : (acc < n ? JOB_RESIDUAL : JOB_BONUS);
+  *jj = acc;
+  if (write && lane == 0) {
+    a.ws.job_kind[r] = *kind;
+    a.ws.job_j[r] = acc;
+  }
+}
+
 // ---- statistics of the target rows (no nucleus: top_p >= 1, or greedy) --------------------------
 // One CTA per row at a time, persistent over rows, several CTAs per SM. Pass 1 takes the row's
 // maximum over the raw 16-byte vectors (the maximum of z = s / T is fl(max s / T) for T > 0);
@@ -149,6 +246,7 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
   __shared__ float s_f[VS_WARPS];
   __shared__ double s_d[VS_WARPS];
   __shared__ uint32_t s_u[VS_WARPS];
+  __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool greedy = !(a.T > 0.0f);
   const float Tz = greedy ? 1.0f : a.T;
@@ -158,7 +256,14 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
     const int64_t r = rid / (a.B + 1);
     const int j = int(rid - r * (a.B + 1));
     const int32_t n = a.n_draft[r];
-    if (n < 0 || n > a.B || j > n) continue;       // not needed (or an error the accept kernel reports)
+    if (n < 0 || n > a.B) {                        // out of contract: the first row's CTA reports it
+      if (j == 0 && warp == 0) {
+        int kind = JOB_NONE, jj = 0;
+        vf_accept_warp(a, r, true, &kind, &jj);
+      }
+      continue;
+    }
+    if (j > n) continue;                           // not needed
     const int64_t prow = a.row_start ? a.row_start[r] + j : rid;
     const T* row = reinterpret_cast<const T*>(a.logits) + prow * a.ld;
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
@@ -186,11 +291,7 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
 #pragma unroll
     for (int k = 1; k < VS_WARPS; ++k) rmax = fmaxf(rmax, s_f[k]);
     const float zmax = ds_temper(rmax, Tz);
-    if (!(zmax > -INFINITY && zmax < INFINITY)) {
-      if (tid == 0) ds_set_error(a.status, DSPARK_ENONFINITE);
-      __syncthreads();
-      continue;
-    }
+    const bool finite = zmax > -INFINITY && zmax < INFINITY;   // else reported, with no mass
     // pass 2: the sum of the weights (two float pairs per thread) and the argmax of greedy rows
     rs::FF2 acc{0, 0};
     rs::FF sc{0.0f, 0.0f};
@@ -200,9 +301,9 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
       rs::ff_add(sc, ds_weight(__fsub_rn(z, zmax)));
       if (greedy && z == zmax) amin = min(amin, uint32_t(i));
     };
-    if (tid < head) scalar(tid);
-    if (tid < a.V - tail0) scalar(tail0 + tid);
-    for (int64_t v0 = tid; v0 < nvec; v0 += int64_t(4) * VS_THREADS) {
+    if (finite && tid < head) scalar(tid);
+    if (finite && tid < a.V - tail0) scalar(tail0 + tid);
+    for (int64_t v0 = tid; finite && v0 < nvec; v0 += int64_t(4) * VS_THREADS) {
       uint4 w[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -241,105 +342,40 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
         W += s_d[k];
         am = min(am, s_u[k]);
       }
+      if (!finite) ds_set_error(a.status, DSPARK_ENONFINITE);
       a.ws.zmax[rid] = zmax;
       a.ws.wsum[rid] = W;
       a.ws.wcut[rid] = 0.0f;
       a.ws.icut[rid] = -1;
       if (greedy) a.ws.amax[rid] = int32_t(am);
       float pw = 0.0f;
-      if (j < n) {
+      if (finite && j < n) {
         const int64_t x = a.draft_tgt[r * a.B + j];
         if (x >= 0 && x < a.V) pw = ds_weight(__fsub_rn(ds_temper(ds_load_elem<T>(row + x), Tz), zmax));
       }
       a.ws.probe_w[rid] = pw;
+      // the CTA that completes the request's last needed row runs its acceptance tests
+      __threadfence();
+      s_last = atomicAdd(&a.ws.tk_stats[r], 1) == n;
+    }
+    __syncthreads();
+    if (s_last && warp == 0) {
+      __threadfence();
+      int kind = JOB_NONE, jj = 0;
+      vf_accept_warp(a, r, true, &kind, &jj);
     }
     __syncthreads();                                 // the reduction slots are reused by the next row
   }
 }
 
-// One warp per request.
+// The acceptance tests after the row sampler's statistics (rows with a nucleus): one warp per request.
 __global__ void __launch_bounds__(128) verify_accept_kernel(const VerifyArgs a, int64_t R) {
   const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   ds_pdl_trigger();
   ds_pdl_wait();
   if (r >= R) return;                                      // whole warps leave together
-  const int B = a.B, n = a.n_draft[r];
-  const int64_t obase = r * (B + 1), rbase = r * (B + 1);
-  if (n < 0 || n > B) {                                    // out of contract: an error, no indexing
-    if (lane == 0) {
-      ds_set_error(a.status, DSPARK_EINVAL);
-      a.n_accepted[r] = -1;
-      a.ws.job_kind[r] = JOB_NONE;
-    }
-    for (int k = lane; k <= B; k += 32) {
-      a.out_tokens[obase + k] = -1;
-      a.logprob[obase + k] = 0.0f;
-    }
-    return;
-  }
-  const bool greedy = !(a.T > 0.0f);
-  const uint64_t vseed = greedy ? 0 : a.vseed[r], step = greedy ? 0 : a.step[r];
-  int first = n;                                           // first position that is not accepted
-  bool first_zero_q = false;
-  for (int j0 = 0; j0 < n; j0 += 32) {
-    const int j = j0 + lane;
-    bool ev = false, zq = false;
-    if (j < n) {
-      const int64_t rid = rbase + j;
-      const int32_t x = a.draft_tgt[r * B + j];
-      if (greedy) {
-        ev = x != a.ws.amax[rid];
-      } else {
-        const double qx = vf_q(a, r * B + j, x);
-        zq = !(qx > 0.0);
-        if (!zq) {
-          const double px = double(a.ws.probe_w[rid]) / a.ws.wsum[rid];
-          const double ua = ds_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
-          ev = !(ua < px / qx);
-        }
-        ev = ev || zq;
-      }
-    }
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, ev);
-    if (bal) {
-      const int l = __ffs(bal) - 1;
-      first = j0 + l;
-      first_zero_q = __shfl_sync(0xFFFFFFFFu, zq, l);
-      break;
-    }
-  }
-  if (first_zero_q) {                                      // the proposal gave a drafted token q = 0
-    if (lane == 0) {
-      ds_set_error(a.status, DSPARK_EPROPOSAL);
-      a.n_accepted[r] = -1;
-      a.ws.job_kind[r] = JOB_NONE;
-    }
-    for (int k = lane; k <= B; k += 32) a.out_tokens[obase + k] = -1;
-    return;
-  }
-  const int acc = first;
-  for (int k = lane; k <= B; k += 32) {
-    if (k < acc) {
-      const int64_t rid = rbase + k;
-      a.out_tokens[obase + k] = a.draft_tgt[r * B + k];
-      a.logprob[obase + k] = float(log(double(a.ws.probe_w[rid])) - log(a.ws.wsum[rid]));
-    } else if (k > acc) {
-      a.out_tokens[obase + k] = -1;
-      a.logprob[obase + k] = 0.0f;
-    } else if (greedy) {
-      // the correction or bonus is the argmax of its row; it reports the temperature-1 log-prob
-      // (the argmax has weight 1)
-      const int64_t rid = rbase + acc;
-      a.out_tokens[obase + acc] = a.ws.amax[rid];
-      a.logprob[obase + acc] = float(-log(a.ws.wsum[rid]));
-    }
-  }
-  if (lane == 0) {
-    a.n_accepted[r] = acc;
-    a.ws.job_kind[r] = greedy ? JOB_NONE : (acc < n ? JOB_RESIDUAL : JOB_BONUS);
-    a.ws.job_j[r] = acc;
-  }
+  int kind = JOB_NONE, jj = 0;
+  vf_accept_warp(a, r, true, &kind, &jj);
 }
 
 // ---- residual masses ---------------------------------------------------------------------------
@@ -441,7 +477,7 @@ DS_DEV void vf_ld8_i32(const int32_t* p, int64_t t, int64_t n, int32_t (&x)[8]) 
 }
 
 // rho' of the eight ids t..t+7 (zero past V). s_q: a sparse record's q by id, indexed from s_q0.
-template <typename T, int QF>
+template <typename T, int QF, bool TONE>
 DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const float* s_q, int64_t s_q0,
                     rs::FF (&out)[8]) {
   float x[8];
@@ -473,20 +509,14 @@ DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const flo
   }
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
-    const float2 w2 = ds_weight2(__fsub_rn(ds_temper(x[e], a.T), g.zmax), __fsub_rn(ds_temper(x[e + 1], a.T), g.zmax));
+    const float2 w2 = ds_weight2(__fsub_rn(ds_temper_t<TONE>(x[e], a.T), g.zmax),
+                                 __fsub_rn(ds_temper_t<TONE>(x[e + 1], a.T), g.zmax));
     float wp0 = w2.x, wp1 = w2.y;
     if (!(t + e < a.V) || !vf_keep(wp0, t + e, g.wcut, g.icut)) wp0 = 0.0f;
     if (!(t + e + 1 < a.V) || !vf_keep(wp1, t + e + 1, g.wcut, g.icut)) wp1 = 0.0f;
     out[e] = vf_rho<T>(a, g, wp0, qt[e]);
     out[e + 1] = vf_rho<T>(a, g, wp1, qt[e + 1]);
   }
-}
-
-DS_DEV void vf_ff_acc(rs::FF& m, const rs::FF& v) {
-  const float lo = __fadd_rn(m.lo, v.lo);
-  m.lo = 0.0f;
-  rs::ff_add(m, v.hi);
-  m.lo = __fadd_rn(m.lo, lo);
 }
 
 // Stages a sparse record's q for ids [lo, lo + len) into s_q (zero elsewhere); whole block.
@@ -501,76 +531,79 @@ DS_DEV void vf_stage_sparse(const VerifyArgs& a, int64_t qrow, int64_t lo, int l
   __syncthreads();
 }
 
-template <typename T, int QF>
-__global__ void __launch_bounds__(VM_THREADS) verify_mass_kernel(const VerifyArgs a) {
-  __shared__ float s_q[QF == QF_SPARSE ? VM_PART : 1];
+// One CTA per (part of a draw row, request). Warp 0 first runs the request's acceptance tests
+// (the same decisions in every part; part 0 writes the accepted tokens), which name the draw job;
+// the CTA then writes the residual mass of every cell of its part, and the part that finishes last
+// (a ticket per request) picks the token: it scans all the row's cells in double, finds the cell
+// whose running sum crosses u * sum(rho), and re-evaluates that cell's ids.
+template <typename T, int QF, bool TONE>
+__global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const VerifyArgs a) {
+  constexpr int PART = (QF == QF_SPARSE) ? VM_PART_SPARSE : VM_PART;
+  constexpr int CPP = PART / VM_CELL;                      // cells per part
+  constexpr int WARPS = VM_THREADS / 32;
+  __shared__ float s_q[QF == QF_SPARSE ? VM_PART_SPARSE : 1];
+  __shared__ double s_run[VM_THREADS + 1];
+  __shared__ int s_last;
+  __shared__ int64_t s_cell, s_pick;
+  __shared__ double s_tau;
   ds_pdl_trigger();
   ds_pdl_wait();
   const int64_t r = blockIdx.y;
-  const int32_t kind = a.ws.job_kind[r];
-  if (kind == JOB_NONE) return;
-  const int64_t t0 = int64_t(blockIdx.x) * VM_PART;
-  if (t0 >= a.V) return;
-  const VfJob<T> g = vf_job<T>(a, r, a.ws.job_j[r], kind == JOB_RESIDUAL);
-  if (QF == QF_SPARSE && g.use_q) vf_stage_sparse(a, g.qrow, t0, VM_PART, s_q);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int PER = VM_CELLS_PER_PART / VM_WARPS;       // cells per warp, loads issued together
-  rs::FF v[PER][8];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int64_t t = t0 + int64_t(warp + k * VM_WARPS) * VM_CELL + lane * 8;
-    if (t < a.V) vf_rho8<T, QF>(a, g, t, s_q, t0, v[k]);
-  }
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int64_t c = t0 / VM_CELL + warp + k * VM_WARPS;
-    if (c * VM_CELL >= a.V) break;                          // warp-uniform
-    const int64_t t = c * VM_CELL + lane * 8;
-    rs::FF m{0.0f, 0.0f};
-    if (t < a.V) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) vf_ff_acc(m, v[k][e]);
-    }
-    const rs::FF cw = rs::warp_ff_reduce(m);
-    if (lane == 0) a.ws.cells[r * a.ncell + c] = make_float2(cw.hi, cw.lo);
-  }
-}
-
-template <typename T, int QF>
-__global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArgs a) {
-  __shared__ double s_run[VP_THREADS + 1];
-  __shared__ float s_q[QF == QF_SPARSE ? VM_CELL : 1];
-  __shared__ int64_t s_cell;
-  __shared__ double s_tau;
-  __shared__ int64_t s_pick;
-  ds_pdl_trigger();
-  ds_pdl_wait();
-  const int64_t r = blockIdx.x;
-  const int32_t kind = a.ws.job_kind[r];
-  if (kind == JOB_NONE) return;
-  const int j = a.ws.job_j[r];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int WARPS = VP_THREADS / 32;
-  const int64_t ncell = a.ncell;
-  float2* cells = a.ws.cells + r * ncell;
+  const int32_t kind = a.ws.job_kind[r];
+  if (kind == JOB_NONE) return;                            // the whole request has no draw
+  const int j = a.ws.job_j[r];
+  const int64_t t0 = int64_t(blockIdx.x) * PART;
   VfJob<T> g = vf_job<T>(a, r, j, kind == JOB_RESIDUAL);
+  if (QF == QF_SPARSE && g.use_q) vf_stage_sparse(a, g.qrow, t0, PART, s_q);
+  float2* cells = a.ws.cells + r * a.ncell;
+  for (int k0 = warp; k0 < CPP; k0 += 2 * WARPS) {        // two cells per warp in flight
+    rs::FF v[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int cl = k0 + u * WARPS;
+      const int64_t t = t0 + int64_t(cl) * VM_CELL + lane * 8;
+      if (cl < CPP && t < a.V) vf_rho8<T, QF, TONE>(a, g, t, s_q, t0, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int cl = k0 + u * WARPS;
+      const int64_t c = t0 / VM_CELL + cl;
+      if (cl >= CPP || c * VM_CELL >= a.V) continue;       // warp-uniform
+      const int64_t t = c * VM_CELL + lane * 8;
+      rs::FF m{0.0f, 0.0f};
+      if (t < a.V) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rs::ff_acc(m, v[u][e]);
+      }
+      const rs::FF cw = rs::warp_ff_reduce(m);
+      if (lane == 0) cells[c] = make_float2(cw.hi, cw.lo);
+    }
+  }
+  // the last part to finish picks the token
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&a.ws.tk_draw[r], 1) == int(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
 
   // this thread's contiguous run of cells: its mass, the mass before it, the row's total
-  const int64_t per = (ncell + VP_THREADS - 1) / VP_THREADS;
+  const int64_t ncell = a.ncell;
+  const int64_t per = (ncell + VM_THREADS - 1) / VM_THREADS;
   const int64_t c0 = min(ncell, tid * per), c1 = min(ncell, c0 + per);
   double mine = 0.0, before = 0.0, total = 0.0;
   for (int attempt = 0; attempt < 2; ++attempt) {
     rs::FF mf{0.0f, 0.0f};
     for (int64_t c = c0; c < c1; ++c) {
-      const float2 cv = cells[c];
-      vf_ff_acc(mf, rs::FF{cv.x, cv.y});
+      const float2 cv = __ldcg(cells + c);
+      rs::ff_acc(mf, rs::FF{cv.x, cv.y});
     }
     mine = rs::ff_value(mf);
-    // exclusive prefix over threads (staged, scanned by warp 0)
-    s_run[tid] = mine;
+    s_run[tid] = mine;                                     // exclusive prefix over threads (warp 0)
     __syncthreads();
     if (tid < 32) {
-      constexpr int PT = VP_THREADS / 32;
+      constexpr int PT = VM_THREADS / 32;
       double loc = 0.0;
 #pragma unroll
       for (int q = 0; q < PT; ++q) loc += s_run[lane * PT + q];
@@ -587,11 +620,11 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
         s_run[lane * PT + q] = run;
         run += x;
       }
-      if (lane == 31) s_run[VP_THREADS] = incl;
+      if (lane == 31) s_run[VM_THREADS] = incl;
     }
     __syncthreads();
     before = s_run[tid];
-    total = s_run[VP_THREADS];
+    total = s_run[VM_THREADS];
     __syncthreads();
     if (total > 0.0 || attempt == 1) break;
     // the residual has no mass (possible only through rounding): draw from p, whose cells this CTA
@@ -602,14 +635,15 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
       rs::FF v[8];
       rs::FF m{0.0f, 0.0f};
       if (t < a.V) {
-        vf_rho8<T, QF>(a, g, t, s_q, 0, v);
+        vf_rho8<T, QF, TONE>(a, g, t, s_q, 0, v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vf_ff_acc(m, v[e]);
+        for (int e = 0; e < 8; ++e) rs::ff_acc(m, v[e]);
       }
       const rs::FF cw = rs::warp_ff_reduce(m);
       if (lane == 0) cells[c] = make_float2(cw.hi, cw.lo);
     }
-    __syncthreads();                                       // global writes are visible block-wide
+    __threadfence_block();
+    __syncthreads();
   }
 
   // the crossing cell: the first whose running sum exceeds u * total
@@ -623,7 +657,8 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
   if (mine > 0.0 && target >= before && target < before + mine) {
     double acc = before;
     for (int64_t c = c0; c < c1; ++c) {
-      const double cv = double(cells[c].x) + double(cells[c].y);
+      const float2 cv2 = __ldcg(cells + c);
+      const double cv = double(cv2.x) + double(cv2.y);
       if (cv > 0.0 && target < acc + cv) {
         s_cell = c;
         s_tau = target - acc;
@@ -634,12 +669,14 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
   }
   __syncthreads();
   if (tid == 0 && s_cell < 0) {                            // rounding: the last cell with mass
-    for (int64_t c = ncell - 1; c >= 0; --c)
-      if (double(cells[c].x) + double(cells[c].y) > 0.0) {
+    for (int64_t c = ncell - 1; c >= 0; --c) {
+      const float2 cv2 = __ldcg(cells + c);
+      if (double(cv2.x) + double(cv2.y) > 0.0) {
         s_cell = c;
         s_tau = INFINITY;
         break;
       }
+    }
   }
   __syncthreads();
   const int64_t cell = s_cell;
@@ -652,7 +689,7 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
       double rv[8], ls = 0.0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = rs::FF{0.0f, 0.0f};
-      if (t < a.V) vf_rho8<T, QF>(a, g, t, s_q, cell * VM_CELL, v);
+      if (t < a.V) vf_rho8<T, QF, TONE>(a, g, t, s_q, cell * VM_CELL, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         rv[e] = rs::ff_value(v[e]);
@@ -687,14 +724,13 @@ __global__ void __launch_bounds__(VP_THREADS) verify_pick_kernel(const VerifyArg
   __syncthreads();
   if (tid == 0) {
     const int64_t pick = s_pick;
-    const int acc = a.n_accepted[r];
     float w = 0.0f;
     if (pick >= 0) {
       const float x = ds_load_elem<T>(g.row + pick);
-      w = ds_weight(__fsub_rn(ds_temper(x, a.T), g.zmax));
+      w = ds_weight(__fsub_rn(ds_temper_t<TONE>(x, a.T), g.zmax));
     }
-    a.out_tokens[r * (a.B + 1) + acc] = int32_t(pick);
-    a.logprob[r * (a.B + 1) + acc] = float(log(double(w)) - log(g.Wp));
+    a.out_tokens[r * (a.B + 1) + j] = int32_t(pick);
+    a.logprob[r * (a.B + 1) + j] = float(log(double(w)) - log(g.Wp));
   }
 }
 
@@ -719,27 +755,33 @@ VerifyWs vf_layout(void* base, int64_t R, int32_t B, int64_t V, size_t* total) {
   w.amax = reinterpret_cast<int32_t*>(take(rows * 4));
   w.job_kind = reinterpret_cast<int32_t*>(take(size_t(R) * 4));
   w.job_j = reinterpret_cast<int32_t*>(take(size_t(R) * 4));
+  w.tk_stats = reinterpret_cast<int32_t*>(take(size_t(R) * 2 * 4));   // both ticket arrays, cleared together
+  w.tk_draw = w.tk_stats ? w.tk_stats + R : nullptr;
   w.cells = reinterpret_cast<float2*>(take(size_t(R) * ncell * sizeof(float2)));
   w.t2d = reinterpret_cast<int32_t*>(take(size_t(V) * 4));
   *total = off;
   return w;
 }
 
-template <typename T, int QF>
+template <typename T, int QF, bool TONE>
 cudaError_t vf_launch_draws(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
-  const dim3 mgrid(unsigned((a.V + VM_PART - 1) / VM_PART), unsigned(R));
-  const cudaError_t e = ds_launch(verify_mass_kernel<T, QF>, mgrid, dim3(VM_THREADS), 0, stream, a);
-  if (e != cudaSuccess) return e;
-  return ds_launch(verify_pick_kernel<T, QF>, dim3(unsigned(R)), dim3(VP_THREADS), 0, stream, a);
+  constexpr int PART = (QF == QF_SPARSE) ? VM_PART_SPARSE : VM_PART;
+  const dim3 grid(unsigned((a.V + PART - 1) / PART), unsigned(R));
+  return ds_launch(verify_draw_kernel<T, QF, TONE>, grid, dim3(VM_THREADS), 0, stream, a);
+}
+
+template <typename T, bool TONE>
+cudaError_t vf_launch_draws_form(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
+  switch (a.q_form) {
+    case QF_SPARSE: return vf_launch_draws<T, QF_SPARSE, TONE>(a, R, stream);
+    case QF_DENSE: return vf_launch_draws<T, QF_DENSE, TONE>(a, R, stream);
+    default: return vf_launch_draws<T, QF_DENSE_PRUNED, TONE>(a, R, stream);
+  }
 }
 
 template <typename T>
 cudaError_t vf_launch_draws_any(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
-  switch (a.q_form) {
-    case QF_SPARSE: return vf_launch_draws<T, QF_SPARSE>(a, R, stream);
-    case QF_DENSE: return vf_launch_draws<T, QF_DENSE>(a, R, stream);
-    default: return vf_launch_draws<T, QF_DENSE_PRUNED>(a, R, stream);
-  }
+  return a.T == 1.0f ? vf_launch_draws_form<T, true>(a, R, stream) : vf_launch_draws_form<T, false>(a, R, stream);
 }
 
 }  // namespace
@@ -809,8 +851,10 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
     DS_CUDA_TRY(cudaGetLastError());
   }
 
-  // 1. statistics of every needed target row
-  if (greedy || !(top_p < 1.0f)) {
+  DS_CUDA_TRY(cudaMemsetAsync(a.ws.tk_stats, 0, size_t(R) * 2 * sizeof(int32_t), stream));
+  // 1. statistics of every needed target row, and the acceptance tests
+  const bool lean = greedy || !(top_p < 1.0f);
+  if (lean) {
     const int64_t grid = std::min<int64_t>(R * (B + 1), int64_t(ds_num_sms()) * VS_PER_SM);
     if (dtype == DSPARK_BF16)
       DS_CUDA_TRY(ds_launch(verify_stats_kernel<__nv_bfloat16>, dim3(unsigned(grid)), dim3(VS_THREADS), 0, stream, a,
@@ -846,16 +890,13 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.probe_w = a.ws.probe_w;
   sa.amax_out = greedy ? a.ws.amax : nullptr;
   DS_CUDA_TRY(rs::sample_rows(sa, R * (B + 1), dtype == DSPARK_BF16, 0, stream));
-  }
-
-  // 2. acceptance tests, one warp per request
   DS_CUDA_TRY(ds_launch(verify_accept_kernel, dim3(unsigned((R * 32 + 127) / 128)), dim3(128), 0, stream, a, R));
-
-  // 3-4. residual or bonus draws
-  if (!greedy) {
-    const cudaError_t e = dtype == DSPARK_BF16 ? vf_launch_draws_any<__nv_bfloat16>(a, R, stream)
-                                               : vf_launch_draws_any<float>(a, R, stream);
-    DS_CUDA_TRY(e);
   }
+
+  if (greedy) return DSPARK_OK;
+  // 2. residual or bonus draws
+  const cudaError_t e = dtype == DSPARK_BF16 ? vf_launch_draws_any<__nv_bfloat16>(a, R, stream)
+                                             : vf_launch_draws_any<float>(a, R, stream);
+  DS_CUDA_TRY(e);
   return DSPARK_OK;
 }
