@@ -34,20 +34,25 @@
 namespace {
 
 constexpr int DW_M = 128;                    // vocabulary rows per tile (MMA M)
-constexpr int DW_MAXR = 128;                 // requests per GEMM launch (MMA N <= 128)
-constexpr int DW_NS = 8;                     // K-chunk stages in the ring (16 KB each)
-constexpr int DW_PROD = 128;                 // producer threads (warps 0-3)
+constexpr int DW_MAXR = 128;                 // requests per GEMM launch with bf16 logits (MMA N <= 128)
+constexpr int DW_MAXR_F32 = 64;              // with float32 logits (their staged tiles are twice as large)
+constexpr int DW_NS_MAX = 8;                 // K-chunk stages of the W ring (16 KB each)
+constexpr int DW_NL_MAX = 4;                 // staged logits tiles
+constexpr int DW_WPROD = 64;                 // W producers (warps 0-1; thread 0 alone with TMA)
+constexpr int DW_LOAD0 = 64;                 // logits loaders (warps 2-3)
+constexpr int DW_LOAD = 64;
 constexpr int DW_MMA_WARP = 4;
 constexpr int DW_EPI_WARP0 = 5;              // epilogue warps 5..12
 constexpr int DW_EPI = 256;
-constexpr int DW_THREADS = DW_PROD + 32 + DW_EPI;
+constexpr int DW_THREADS = DW_WPROD + DW_LOAD + 32 + DW_EPI;
 constexpr uint32_t DW_STAGE = DW_M * 128;    // bytes of one K-chunk of a tile
+constexpr size_t DW_SMEM_BUDGET = 216 * 1024;
 
 struct DwArgs {
   const void* logits;
   int64_t ld;
   const int64_t* row_start;
-  int32_t B, j, R, rank;
+  int32_t B, j, R, Rp, rank, ns, nl;
   int64_t V, V_t, ntiles;
   const int32_t* prev_cur;
   const __nv_bfloat16* E;
@@ -61,6 +66,7 @@ struct DwArgs {
   int32_t* status;
   uint32_t first_wait;       // polls of the epilogue's first wait for an accumulator
   int use_tma;               // W rows are contiguous (no d2t): one TMA load fills a stage
+  int lvec;                  // every logits row starts on a 16-byte boundary
 };
 
 template <bool XFORM>
@@ -99,36 +105,15 @@ __global__ void __launch_bounds__(128) dense_walk_gate_kernel(const HT* hidden, 
   }
 }
 
-// Eight consecutive logits of a row as float (vector load when aligned and whole; zero past V)
-template <typename T>
-DS_DEV void dw_ld8(const T* p, int64_t i, int64_t V, float (&x)[8]) {
-  if (i + 8 <= V && (reinterpret_cast<uintptr_t>(p + i) & 15) == 0) {
-    if constexpr (sizeof(T) == 2) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p + i));
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = ds_vec_elem<T>(v, e);
-    } else {
-      const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(p + i)), v1 = __ldcs(reinterpret_cast<const uint4*>(p + i) + 1);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[e] = ds_vec_elem<T>(v0, e);
-        x[e + 4] = ds_vec_elem<T>(v1, e);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = (i + e < V) ? ds_load_elem<T>(p + i + e) : 0.0f;
-  }
-}
-
-// D[request, vocabulary] = E[prev] . W[m(i)]^T: TMEM lanes are requests (M = 128, rows past R
-// zero), columns the tile's 128 vocabulary indices, so an epilogue lane owns one request: its logits
-// and z are contiguous vectors and its maximum is a running value in a register.
+// D[vocabulary, request] = W[m(i)] . E[prev]^T: TMEM lanes are the tile's 128 vocabulary rows and
+// columns the requests (N = R rounded up to 16), so an epilogue lane owns one vocabulary index and
+// every load and store of a warp is one contiguous stretch of one request's row.
 template <typename T, bool XFORM, bool TONE>
 __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const DwArgs a,
                                                                        const __grid_constant__ CUtensorMap tmW) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t s_full[DW_NS], s_empty[DW_NS], s_accf[2], s_acce[2], s_drain;
+  __shared__ uint64_t s_full[DW_NS_MAX], s_empty[DW_NS_MAX], s_lfull[DW_NL_MAX], s_lempty[DW_NL_MAX];
+  __shared__ uint64_t s_accf[2], s_acce[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_prev[DW_MAXR];
@@ -136,19 +121,24 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
   __shared__ int64_t s_lrow[DW_MAXR];
   __shared__ unsigned long long s_kmax[DW_MAXR];
 
-  const int rank = a.rank, nkb = rank / 64;
+  const int R = a.R, Rp = a.Rp, ns = a.ns, nl = a.nl, nkb = a.rank / 64;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;                                  // nkb x [128 request rows x 128 B]
-  uint8_t* sB = base + nkb * (DW_MAXR * 128);          // DW_NS x [128 vocabulary rows x 128 B]
-  constexpr uint32_t ncols = 2 * DW_M;                 // two accumulators of 128 columns
+  uint8_t* sW = base;                                           // ns x [128 vocabulary rows x 128 B]
+  uint8_t* sA = sW + size_t(ns) * DW_STAGE;                     // nkb x [Rp request rows x 128 B]
+  T* sL = reinterpret_cast<T*>(sA + size_t(nkb) * Rp * 128);    // nl x [Rp requests x 128 logits]
+  const size_t lstride = size_t(Rp) * DW_M;                     // elements of one staged logits tile
+  constexpr uint32_t ncols = 2 * DW_M;                          // two accumulators of up to 128 columns
 
   ds_pdl_trigger();
-  ds_pdl_wait();                                       // previous tokens come from the last position
   if (tid == 0) {
-    for (int s = 0; s < DW_NS; ++s) {
-      ds_mbar_init(&s_full[s], a.use_tma ? 1 : DW_PROD);
+    for (int s = 0; s < ns; ++s) {
+      ds_mbar_init(&s_full[s], a.use_tma ? 1 : DW_WPROD);
       ds_mbar_init(&s_empty[s], 1);
+    }
+    for (int l = 0; l < nl; ++l) {
+      ds_mbar_init(&s_lfull[l], DW_LOAD);
+      ds_mbar_init(&s_lempty[l], DW_EPI / 32);
     }
     for (int b = 0; b < 2; ++b) {
       ds_mbar_init(&s_accf[b], 1);
@@ -157,75 +147,55 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
     ds_mbar_init(&s_drain, 1);
     s_abort = 0;
   }
-  if (warp == DW_MMA_WARP) ds_tmem_alloc(&s_tmem, ncols);
   for (int r = tid; r < DW_MAXR; r += DW_THREADS) {
-    int32_t p = -1;
-    if (r < a.R) {
-      p = a.prev_cur[r];
-      if (p < 0 || p >= a.V_t) {
-        ds_set_error(a.status, DSPARK_ERANGE);
-        p = -1;
-      }
-      s_gate[r] = a.gate[int64_t(r) * a.B + a.j];
-      s_lrow[r] = a.row_start ? a.row_start[r] + a.j : int64_t(r) * a.B + a.j;
-    }
-    s_prev[r] = p;
+    if (r < R) s_lrow[r] = a.row_start ? a.row_start[r] + a.j : int64_t(r) * a.B + a.j;
     s_kmax[r] = 0ull;
   }
   __syncthreads();
-  // the A operand: E[prev_r] of every request (zero rows past R and for bad ids), once. With at
-  // most 64 requests, rows 64..127 repeat rows 0..63, so every TMEM lane quarter holds requests.
-  const bool dup = a.R <= 64;
-  const int cpr = rank / 8;
-  for (int t = tid; t < DW_MAXR * cpr; t += DW_THREADS) {
-    const int m = t / cpr, c = t % cpr, kb = c >> 3, cc = c & 7;
-    uint8_t* dst = sA + kb * (DW_MAXR * 128) + m * 128 + ((cc ^ (m & 7)) << 4);
-    const int32_t id = s_prev[dup ? (m & 63) : m];
-    if (id >= 0) ds_cp_async16(dst, a.E + int64_t(id) * rank + c * 8);
-    else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-  }
-  ds_cp_async_wait_all();
-  ds_fence_proxy_async_smem();
-  __syncthreads();
-  ds_tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+  auto wait = [&](uint64_t* bar, uint32_t parity, uint32_t limit) {
+    if (!ds_mbar_wait_or_abort(bar, parity, limit, &s_abort)) {
+      if (!aborted()) ds_set_error(a.status, DSPARK_ETIMEOUT);
+      s_abort = 1;
+    }
+    return !aborted();
+  };
 
-  if (warp < DW_PROD / 32 && a.use_tma) {
-    // ---- producer: one thread loads each K-chunk of a tile (128 contiguous W rows x 128 bytes,
+  // The table and the logits are inputs that no kernel of this library writes, so the producers
+  // and loaders start before the wait for the previous kernel; the previous tokens (the B operand),
+  // the gates and everything written come after it.
+  if (warp < DW_WPROD / 32 && a.use_tma) {
+    // ---- W producer: one thread loads each K-chunk of a tile (128 contiguous W rows x 128 bytes,
     // 128-byte swizzle) with one TMA copy; rows past the table read as zero ----
     if (tid == 0) {
       const uint64_t pol = ds_policy_evict_last();
       uint32_t g = 0;
-      for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+      for (int64_t tile = blockIdx.x; tile < a.ntiles && !aborted(); tile += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const uint32_t s = g % DW_NS, ph = (g / DW_NS) & 1u;
-          if (!ds_mbar_wait_or_abort(&s_empty[s], ph ^ 1u, DS_WAIT_LIMIT, &s_abort)) {
-            if (!*reinterpret_cast<volatile int*>(&s_abort)) ds_set_error(a.status, DSPARK_ETIMEOUT);
-            s_abort = 1;
-          }
-          if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+          const uint32_t s = g % ns, ph = (g / ns) & 1u;
+          if (!wait(&s_empty[s], ph ^ 1u, DS_WAIT_LIMIT)) break;
           ds_mbar_arrive_expect_tx(&s_full[s], DW_STAGE);
-          ds_tma_load_2d(sB + s * DW_STAGE, &tmW, kb * 64, int32_t(tile * DW_M), &s_full[s], pol);
+          ds_tma_load_2d(sW + s * DW_STAGE, &tmW, kb * 64, int32_t(tile * DW_M), &s_full[s], pol);
         }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
       }
       // every TMA copy this thread issued lands before the CTA leaves (or the wait gives up)
-      for (uint32_t k = (g > DW_NS ? g - DW_NS : 0); k < g; ++k)
-        (void)ds_mbar_wait(&s_full[k % DW_NS], (k / DW_NS) & 1u, DS_WAIT_LIMIT);
+      for (uint32_t k = (g > uint32_t(ns) ? g - ns : 0); k < g; ++k)
+        (void)ds_mbar_wait(&s_full[k % ns], (k / ns) & 1u, DS_WAIT_LIMIT);
     }
     __syncwarp();
-  } else if (warp < DW_PROD / 32) {
-    // ---- producers: thread p copies 16-byte column p % 8 of rows p / 8 + 16 kk of each K-chunk ----
+  } else if (warp < DW_WPROD / 32) {
+    // ---- W producers (gathered rows m(i) = i + d2t[i]): thread p copies 16-byte column p % 8 of
+    // rows p / 8 + 8 kk of each K-chunk ----
     const uint64_t pol = ds_policy_evict_last();
     const int cc = tid & 7, m0 = tid >> 3;
-    uint32_t g = 0;                                    // K-chunks issued by this CTA
-    for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    uint32_t g = 0;
+    for (int64_t tile = blockIdx.x; tile < a.ntiles && !aborted(); tile += gridDim.x) {
       const int64_t i0 = tile * DW_M;
-      int64_t rid[8];
+      int64_t rid[16];
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int64_t i = i0 + m0 + 16 * kk;
-        int64_t t = -2;                                // -2: past the vocabulary (column never read)
+      for (int kk = 0; kk < 16; ++kk) {
+        const int64_t i = i0 + m0 + 8 * kk;
+        int64_t t = -2;                                // -2: past the vocabulary (row never read)
         if (i < a.V) {
           t = a.d2t ? i + a.d2t[i] : i;
           if (t < 0 || t >= a.V_t) {
@@ -236,20 +206,16 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
         rid[kk] = t;
       }
       for (int kb = 0; kb < nkb; ++kb, ++g) {
-        const uint32_t s = g % DW_NS, ph = (g / DW_NS) & 1u;
-        if (!ds_mbar_wait_or_abort(&s_empty[s], ph ^ 1u, DS_WAIT_LIMIT, &s_abort)) {
-          if (!*reinterpret_cast<volatile int*>(&s_abort)) ds_set_error(a.status, DSPARK_ETIMEOUT);
-          s_abort = 1;
-        }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        uint8_t* stage = sB + s * DW_STAGE;
+        const uint32_t s = g % ns, ph = (g / ns) & 1u;
+        if (!wait(&s_empty[s], ph ^ 1u, DS_WAIT_LIMIT)) break;
+        uint8_t* stage = sW + s * DW_STAGE;
         bool zeroed = false;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int m = m0 + 16 * kk;
+        for (int kk = 0; kk < 16; ++kk) {
+          const int m = m0 + 8 * kk;
           uint8_t* dst = stage + m * 128 + ((cc ^ (m & 7)) << 4);
           if (rid[kk] >= 0) {
-            ds_cp_async16_hint(dst, a.W + rid[kk] * rank + kb * 64 + cc * 8, pol);
+            ds_cp_async16_hint(dst, a.W + rid[kk] * a.rank + kb * 64 + cc * 8, pol);
           } else if (rid[kk] == -1) {
             *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
             zeroed = true;
@@ -258,153 +224,187 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
         if (zeroed) ds_fence_proxy_async_smem();
         ds_cp_async_mbar_arrive(&s_full[s]);
       }
-      if (*reinterpret_cast<volatile int*>(&s_abort)) break;
     }
     ds_cp_async_wait_all();                            // no copy lands after the CTA is gone
-  } else if (warp == DW_MMA_WARP) {
-    // ---- one thread issues the MMAs; the accumulator buffers alternate by tile ----
-    if (lane == 0) {
-      constexpr uint32_t idesc = ds_idesc_bf16_f32(DW_MAXR, DW_M);
-      const uint32_t aaddr = ds_smem_addr(sA), baddr = ds_smem_addr(sB);
-      uint32_t g = 0, k = 0;
-      for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
-        const uint32_t b = k & 1u, use = k >> 1;
-        if (!ds_mbar_wait_or_abort(&s_acce[b], (use & 1u) ^ 1u, DS_WAIT_LIMIT, &s_abort)) {
-          if (!*reinterpret_cast<volatile int*>(&s_abort)) ds_set_error(a.status, DSPARK_ETIMEOUT);
-          s_abort = 1;
-        }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        ds_tc_fence_after();
-        const uint32_t dacc = tmem + b * uint32_t(DW_M);
-        bool stop = false;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const uint32_t s = g % DW_NS, ph = (g / DW_NS) & 1u;
-          if (!ds_mbar_wait_or_abort(&s_full[s], ph, DS_WAIT_LIMIT, &s_abort)) {
-            if (!*reinterpret_cast<volatile int*>(&s_abort)) ds_set_error(a.status, DSPARK_ETIMEOUT);
-            s_abort = 1;
-          }
-          if (*reinterpret_cast<volatile int*>(&s_abort)) {
-            stop = true;
-            break;
-          }
-          ds_tc_fence_after();
-#pragma unroll
-          for (int sub = 0; sub < 4; ++sub) {
-            const uint64_t ad = ds_smem_desc_sw128(aaddr + kb * (DW_MAXR * 128) + sub * 32);
-            const uint64_t bd = ds_smem_desc_sw128(baddr + s * DW_STAGE + sub * 32);
-            ds_umma_f16(dacc, ad, bd, idesc, (kb | sub) != 0);
-          }
-          ds_umma_commit(&s_empty[s]);                 // the stage is free once these MMAs are done
-        }
-        if (stop) break;
-        ds_umma_commit(&s_accf[b]);                    // the tile's accumulator is complete
-      }
-      // every MMA this thread issued completes before tensor memory is released
-      ds_umma_commit(&s_drain);
-      (void)ds_mbar_wait(&s_drain, 0, DS_WAIT_LIMIT);
-    }
-    __syncwarp();
-  } else {
-    // ---- epilogue: warp ew reads TMEM lanes 32 (warp % 4) .. (requests). With duplicated request
-    // rows every warp owns one 32-column chunk of each tile and prefetches the next tile's logits
-    // for it; otherwise the quarters holding requests take chunks h and h + 2, h = ew / 4 ----
-    constexpr int VPC = 32 * int(sizeof(T)) / 16;      // 16-byte vectors of logits per chunk
-    const int ew = warp - DW_EPI_WARP0, q = warp & 3, h = ew >> 2;
-    const int r = dup ? (q & 1) * 32 + lane : q * 32 + lane;   // this lane's request
-    const bool live = r < a.R;
-    const bool any = dup || q * 32 < a.R;              // warp-uniform: the quarter holds requests
-    const int ch0 = dup ? (q >> 1) * 2 + h : h, chs = dup ? 4 : 2;
-    const T* lrow = live ? reinterpret_cast<const T*>(a.logits) + s_lrow[r] * a.ld : nullptr;
-    float* zrow = live ? a.z + (int64_t(r) * a.z_row_mul + a.z_row_add) * a.ldz : nullptr;
-    const float gam = live ? s_gate[r] : 0.0f;
-    const bool vec_l = live && (reinterpret_cast<uintptr_t>(lrow) & 15) == 0;
-    const bool vec_z = live && (reinterpret_cast<uintptr_t>(zrow) & 15) == 0;
-    auto fetch = [&](int64_t i0, uint4 (&buf)[VPC]) {  // one chunk's logits, whole vectors only
-      if (vec_l && i0 + 32 <= a.V) {
-#pragma unroll
-        for (int v = 0; v < VPC; ++v) buf[v] = __ldcs(reinterpret_cast<const uint4*>(lrow + i0) + v);
-      }
-    };
-    auto chunk = [&](int64_t i0, const uint4 (&buf)[VPC], float (&acc)[32], unsigned long long& kb) {
-      constexpr int EPV = 16 / int(sizeof(T));
-      const bool whole = vec_l && i0 + 32 <= a.V;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {                   // z in place of the accumulator
-        const float sv = whole ? ds_vec_elem<T>(buf[c / EPV], c % EPV) : ((i0 + c < a.V) ? ds_load_elem<T>(lrow + i0 + c) : 0.0f);
-        acc[c] = ds_temper_t<TONE>(__fmaf_rn(gam, acc[c], dw_xform<XFORM>(sv, a.mult, a.softcap)), a.Tz);
-        if (i0 + c < a.V) {
-          const unsigned long long key = ds_key64(ds_canon_zero(acc[c]), uint32_t(i0 + c));
-          kb = key > kb ? key : kb;
-        }
-      }
-      if (vec_z && i0 + 32 <= a.V) {
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          reinterpret_cast<float4*>(zrow + i0)[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (i0 + c < a.V) zrow[i0 + c] = acc[c];
-      }
-    };
-    // the next tile's logits are prefetched into registers for bf16 rows (the register budget of
-    // 13 warps, 128 a thread, does not hold two float32 chunks)
-    constexpr bool PREF = sizeof(T) == 2;
-    unsigned long long kbest = 0ull;
-    uint4 pf[VPC];
-    if (PREF && dup && live) fetch(int64_t(blockIdx.x) * DW_M + ch0 * 32, pf);
+  } else if (warp < (DW_WPROD + DW_LOAD) / 32) {
+    // ---- logits loaders: the tile's 128 logits of every request into [request][128], read once
+    // (L2 evict first); a ragged last tile or unaligned rows go element by element ----
+    const uint64_t pol = ds_policy_evict_first();
+    const int lt = tid - DW_LOAD0;
+    constexpr int EPV = 16 / int(sizeof(T));           // elements per 16-byte copy
+    constexpr int CPR = DW_M / EPV;                    // copies per request row
+    const T* lg = reinterpret_cast<const T*>(a.logits);
     uint32_t k = 0;
-    bool first = true;
     for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
-      const uint32_t b = k & 1u, use = k >> 1;
-      uint4 cur[VPC];
-      if (PREF && dup) {                               // this tile's logits; fetch the next tile's
+      const uint32_t lb = k % nl, ph = (k / nl) & 1u;
+      if (!wait(&s_lempty[lb], ph ^ 1u, DS_WAIT_LIMIT)) break;
+      T* dst = sL + lb * lstride;
+      const int64_t v0 = tile * DW_M;
+      if (a.lvec && v0 + DW_M <= a.V) {
+        for (int t = lt; t < R * CPR; t += DW_LOAD) {
+          const int cr = t / CPR, c = t % CPR;
+          ds_cp_async16_hint(dst + cr * DW_M + c * EPV, lg + s_lrow[cr] * a.ld + v0 + c * EPV, pol);
+        }
+        ds_cp_async_mbar_arrive(&s_lfull[lb]);
+      } else {
+        for (int t = lt; t < R * DW_M; t += DW_LOAD) {
+          const int cr = t / DW_M, c = t % DW_M;
+          dst[cr * DW_M + c] = (v0 + c < a.V) ? lg[s_lrow[cr] * a.ld + v0 + c] : T(0.0f);
+        }
+        ds_cp_async_wait_all();
+        ds_mbar_arrive(&s_lfull[lb]);
+      }
+    }
+    ds_cp_async_wait_all();
+  } else {
+    // ---- after the previous kernel: the MMA warp takes tensor memory, the epilogue warps stage
+    // the B operand E[prev_r] (zero rows past R and for bad ids) ----
+    ds_pdl_wait();
+    if (warp == DW_MMA_WARP) {
+      ds_tmem_alloc(&s_tmem, ncols);
+    } else {
+      const int et = tid - DW_EPI_WARP0 * 32;
+      for (int r = et; r < Rp; r += DW_EPI) {
+        int32_t p = -1;
+        float gm = 0.0f;
+        if (r < R) {
+          p = a.prev_cur[r];
+          if (p < 0 || p >= a.V_t) {
+            ds_set_error(a.status, DSPARK_ERANGE);
+            p = -1;
+          }
+          gm = a.gate[int64_t(r) * a.B + a.j];
+        }
+        s_prev[r] = p;
+        s_gate[r] = gm;
+      }
+      ds_named_sync(1, DW_EPI);
+      const int cpr = a.rank / 8;
+      for (int t = et; t < Rp * cpr; t += DW_EPI) {
+        const int m = t / cpr, c = t % cpr, kb = c >> 3, cc = c & 7;
+        uint8_t* dst = sA + kb * (Rp * 128) + m * 128 + ((cc ^ (m & 7)) << 4);
+        const int32_t id = s_prev[m];
+        if (id >= 0) ds_cp_async16(dst, a.E + int64_t(id) * a.rank + c * 8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
+      ds_cp_async_wait_all();
+      ds_fence_proxy_async_smem();
+    }
+    ds_tc_fence_before();
+    ds_named_sync(2, 32 + DW_EPI);
+    ds_tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == DW_MMA_WARP) {
+      // ---- one thread issues the MMAs; the accumulator buffers alternate by tile ----
+      if (lane == 0) {
+        const uint32_t idesc = ds_idesc_bf16_f32(DW_M, Rp);
+        const uint32_t waddr = ds_smem_addr(sW), aaddr = ds_smem_addr(sA);
+        uint32_t g = 0, k = 0;
+        for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
+          const uint32_t b = k & 1u, use = k >> 1;
+          if (!wait(&s_acce[b], (use & 1u) ^ 1u, DS_WAIT_LIMIT)) break;
+          ds_tc_fence_after();
+          const uint32_t dacc = tmem + b * uint32_t(DW_M);
+          bool stop = false;
+          for (int kb = 0; kb < nkb; ++kb, ++g) {
+            const uint32_t s = g % ns, ph = (g / ns) & 1u;
+            if (!wait(&s_full[s], ph, DS_WAIT_LIMIT)) {
+              stop = true;
+              break;
+            }
+            ds_tc_fence_after();
 #pragma unroll
-        for (int v = 0; v < VPC; ++v) cur[v] = pf[v];
-        if (live && tile + gridDim.x < a.ntiles) fetch((tile + gridDim.x) * DW_M + ch0 * 32, pf);
+            for (int sub = 0; sub < 4; ++sub) {
+              const uint64_t wd = ds_smem_desc_sw128(waddr + s * DW_STAGE + sub * 32);
+              const uint64_t ed = ds_smem_desc_sw128(aaddr + kb * (Rp * 128) + sub * 32);
+              ds_umma_f16(dacc, wd, ed, idesc, (kb | sub) != 0);
+            }
+            ds_umma_commit(&s_empty[s]);               // the stage is free once these MMAs are done
+          }
+          if (stop) break;
+          ds_umma_commit(&s_accf[b]);                  // the tile's accumulator is complete
+        }
+        // every MMA this thread issued completes before tensor memory is released
+        ds_umma_commit(&s_drain);
+        (void)ds_mbar_wait(&s_drain, 0, DS_WAIT_LIMIT);
       }
-      const bool ok =
-          ds_mbar_wait_or_abort(&s_accf[b], use & 1u, first ? a.first_wait : DS_WAIT_LIMIT, &s_abort);
-      first = false;
-      if (!ok) {
-        if (!*reinterpret_cast<volatile int*>(&s_abort)) ds_set_error(a.status, DSPARK_ETIMEOUT);
-        s_abort = 1;
-      }
-      if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-      ds_tc_fence_after();
-      if (any) {
-#pragma unroll 1
-        for (int ch = ch0; ch < DW_M / 32; ch += chs) {
+      __syncwarp();
+    } else {
+      // ---- epilogue: warp (q, h) reads TMEM lanes 32 q.. (vocabulary rows) and the 32-request
+      // column chunks h, h + 2; per request the warp reduces its 32 keys (largest z, lowest index)
+      // and lane c keeps the running best of request 32 kc + c ----
+      const int q = warp & 3, h = (warp - DW_EPI_WARP0) >> 2;
+      const int ql = q * 32 + lane;
+      const int64_t zstep = a.z_row_mul * a.ldz;
+      uint32_t best[2] = {0u, 0u}, bidx[2] = {0u, 0u};
+      uint32_t k = 0;
+      bool first = true;
+      for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
+        const uint32_t b = k & 1u, use = k >> 1, lb = k % nl;
+        if (!wait(&s_accf[b], use & 1u, first ? a.first_wait : DS_WAIT_LIMIT)) break;
+        first = false;
+        if (!wait(&s_lfull[lb], (k / nl) & 1u, DS_WAIT_LIMIT)) break;
+        ds_tc_fence_after();
+        const int64_t v = tile * DW_M + ql;
+        const bool valid = v < a.V;
+        const T* L = sL + lb * lstride + ql;
+        float* zv = a.z + a.z_row_add * a.ldz + v;
+#pragma unroll
+        for (int sc = 0; sc < 2; ++sc) {
+          const int kc = h + 2 * sc;
+          if (kc * 32 >= R) break;                     // warp-uniform
           float acc[32];
-          ds_tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + b * uint32_t(DW_M) + uint32_t(ch * 32), acc);
-          const int64_t i0 = tile * DW_M + ch * 32;
-          if (live && i0 < a.V) {
-            if (!(PREF && dup)) fetch(i0, cur);
-            chunk(i0, cur, acc, kbest);
+          ds_tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + b * uint32_t(DW_M) + uint32_t(kc * 32), acc);
+          float* zp = zv + int64_t(kc * 32) * zstep;
+#pragma unroll
+          for (int c = 0; c < 32; ++c, zp += zstep) {
+            const int cr = kc * 32 + c;
+            if (cr >= R) break;                        // warp-uniform
+            const float x = dw_xform<XFORM>(ds_load_elem<T>(L + cr * DW_M), a.mult, a.softcap);
+            const float zc = ds_temper_t<TONE>(__fmaf_rn(s_gate[cr], acc[c], x), a.Tz);
+            if (valid) *zp = zc;
+            const uint32_t ob = valid ? ds_key32(ds_canon_zero(zc)) : 0u;
+            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ob);
+            const uint32_t cur = __shfl_sync(0xFFFFFFFFu, best[sc], c);
+            if (mx > cur) {                            // warp-uniform; ties keep the earlier tile
+              const unsigned bal = __ballot_sync(0xFFFFFFFFu, ob == mx);
+              if (lane == c) {
+                best[sc] = mx;
+                bidx[sc] = uint32_t(tile * DW_M + q * 32 + __ffs(int(bal)) - 1);
+              }
+            }
           }
         }
+        ds_tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ds_mbar_arrive(&s_acce[b]);
+          ds_mbar_arrive(&s_lempty[lb]);
+        }
       }
-      ds_tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ds_mbar_arrive(&s_acce[b]);
+#pragma unroll
+      for (int sc = 0; sc < 2; ++sc) {
+        const int cr = (h + 2 * sc) * 32 + lane;
+        if (cr < R && best[sc] != 0u)
+          atomicMax(&s_kmax[cr], (static_cast<unsigned long long>(best[sc]) << 32) | (0xFFFFFFFFull - bidx[sc]));
+      }
+      ds_named_sync(1, DW_EPI);                        // every epilogue warp has folded its keys
+      for (int rr = tid - DW_EPI_WARP0 * 32; rr < R; rr += DW_EPI)
+        if (s_kmax[rr] != 0ull) atomicMax(&a.zkey[int64_t(rr) * a.B + a.j], s_kmax[rr]);
     }
-    if (live && kbest != 0ull) atomicMax(&s_kmax[r], kbest);
-    ds_named_sync(1, DW_EPI);                          // every epilogue warp has folded its keys
-    for (int rr = tid - DW_EPI_WARP0 * 32; rr < a.R; rr += DW_EPI)
-      if (s_kmax[rr] != 0ull) atomicMax(&a.zkey[int64_t(rr) * a.B + a.j], s_kmax[rr]);
   }
   __syncthreads();
   if (warp == DW_MMA_WARP) {
     ds_tc_fence_after();
-    ds_tmem_dealloc(tmem, ncols);
+    ds_tmem_dealloc(s_tmem, ncols);
   }
 }
 
 // ---- sampled positions without a nucleus: draws over the z rows ------------------------------
-constexpr int DD_THREADS = 512;
+constexpr int DD_THREADS = 256;
 constexpr int DD_WARPS = DD_THREADS / 32;
 constexpr int DD_CELL = 256;                 // indices per cell: one warp, eight consecutive a lane
-constexpr int DD_PART = 32768;               // indices per CTA (128 cells)
 
 struct DwDraw {
   const float* z;
@@ -422,7 +422,7 @@ struct DwDraw {
   int has_q;
   int64_t q_row_mul, q_row_add;
   float2* cells;                             // [R, ncell]
-  int64_t ncell;
+  int64_t ncell, part_cells;                 // cells of a row, cells of one CTA
   int32_t* ticket;                           // [R]
   int32_t* status;
 };
@@ -467,7 +467,7 @@ DS_DEV void dd_w8(const float* zr, int64_t t, int64_t V, float zmax, float (&w)[
   }
 }
 
-__global__ void __launch_bounds__(DD_THREADS) dense_walk_draw_kernel(const DwDraw d) {
+__global__ void __launch_bounds__(DD_THREADS, 3) dense_walk_draw_kernel(const DwDraw d) {
   __shared__ double s_run[DD_THREADS + 1];
   __shared__ int s_last;
   __shared__ int64_t s_cell, s_pick;
@@ -488,19 +488,18 @@ __global__ void __launch_bounds__(DD_THREADS) dense_walk_draw_kernel(const DwDra
   }
   const float* zr = d.z + (r * d.z_row_mul + d.z_row_add) * d.ldz;
   float2* cells = d.cells + r * d.ncell;
-  const int64_t t0 = int64_t(blockIdx.x) * DD_PART;
-  constexpr int CPP = DD_PART / DD_CELL;
-  for (int k0 = warp; k0 < CPP; k0 += 4 * DD_WARPS) {  // four cells per warp in flight
+  const int64_t cbeg = int64_t(blockIdx.x) * d.part_cells, cend = min(d.ncell, cbeg + d.part_cells);
+  for (int64_t k0 = cbeg + warp; k0 < cend; k0 += 4 * DD_WARPS) {  // four cells per warp in flight
     float w[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t t = t0 + int64_t(k0 + u * DD_WARPS) * DD_CELL + lane * 8;
-      if (t < d.V) dd_w8(zr, t, d.V, zmax, w[u]);
+      const int64_t t = (k0 + u * DD_WARPS) * DD_CELL + lane * 8;
+      if (k0 + u * DD_WARPS < cend && t < d.V) dd_w8(zr, t, d.V, zmax, w[u]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t c = t0 / DD_CELL + k0 + u * DD_WARPS;
-      if (c * DD_CELL >= d.V) continue;                // warp-uniform
+      const int64_t c = k0 + u * DD_WARPS;
+      if (c >= cend) continue;                         // warp-uniform
       const int64_t t = c * DD_CELL + lane * 8;
       rs::FF m{0.0f, 0.0f};
       if (t < d.V) {
@@ -676,10 +675,23 @@ bool dw_tensor_map(CUtensorMap* m, const void* W, int64_t V_t, int rank) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared memory of one GEMM CTA: the W ring, the B operand and the staged logits tiles. The ring
+// and the logits tiles take what the budget leaves after the B operand (at least 4 and 2).
+void dw_plan_smem(DwArgs& a, size_t elem) {
+  const size_t abytes = size_t(a.rank / 64) * a.Rp * 128, lbytes = size_t(a.Rp) * DW_M * elem;
+  int nl = DW_NL_MAX;
+  while (nl > 2 && abytes + nl * lbytes + 4 * size_t(DW_STAGE) > DW_SMEM_BUDGET) --nl;
+  a.nl = nl;
+  a.ns = int(std::min<size_t>(DW_NS_MAX, (DW_SMEM_BUDGET - abytes - nl * lbytes) / DW_STAGE));
+}
+size_t dw_smem_bytes(const DwArgs& a, size_t elem) {
+  return size_t(a.ns) * DW_STAGE + size_t(a.rank / 64) * a.Rp * 128 + size_t(a.nl) * a.Rp * DW_M * elem + 1024;
+}
+
 template <typename T, bool XFORM, bool TONE>
 cudaError_t dw_launch_gemm_t(const DwArgs& a, const CUtensorMap& tm, cudaStream_t stream) {
   auto kern = dense_walk_gemm_kernel<T, XFORM, TONE>;
-  const size_t smem = size_t(a.rank / 64) * DW_MAXR * 128 + size_t(DW_NS) * DW_STAGE + 1024;
+  const size_t smem = dw_smem_bytes(a, sizeof(T));
   const cudaError_t e = ds_ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(a.ntiles, int64_t(ds_num_sms()));
@@ -689,6 +701,20 @@ cudaError_t dw_launch_gemm_t(const DwArgs& a, const CUtensorMap& tm, cudaStream_
 template <typename T, bool XFORM>
 cudaError_t dw_launch_gemm(const DwArgs& a, const CUtensorMap& tm, cudaStream_t stream) {
   return a.Tz == 1.0f ? dw_launch_gemm_t<T, XFORM, true>(a, tm, stream) : dw_launch_gemm_t<T, XFORM, false>(a, tm, stream);
+}
+
+// Draw CTAs resident on the whole GPU at once
+int dd_ctas_per_wave() {
+  static std::once_flag once;
+  static int per_sm = 1;
+  std::call_once(once, [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dense_walk_draw_kernel, DD_THREADS, 0) == cudaSuccess && n > 0)
+      per_sm = n;
+    else
+      (void)cudaGetLastError();
+  });
+  return per_sm * ds_num_sms();
 }
 
 size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
@@ -777,15 +803,21 @@ extern "C" dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtyp
   const int Cz = rs::cluster_size_for(V_d, 4);
   DS_REQUIRE(Cz > 0);
   const int64_t ncell = (V_d + DD_CELL - 1) / DD_CELL;
-  for (int64_t c0 = 0; c0 < R; c0 += DW_MAXR) {
-    const int32_t Rc = int32_t(std::min<int64_t>(DW_MAXR, R - c0));
+  const int64_t G = dtype == DSPARK_BF16 ? DW_MAXR : DW_MAXR_F32;   // requests per GEMM launch
+  const size_t esz = ds_dtype_size(dtype);
+  const bool lvec = ds_aligned(logits, 16) && (ld * int64_t(esz)) % 16 == 0;
+  for (int64_t c0 = 0; c0 < R; c0 += G) {
+    const int32_t Rc = int32_t(std::min<int64_t>(G, R - c0));
     DwArgs a = {};
     a.logits = reinterpret_cast<const uint8_t*>(logits) + (row_start ? 0 : c0 * B * ld * ds_dtype_size(dtype));
     a.ld = ld;
     a.row_start = row_start ? row_start + c0 : nullptr;
     a.B = B;
     a.R = Rc;
+    a.Rp = (Rc + 15) / 16 * 16;
     a.rank = rank;
+    dw_plan_smem(a, esz);
+    a.lvec = lvec ? 1 : 0;
     a.V = V_d;
     a.V_t = V_t;
     a.ntiles = (V_d + DW_M - 1) / DW_M;
@@ -827,6 +859,10 @@ extern "C" dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtyp
     d.prev_cur = w.prev_cur + c0;
     d.cells = w.cells;
     d.ncell = ncell;
+    {  // one wave of draw CTAs: the parts of a row split the cells evenly
+      const int64_t parts = std::max<int64_t>(1, std::min<int64_t>(ncell, int64_t(dd_ctas_per_wave()) / Rc));
+      d.part_cells = (ncell + parts - 1) / parts;
+    }
     d.ticket = w.ticket + c0;
     d.status = dev_status;
     if (record) {
@@ -879,7 +915,7 @@ extern "C" dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtyp
       if (greedy) {
         DS_CUDA_TRY(ds_launch(dense_walk_greedy_kernel, dim3(unsigned((Rc + 127) / 128)), dim3(128), 0, st, d, Rc));
       } else if (!nucleus) {
-        const dim3 grid(unsigned((V_d + DD_PART - 1) / DD_PART), unsigned(Rc));
+        const dim3 grid(unsigned((ncell + d.part_cells - 1) / d.part_cells), unsigned(Rc));
         DS_CUDA_TRY(ds_launch(dense_walk_draw_kernel, grid, dim3(DD_THREADS), 0, st, d));
       } else {
         sa.row_base = record ? j : 0;

@@ -536,6 +536,12 @@ DS_DEV uint64_t ds_policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// An L2 policy that lets lines go first (evict first), for data read once.
+DS_DEV uint64_t ds_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 DS_DEV void ds_cp_async16_hint(void* smem_dst, const void* gmem_src, uint64_t pol) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(ds_smem_addr(smem_dst)),
                "l"(gmem_src), "l"(pol)
