@@ -9,20 +9,25 @@
 //
 // Per position j (B positions run in sequence; position j + 1 needs the token drawn at j):
 //  1. dense_walk_gemm_kernel - a persistent, warp-specialised tcgen05 GEMM over the draft
-//     vocabulary in 128-row tiles. The W rows m(i) of a tile go into a ring of 128-byte swizzled
-//     K-chunks, one stage per mbarrier, with an L2 evict-last policy (the table is read again at
-//     every position): one TMA copy per stage when the rows are contiguous (no d2t), else four
-//     producer warps gathering them with cp.async; one thread issues the MMAs (M = 128 request rows
-//     of E[prev_r], staged once; N = the tile's 128 vocabulary rows; K = rank) into one of two TMEM
-//     accumulators; the epilogue warps drain the other accumulator, one request per TMEM lane, so
-//     each lane reads its logits and writes z = (s + gamma tau) / T into the dense record (or the
-//     workspace) as contiguous vectors, and keeps its request's largest (z, lowest index) key in a
-//     register (then reduced across the CTA and the GPU).
-//  2. sampled positions without a nucleus: dense_walk_draw_kernel - the z rows in parts over many
-//     CTAs: weights of z - zmax, the kept mass of every cell of 256 indices; the part that finishes
-//     last draws the token (double running sums over the cells, then the cell's elements) and
-//     writes it as the next position's previous token. Greedy positions finish with the argmax key
-//     (dense_walk_greedy_kernel); nucleus positions use the row sampler of sample.cu on the z rows.
+//     vocabulary in 128-row tiles, D[vocabulary, request] = W[m(i)] . E[prev]^T: TMEM lanes are the
+//     tile's vocabulary rows, columns the requests. The W rows m(i) of a tile go into a ring of
+//     128-byte swizzled K-chunks, one stage per mbarrier (one TMA copy per stage when the rows are
+//     contiguous, no d2t; else two producer warps gathering them with cp.async). Two loader warps
+//     stage the tile's logits of every request into shared memory. One thread issues the MMAs
+//     (M = 128 vocabulary rows, N = the requests rounded up to 16, K = rank) into one of two or
+//     four TMEM accumulators; the epilogue warps drain another, one vocabulary index per lane, so
+//     each load and store of a warp is one contiguous stretch of one request's row, and write
+//     z = (s + gamma tau) / T into the dense record (or the workspace). Every lane keeps the running
+//     largest (z, lowest index) key of its index for each request (or the warp reduces them per
+//     tile), then the CTA and the GPU fold them. The table, the logits and z are all streamed once
+//     per position with an L2 evict-first policy: the 78 MB table does not stay in L2 next to the
+//     other streams, and marking it evict-last only pushes out the z rows the draw reads next.
+//  2. sampled positions without a nucleus: dense_walk_draw_kernel - the z rows (mostly from L2)
+//     in parts over one wave of CTAs: weights of z - zmax, the kept mass of every cell of 1024
+//     indices; the part that finishes last draws the token with float-pair running sums over the
+//     cells, then the cell's elements, and writes it as the next position's previous token. Greedy
+//     positions finish with the argmax key (dense_walk_greedy_kernel); nucleus positions use the
+//     row sampler of sample.cu on the z rows.
 #include <cuda.h>
 
 #include <cstring>
@@ -113,7 +118,7 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
                                                                        const __grid_constant__ CUtensorMap tmW) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t s_full[DW_NS_MAX], s_empty[DW_NS_MAX], s_lfull[DW_NL_MAX], s_lempty[DW_NL_MAX];
-  __shared__ uint64_t s_accf[2], s_acce[2], s_drain;
+  __shared__ uint64_t s_accf[4], s_acce[4], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_prev[DW_MAXR];
@@ -128,7 +133,9 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
   uint8_t* sA = sW + size_t(ns) * DW_STAGE;                     // nkb x [Rp request rows x 128 B]
   T* sL = reinterpret_cast<T*>(sA + size_t(nkb) * Rp * 128);    // nl x [Rp requests x 128 logits]
   const size_t lstride = size_t(Rp) * DW_M;                     // elements of one staged logits tile
-  constexpr uint32_t ncols = 2 * DW_M;                          // two accumulators of up to 128 columns
+  constexpr uint32_t ncols = 2 * DW_M;                          // tensor memory columns taken
+  const uint32_t acs = Rp <= 64 ? 64u : 128u;                   // columns of one accumulator
+  const uint32_t nacc = ncols / acs;                            // 4 or 2 accumulators
 
   ds_pdl_trigger();
   if (tid == 0) {
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
       ds_mbar_init(&s_lfull[l], DW_LOAD);
       ds_mbar_init(&s_lempty[l], DW_EPI / 32);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (uint32_t b = 0; b < nacc; ++b) {
       ds_mbar_init(&s_accf[b], 1);
       ds_mbar_init(&s_acce[b], DW_EPI / 32);
     }
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
     // ---- W producer: one thread loads each K-chunk of a tile (128 contiguous W rows x 128 bytes,
     // 128-byte swizzle) with one TMA copy; rows past the table read as zero ----
     if (tid == 0) {
-      const uint64_t pol = ds_policy_evict_last();
+      const uint64_t pol = ds_policy_evict_first();
       uint32_t g = 0;
       for (int64_t tile = blockIdx.x; tile < a.ntiles && !aborted(); tile += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++g) {
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
   } else if (warp < DW_WPROD / 32) {
     // ---- W producers (gathered rows m(i) = i + d2t[i]): thread p copies 16-byte column p % 8 of
     // rows p / 8 + 8 kk of each K-chunk ----
-    const uint64_t pol = ds_policy_evict_last();
+    const uint64_t pol = ds_policy_evict_first();
     const int cc = tid & 7, m0 = tid >> 3;
     uint32_t g = 0;
     for (int64_t tile = blockIdx.x; tile < a.ntiles && !aborted(); tile += gridDim.x) {
@@ -302,10 +309,10 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
         const uint32_t waddr = ds_smem_addr(sW), aaddr = ds_smem_addr(sA);
         uint32_t g = 0, k = 0;
         for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
-          const uint32_t b = k & 1u, use = k >> 1;
+          const uint32_t b = k % nacc, use = k / nacc;
           if (!wait(&s_acce[b], (use & 1u) ^ 1u, DS_WAIT_LIMIT)) break;
           ds_tc_fence_after();
-          const uint32_t dacc = tmem + b * uint32_t(DW_M);
+          const uint32_t dacc = tmem + b * acs;
           bool stop = false;
           for (int kb = 0; kb < nkb; ++kb, ++g) {
             const uint32_t s = g % ns, ph = (g / ns) & 1u;
@@ -337,11 +344,21 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
       const int q = warp & 3, h = (warp - DW_EPI_WARP0) >> 2;
       const int ql = q * 32 + lane;
       const int64_t zstep = a.z_row_mul * a.ldz;
+      // With one chunk a warp (R <= 64) and at most 255 tiles a CTA, every lane keeps the running
+      // best key of its own index for each of the chunk's 32 requests, with the tile ordinal of
+      // that best in a byte, and the warp reduces them once at the end; otherwise each request's
+      // 32 keys are reduced across the warp at every tile.
+      const bool regmax = Rp <= 64 && (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x <= 255;
+      uint32_t bk[32], bt[8];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) bk[c] = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) bt[c] = 0u;
       uint32_t best[2] = {0u, 0u}, bidx[2] = {0u, 0u};
       uint32_t k = 0;
       bool first = true;
       for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++k) {
-        const uint32_t b = k & 1u, use = k >> 1, lb = k % nl;
+        const uint32_t b = k % nacc, use = k / nacc, lb = k % nl;
         if (!wait(&s_accf[b], use & 1u, first ? a.first_wait : DS_WAIT_LIMIT)) break;
         first = false;
         if (!wait(&s_lfull[lb], (k / nl) & 1u, DS_WAIT_LIMIT)) break;
@@ -350,29 +367,49 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
         const bool valid = v < a.V;
         const T* L = sL + lb * lstride + ql;
         float* zv = a.z + a.z_row_add * a.ldz + v;
+        if (regmax) {
+          if (h * 32 < R) {                            // warp-uniform
+            float acc[32];
+            ds_tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + b * acs + uint32_t(h * 32), acc);
+            float* zp = zv + int64_t(h * 32) * zstep;
 #pragma unroll
-        for (int sc = 0; sc < 2; ++sc) {
-          const int kc = h + 2 * sc;
-          if (kc * 32 >= R) break;                     // warp-uniform
-          float acc[32];
-          ds_tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + b * uint32_t(DW_M) + uint32_t(kc * 32), acc);
-          float* zp = zv + int64_t(kc * 32) * zstep;
+            for (int c = 0; c < 32; ++c, zp += zstep) {
+              const int cr = h * 32 + c;
+              if (cr >= R) break;                      // warp-uniform
+              const float x = dw_xform<XFORM>(ds_load_elem<T>(L + cr * DW_M), a.mult, a.softcap);
+              const float zc = ds_temper_t<TONE>(__fmaf_rn(s_gate[cr], acc[c], x), a.Tz);
+              if (valid) *zp = zc;
+              const uint32_t ob = valid ? ds_key32(ds_canon_zero(zc)) : 0u;
+              const bool up = ob > bk[c];              // ties keep the earlier tile (lower index)
+              bk[c] = up ? ob : bk[c];
+              bt[c >> 2] = up ? ((bt[c >> 2] & ~(0xFFu << (8 * (c & 3)))) | (k << (8 * (c & 3)))) : bt[c >> 2];
+            }
+          }
+        } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c, zp += zstep) {
-            const int cr = kc * 32 + c;
-            if (cr >= R) break;                        // warp-uniform
-            const float x = dw_xform<XFORM>(ds_load_elem<T>(L + cr * DW_M), a.mult, a.softcap);
-            const float zc = ds_temper_t<TONE>(__fmaf_rn(s_gate[cr], acc[c], x), a.Tz);
-            if (valid) *zp = zc;
-            const uint32_t ob = valid ? ds_key32(ds_canon_zero(zc)) : 0u;
-            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ob);
-            const uint32_t cur = __shfl_sync(0xFFFFFFFFu, best[sc], c);
-            if (mx > cur) {                            // warp-uniform; ties keep the earlier tile
+          for (int sc = 0; sc < 2; ++sc) {
+            const int kc = h + 2 * sc;
+            if (kc * 32 >= R) break;                   // warp-uniform
+            float acc[32];
+            ds_tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + b * acs + uint32_t(kc * 32), acc);
+            float* zp = zv + int64_t(kc * 32) * zstep;
+            uint32_t tmx = 0u, tbal = 0u;              // lane c: the tile's best of request 32 kc + c
+#pragma unroll
+            for (int c = 0; c < 32; ++c, zp += zstep) {
+              const int cr = kc * 32 + c;
+              if (cr >= R) break;                      // warp-uniform
+              const float x = dw_xform<XFORM>(ds_load_elem<T>(L + cr * DW_M), a.mult, a.softcap);
+              const float zc = ds_temper_t<TONE>(__fmaf_rn(s_gate[cr], acc[c], x), a.Tz);
+              if (valid) *zp = zc;
+              const uint32_t ob = valid ? ds_key32(ds_canon_zero(zc)) : 0u;
+              const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, ob);
               const unsigned bal = __ballot_sync(0xFFFFFFFFu, ob == mx);
-              if (lane == c) {
-                best[sc] = mx;
-                bidx[sc] = uint32_t(tile * DW_M + q * 32 + __ffs(int(bal)) - 1);
-              }
+              tmx = lane == c ? mx : tmx;
+              tbal = lane == c ? bal : tbal;
+            }
+            if (tmx > best[sc]) {                      // ties keep the earlier tile (lower indices)
+              best[sc] = tmx;
+              bidx[sc] = uint32_t(tile * DW_M + q * 32 + __ffs(int(tbal)) - 1);
             }
           }
         }
@@ -383,11 +420,29 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
           ds_mbar_arrive(&s_lempty[lb]);
         }
       }
+      if (regmax) {
+        // per request: the largest (key, lowest index) over the warp's lanes
 #pragma unroll
-      for (int sc = 0; sc < 2; ++sc) {
-        const int cr = (h + 2 * sc) * 32 + lane;
-        if (cr < R && best[sc] != 0u)
-          atomicMax(&s_kmax[cr], (static_cast<unsigned long long>(best[sc]) << 32) | (0xFFFFFFFFull - bidx[sc]));
+        for (int c = 0; c < 32; ++c) {
+          const int cr = h * 32 + c;
+          if (cr >= R) break;                          // warp-uniform
+          const uint32_t kt = (bt[c >> 2] >> (8 * (c & 3))) & 0xFFu;
+          const uint32_t vi = uint32_t((int64_t(blockIdx.x) + int64_t(kt) * gridDim.x) * DW_M + ql);
+          unsigned long long key = bk[c] ? ((static_cast<unsigned long long>(bk[c]) << 32) | (0xFFFFFFFFull - vi)) : 0ull;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+            key = other > key ? other : key;
+          }
+          if (lane == 0 && key != 0ull) atomicMax(&s_kmax[cr], key);
+        }
+      } else {
+#pragma unroll
+        for (int sc = 0; sc < 2; ++sc) {
+          const int cr = (h + 2 * sc) * 32 + lane;
+          if (cr < R && best[sc] != 0u)
+            atomicMax(&s_kmax[cr], (static_cast<unsigned long long>(best[sc]) << 32) | (0xFFFFFFFFull - bidx[sc]));
+        }
       }
       ds_named_sync(1, DW_EPI);                        // every epilogue warp has folded its keys
       for (int rr = tid - DW_EPI_WARP0 * 32; rr < R; rr += DW_EPI)
@@ -404,7 +459,7 @@ __global__ void __launch_bounds__(DW_THREADS, 1) dense_walk_gemm_kernel(const Dw
 // ---- sampled positions without a nucleus: draws over the z rows ------------------------------
 constexpr int DD_THREADS = 256;
 constexpr int DD_WARPS = DD_THREADS / 32;
-constexpr int DD_CELL = 256;                 // indices per cell: one warp, eight consecutive a lane
+constexpr int DD_CELL = 1024;                // indices per cell: one warp, 32 a lane
 
 struct DwDraw {
   const float* z;
@@ -448,30 +503,37 @@ DS_DEV void dd_emit(const DwDraw& d, int64_t r, int64_t pick, float zmax, double
   }
 }
 
-// Weights of eight z values (zero past V)
-DS_DEV void dd_w8(const float* zr, int64_t t, int64_t V, float zmax, float (&w)[8]) {
-  float x[8];
-  if (t + 8 <= V && (reinterpret_cast<uintptr_t>(zr + t) & 15) == 0) {
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(zr + t));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(zr + t) + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else {
+// Four z values from t on (minus infinity past V; a vector load when whole and aligned)
+DS_DEV float4 dd_ld4(const float* zr, int64_t t, int64_t V, bool vec) {
+  if (vec && t + 4 <= V) return __ldcg(reinterpret_cast<const float4*>(zr + t));
+  float4 x;
+  x.x = (t < V) ? __ldcg(zr + t) : -INFINITY;
+  x.y = (t + 1 < V) ? __ldcg(zr + t + 1) : -INFINITY;
+  x.z = (t + 2 < V) ? __ldcg(zr + t + 2) : -INFINITY;
+  x.w = (t + 3 < V) ? __ldcg(zr + t + 3) : -INFINITY;
+  return x;
+}
+
+// Kept mass of cell c (indices c * 1024 ..): lane l weighs the four values at k * 128 + 4 l for
+// k = 0..7 (each load of the warp is 512 contiguous bytes) and the warp adds its float pairs.
+DS_DEV rs::FF dd_cell_mass(const float* zr, int64_t c, int64_t V, float zmax, bool vec, int lane) {
+  float4 x[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = (t + e < V) ? __ldcg(zr + t + e) : -INFINITY;
-  }
+  for (int k = 0; k < 8; ++k) x[k] = dd_ld4(zr, c * DD_CELL + k * 128 + lane * 4, V, vec);
+  rs::FF2 acc{0ull, 0ull};
 #pragma unroll
-  for (int e = 0; e < 8; e += 2) {
-    const float2 w2 = ds_weight2(__fsub_rn(x[e], zmax), __fsub_rn(x[e + 1], zmax));
-    w[e] = w2.x;
-    w[e + 1] = w2.y;
+  for (int k = 0; k < 8; ++k) {
+    const float2 w01 = ds_weight2(__fsub_rn(x[k].x, zmax), __fsub_rn(x[k].y, zmax));
+    const float2 w23 = ds_weight2(__fsub_rn(x[k].z, zmax), __fsub_rn(x[k].w, zmax));
+    rs::ff2_add(acc, ds_f2(w01.x, w01.y));
+    rs::ff2_add(acc, ds_f2(w23.x, w23.y));
   }
+  return rs::warp_ff_reduce(rs::ff2_fold(acc));
 }
 
 __global__ void __launch_bounds__(DD_THREADS, 3) dense_walk_draw_kernel(const DwDraw d) {
-  __shared__ double s_run[DD_THREADS + 1];
+  __shared__ rs::PickShared<DD_THREADS> s_pk;
   __shared__ int s_last;
-  __shared__ int64_t s_cell, s_pick;
-  __shared__ double s_tau;
   ds_pdl_trigger();
   ds_pdl_wait();                                       // z and the maximum keys come from the GEMM
   const int64_t r = blockIdx.y;
@@ -489,26 +551,10 @@ __global__ void __launch_bounds__(DD_THREADS, 3) dense_walk_draw_kernel(const Dw
   const float* zr = d.z + (r * d.z_row_mul + d.z_row_add) * d.ldz;
   float2* cells = d.cells + r * d.ncell;
   const int64_t cbeg = int64_t(blockIdx.x) * d.part_cells, cend = min(d.ncell, cbeg + d.part_cells);
-  for (int64_t k0 = cbeg + warp; k0 < cend; k0 += 4 * DD_WARPS) {  // four cells per warp in flight
-    float w[4][8];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t t = (k0 + u * DD_WARPS) * DD_CELL + lane * 8;
-      if (k0 + u * DD_WARPS < cend && t < d.V) dd_w8(zr, t, d.V, zmax, w[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t c = k0 + u * DD_WARPS;
-      if (c >= cend) continue;                         // warp-uniform
-      const int64_t t = c * DD_CELL + lane * 8;
-      rs::FF m{0.0f, 0.0f};
-      if (t < d.V) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) rs::ff_add(m, w[u][e]);
-      }
-      const rs::FF cw = rs::warp_ff_reduce(m);
-      if (lane == 0) cells[c] = make_float2(cw.hi, cw.lo);
-    }
+  const bool vec = (reinterpret_cast<uintptr_t>(zr) & 15) == 0;
+  for (int64_t c = cbeg + warp; c < cend; c += DD_WARPS) {
+    const rs::FF cw = dd_cell_mass(zr, c, d.V, zmax, vec, lane);
+    if (lane == 0) cells[c] = make_float2(cw.hi, cw.lo);
   }
   __threadfence();
   __syncthreads();
@@ -516,113 +562,32 @@ __global__ void __launch_bounds__(DD_THREADS, 3) dense_walk_draw_kernel(const Dw
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // the last part: the first kept index whose running sum exceeds u * W_kept
-  const int64_t ncell = d.ncell;
-  const int64_t per = (ncell + DD_THREADS - 1) / DD_THREADS;
-  const int64_t c0 = min(ncell, tid * per), c1 = min(ncell, c0 + per);
-  rs::FF mf{0.0f, 0.0f};
-  for (int64_t c = c0; c < c1; ++c) {
-    const float2 cv = __ldcg(cells + c);
-    rs::ff_acc(mf, rs::FF{cv.x, cv.y});
-  }
-  const double mine = rs::ff_value(mf);
-  s_run[tid] = mine;
-  __syncthreads();
-  if (tid < 32) {
-    constexpr int PT = DD_THREADS / 32;
-    double loc = 0.0;
+  // the last part: the first kept index whose running sum exceeds u * W_kept (float pairs)
+  if (tid == 0) d.ticket[r] = 0;                       // ready for the next position
+  rs::pick_cell<DD_THREADS>(cells, d.ncell, rs::ff_uniform(d.seed[r], d.step[r], uint32_t(d.j), DS_PURPOSE_DRAFT), s_pk);
+  const int64_t cell = s_pk.cell == ~0ull ? -1 : int64_t(s_pk.cell);
+  if (warp == 0) {
+    int64_t pick = -1;
+    if (cell >= 0) {
+      // the cell in index order: lane l holds indices t .. t + 31, t = cell * 1024 + 32 l
+      const int64_t t = cell * DD_CELL + lane * 32;
+      rs::FF w[32];
 #pragma unroll
-    for (int q = 0; q < PT; ++q) loc += s_run[lane * PT + q];
-    double incl = loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += nb;
-    }
-    double run = incl - loc;
-#pragma unroll
-    for (int q = 0; q < PT; ++q) {
-      const double x = s_run[lane * PT + q];
-      s_run[lane * PT + q] = run;
-      run += x;
-    }
-    if (lane == 31) s_run[DD_THREADS] = incl;
-  }
-  __syncthreads();
-  const double before = s_run[tid], total = s_run[DD_THREADS];
-  const double u = ds_uniform(d.seed[r], d.step[r], uint32_t(d.j), DS_PURPOSE_DRAFT);
-  const double target = u * total;
-  if (tid == 0) {
-    s_cell = -1;
-    s_pick = -1;
-    d.ticket[r] = 0;                                   // ready for the next position
-  }
-  __syncthreads();
-  if (mine > 0.0 && target >= before && target < before + mine) {
-    double acc = before;
-    for (int64_t c = c0; c < c1; ++c) {
-      const float2 cv2 = __ldcg(cells + c);
-      const double cv = double(cv2.x) + double(cv2.y);
-      if (cv > 0.0 && target < acc + cv) {
-        s_cell = c;
-        s_tau = target - acc;
-        break;
+      for (int k = 0; k < 8; ++k) {
+        const float4 x = dd_ld4(zr, t + 4 * k, d.V, vec);
+        const float2 w01 = ds_weight2(__fsub_rn(x.x, zmax), __fsub_rn(x.y, zmax));
+        const float2 w23 = ds_weight2(__fsub_rn(x.z, zmax), __fsub_rn(x.w, zmax));
+        w[4 * k] = rs::FF{w01.x, 0.0f};
+        w[4 * k + 1] = rs::FF{w01.y, 0.0f};
+        w[4 * k + 2] = rs::FF{w23.x, 0.0f};
+        w[4 * k + 3] = rs::FF{w23.y, 0.0f};
       }
-      acc += cv;
+      pick = rs::warp_pick<32>(w, s_pk.tau, s_pk.tinf != 0, cell * DD_CELL);
     }
+    if (lane == 0) dd_emit(d, r, pick, zmax, rs::ff_value(s_pk.total), 0.0f, -1);
   }
-  __syncthreads();
-  if (tid == 0 && s_cell < 0) {                        // rounding: the last cell with mass
-    for (int64_t c = ncell - 1; c >= 0; --c) {
-      const float2 cv2 = __ldcg(cells + c);
-      if (double(cv2.x) + double(cv2.y) > 0.0) {
-        s_cell = c;
-        s_tau = INFINITY;
-        break;
-      }
-    }
-  }
-  __syncthreads();
-  const int64_t cell = s_cell;
-  if (cell >= 0 && warp == 0) {
-    const int64_t t = cell * DD_CELL + lane * 8;
-    const double tau = s_tau;
-    float w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = 0.0f;
-    if (t < d.V) dd_w8(zr, t, d.V, zmax, w);
-    rs::FF lm{0.0f, 0.0f};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) rs::ff_add(lm, w[e]);
-    const double ls = rs::ff_value(lm);
-    double incl = ls;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += nb;
-    }
-    const double ex = incl - ls;
-    const unsigned withm = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
-    const int lastl = withm ? 31 - __clz(int(withm)) : -1;
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, ls > 0.0 && tau >= ex && tau < incl);
-    const int hl = hit ? __ffs(hit) - 1 : lastl;
-    if (lane == hl) {
-      double run = ex;
-      int64_t pick = -1, last = -1;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (pick < 0 && w[e] > 0.0f) {
-          run += double(w[e]);
-          last = t + e;
-          if (run > tau) pick = t + e;
-        }
-      }
-      s_pick = pick >= 0 ? pick : last;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) dd_emit(d, r, s_pick, zmax, total, 0.0f, -1);
 }
+
 
 // Greedy positions: the argmax key is the token (lowest index among equal maxima).
 __global__ void dense_walk_greedy_kernel(const DwDraw d, int32_t R) {

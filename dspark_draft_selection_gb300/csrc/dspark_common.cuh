@@ -108,13 +108,18 @@ DS_DEV DsU4 ds_philox4x32_10(DsU4 c, uint32_t k0, uint32_t k1) {
 
 enum : uint32_t { DS_PURPOSE_DRAFT = 0, DS_PURPOSE_ACCEPT = 1, DS_PURPOSE_RESIDUAL = 2 };
 
+// The 53-bit integer m of the uniform u = m * 2^-53 for (seed, step, position, purpose, draw):
+// m = (x0 >> 5) * 2^26 + (x1 >> 6) from the first two Philox outputs.
+DS_DEV uint64_t ds_uniform_bits(uint64_t seed, uint64_t step, uint32_t position, uint32_t purpose,
+                                uint32_t draw = 0) {
+  const DsU4 c{uint32_t(step), position, (purpose << 20) + draw, uint32_t(step >> 32)};
+  const DsU4 o = ds_philox4x32_10(c, uint32_t(seed), uint32_t(seed >> 32));
+  return (uint64_t(o.x >> 5) << 26) | uint64_t(o.y >> 6);
+}
 // Double uniform in [0, 1) for (seed, step, position, purpose, draw).
 DS_DEV double ds_uniform(uint64_t seed, uint64_t step, uint32_t position, uint32_t purpose,
                          uint32_t draw = 0) {
-  const DsU4 c{uint32_t(step), position, (purpose << 20) + draw, uint32_t(step >> 32)};
-  const DsU4 o = ds_philox4x32_10(c, uint32_t(seed), uint32_t(seed >> 32));
-  const double a = double(o.x >> 5), b = double(o.y >> 6);
-  return (a * 67108864.0 + b) * (1.0 / 9007199254740992.0);
+  return double(ds_uniform_bits(seed, step, position, purpose, draw)) * (1.0 / 9007199254740992.0);
 }
 
 // ----------------------------------------------------------------------------------------

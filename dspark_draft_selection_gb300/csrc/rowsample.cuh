@@ -2,10 +2,11 @@
 // dense Markov walk and verification reuse.
 //
 // Sums of weights: each thread adds the weights of its elements with the error-free 2Sum
-// transformation in float32 pairs (about 48 significant bits), then converts to double; every
-// larger sum is in double. A double accumulation per element would run on the GPU's narrow
-// FP64 pipe; the float pairs keep the running sums within ~1e-14 of the exact value, far below
-// the spacing of any decision.
+// transformation in float32 pairs (about 48 significant bits). A double operation costs about as
+// much as 64 float32 ones on this part (its FP64 pipe is narrow), so per-element and running sums
+// stay in float pairs; the row sampler converts block totals to double, the draws of the dense walk
+// and of verification keep float pairs to the decision (pick_cell, warp_pick). The float pairs keep
+// the running sums within ~1e-14 of the exact value, far below the spacing of any decision.
 #pragma once
 
 #include "dspark_common.cuh"
@@ -69,6 +70,160 @@ DS_DEV FF warp_ff_reduce(FF v) {
     v.lo = __fadd_rn(v.lo, lo);
   }
   return v;
+}
+
+// ---- float-pair decisions ---------------------------------------------------------------------
+// A double operation costs about as much as 64 float32 ones on this part, so the running sums and
+// comparisons that pick a token are float pairs; a comparison is right unless the two values agree
+// to about 2^-48 relative, where a double sum in another order could fall either way as well.
+
+// a - b as one float, whose sign is the sign of the difference (2Sum on the leading terms)
+DS_DEV float ff_diff(const FF& a, const FF& b) {
+  const float s = __fsub_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(-b.hi, bb));
+  return __fadd_rn(s, __fadd_rn(err, __fsub_rn(a.lo, b.lo)));
+}
+DS_DEV FF ff_neg(const FF& a) { return FF{-a.hi, -a.lo}; }
+// a * b as a float pair (the leading product's error from an FMA)
+DS_DEV FF ff_mul(const FF& a, const FF& b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  const float e = __fmaf_rn(a.hi, b.hi, -p);
+  const float t = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, e));
+  const float s = __fadd_rn(p, t);
+  return FF{s, __fsub_rn(t, __fsub_rn(s, p))};
+}
+// The uniform m * 2^-53 of ds_uniform as a float pair: the top 24 bits of m exactly, the other 29
+// rounded to 24 (within 2^-49 of the double).
+DS_DEV FF ff_uniform(uint64_t seed, uint64_t step, uint32_t position, uint32_t purpose, uint32_t draw = 0) {
+  const uint64_t m = ds_uniform_bits(seed, step, position, purpose, draw);
+  return FF{__fmul_rn(__uint2float_rn(uint32_t(m >> 29)), 0x1p-24f),
+            __fmul_rn(__uint2float_rn(uint32_t(m & 0x1FFFFFFFull)), 0x1p-53f)};
+}
+
+// Shared state of pick_cell.
+template <int NTHREADS>
+struct PickShared {
+  FF wsum[NTHREADS / 32];
+  FF total, tau;
+  unsigned long long cell;   // the crossing cell (~0 when none)
+  int tinf;                  // rounding fallback: the last cell with mass, every running sum below tau
+};
+
+// Whole block: the cell whose running sum first exceeds target = u * total over `ncell` float-pair
+// cell masses (each thread a contiguous run of cells), and tau = target minus the mass before it.
+// Without such a cell (rounding), the last cell with mass and tinf.
+template <int NTHREADS>
+DS_DEV void pick_cell(const float2* cells, int64_t ncell, const FF& u, PickShared<NTHREADS>& s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t per = (ncell + NTHREADS - 1) / NTHREADS;
+  const int64_t c0 = min(ncell, tid * per), c1 = min(ncell, c0 + per);
+  FF mf{0.0f, 0.0f};
+  for (int64_t c = c0; c < c1; ++c) {
+    const float2 cv = __ldcg(cells + c);
+    ff_acc(mf, FF{cv.x, cv.y});
+  }
+  FF incl = mf;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const FF nb{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
+    if (lane >= o) ff_acc(incl, nb);
+  }
+  FF before{__shfl_up_sync(0xFFFFFFFFu, incl.hi, 1), __shfl_up_sync(0xFFFFFFFFu, incl.lo, 1)};
+  if (lane == 0) before = FF{0.0f, 0.0f};
+  if (lane == 31) s.wsum[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    FF run{0.0f, 0.0f};
+#pragma unroll
+    for (int w = 0; w < NTHREADS / 32; ++w) {
+      const FF x = s.wsum[w];
+      s.wsum[w] = run;
+      ff_acc(run, x);
+    }
+    s.total = run;
+    s.cell = ~0ull;
+    s.tinf = 0;
+  }
+  __syncthreads();
+  ff_acc(before, s.wsum[warp]);
+  const FF target = ff_mul(u, s.total);
+  FF end = before;
+  ff_acc(end, mf);
+  if (mf.hi > 0.0f && ff_diff(target, before) >= 0.0f && ff_diff(target, end) < 0.0f) {
+    FF acc = before;
+    for (int64_t c = c0; c < c1; ++c) {
+      const float2 cv = __ldcg(cells + c);
+      FF nxt = acc;
+      ff_acc(nxt, FF{cv.x, cv.y});
+      if (cv.x > 0.0f && ff_diff(target, nxt) < 0.0f) {
+        atomicMin(&s.cell, static_cast<unsigned long long>(c));
+        break;
+      }
+      acc = nxt;
+    }
+  }
+  __syncthreads();
+  if (s.cell != ~0ull && int64_t(s.cell) >= c0 && int64_t(s.cell) < c1) {   // the owner: tau
+    FF acc = before;
+    for (int64_t c = c0; c < int64_t(s.cell); ++c) {
+      const float2 cv = __ldcg(cells + c);
+      ff_acc(acc, FF{cv.x, cv.y});
+    }
+    FF tau = target;
+    ff_acc(tau, ff_neg(acc));
+    s.tau = tau;
+  }
+  if (tid == 0 && s.cell == ~0ull) {                   // rounding: the last cell with mass
+    for (int64_t c = ncell - 1; c >= 0; --c) {
+      if (__ldcg(cells + c).x > 0.0f) {
+        s.cell = static_cast<unsigned long long>(c);
+        s.tinf = 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// One warp: lane l holds the N masses v[e] of indices base + N l + e (in index order). The first
+// index whose running sum exceeds tau; with tinf, or when no running sum does, the last index with
+// mass; -1 when there is none. Every lane gets the result.
+template <int N>
+DS_DEV int64_t warp_pick(const FF (&v)[N], const FF& tau, bool tinf, int64_t base) {
+  static_assert(N <= 32, "one bit per mass");
+  const int lane = threadIdx.x & 31;
+  FF ls{0.0f, 0.0f};
+#pragma unroll
+  for (int e = 0; e < N; ++e) ff_acc(ls, v[e]);
+  FF li = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const FF nb{__shfl_up_sync(0xFFFFFFFFu, li.hi, o), __shfl_up_sync(0xFFFFFFFFu, li.lo, o)};
+    if (lane >= o) ff_acc(li, nb);
+  }
+  FF lx{__shfl_up_sync(0xFFFFFFFFu, li.hi, 1), __shfl_up_sync(0xFFFFFFFFu, li.lo, 1)};
+  if (lane == 0) lx = FF{0.0f, 0.0f};
+  const bool has = ls.hi > 0.0f;
+  const unsigned withm = __ballot_sync(0xFFFFFFFFu, has);
+  const int lastl = withm ? 31 - __clz(int(withm)) : -1;
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, !tinf && has && ff_diff(tau, lx) >= 0.0f && ff_diff(tau, li) < 0.0f);
+  const int hl = hit ? __ffs(int(hit)) - 1 : lastl;
+  int64_t pick = -1;
+  if (lane == hl) {
+    FF run = lx;
+    uint32_t gt = 0u, nz = 0u;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      ff_acc(run, v[e]);
+      gt |= uint32_t(!tinf && ff_diff(run, tau) > 0.0f) << e;
+      nz |= uint32_t(v[e].hi > 0.0f) << e;
+    }
+    gt &= nz;
+    const int64_t b = base + int64_t(N) * lane;
+    pick = gt ? b + (__ffs(int(gt)) - 1) : (nz ? b + (31 - __clz(int(nz))) : -1);
+  }
+  return hl >= 0 ? __shfl_sync(0xFFFFFFFFu, pick, hl) : -1;
 }
 
 // 1 when a V-element row is within the sampler's row length, else -1 (the row-length check the

@@ -33,7 +33,6 @@
 namespace {
 
 constexpr int VM_THREADS = 512;            // residual-mass CTAs
-constexpr int VM_WARPS = VM_THREADS / 32;
 constexpr int VM_CELL = 256;               // ids per cell: one warp, eight consecutive ids a lane
 constexpr int VM_PART = 32768;             // ids per draw CTA (128 cells) for dense records
 constexpr int VM_PART_SPARSE = 8192;       // ... for sparse records (staged in shared memory by id)
@@ -96,17 +95,23 @@ DS_DEV float vf_wq(const VerifyArgs& a, int64_t qrow, int64_t i) {
   return vf_keep(w, i, a.q.wcut[qrow], a.q.icut[qrow]) ? w : 0.0f;
 }
 
-// q_j(x) from the record (double); ids outside the record have probability zero
-DS_DEV double vf_q(const VerifyArgs& a, int64_t qrow, int64_t x) {
-  if (x < 0) return 0.0;
+// A double as a float pair (its leading 48 bits)
+DS_DEV rs::FF vf_ff(double x) {
+  const float hi = float(x);
+  return rs::FF{hi, float(x - double(hi))};
+}
+
+// q_j(x) = num / den from the record: a sparse record's probability over 1, a dense record's kept
+// weight over the row's kept mass; ids outside the record have num = 0
+DS_DEV float vf_qnum(const VerifyArgs& a, int64_t qrow, int64_t x) {
+  if (x < 0) return 0.0f;
   if (a.q_form == QF_SPARSE) {
     const int n = a.q.n[qrow];
     for (int k = 0; k < n && k < a.q.cap; ++k)
-      if (a.q.ids[qrow * a.q.cap + k] == x) return double(a.q.p[qrow * a.q.cap + k]);
-    return 0.0;
+      if (a.q.ids[qrow * a.q.cap + k] == x) return a.q.p[qrow * a.q.cap + k];
+    return 0.0f;
   }
-  const float w = vf_wq(a, qrow, vf_qindex(a, x));
-  return w > 0.0f ? double(w) / a.q.wsum[qrow] : 0.0;
+  return vf_wq(a, qrow, vf_qindex(a, x));
 }
 
 __global__ void verify_t2d_kernel(const int64_t* d2t, int64_t V_d, int64_t V_t, int32_t* t2d, int32_t* status) {
@@ -158,12 +163,16 @@ DS_DEV void vf_accept_warp(const VerifyArgs& a, int64_t r, bool write, int* kind
       if (greedy) {
         ev = x != a.ws.amax[rid];
       } else {
-        const double qx = vf_q(a, r * B + j, x);
-        zq = !(qx > 0.0);
+        const float qn = vf_qnum(a, r * B + j, x);
+        zq = !(qn > 0.0f);
         if (!zq) {
-          const double px = double(a.ws.probe_w[rid]) / a.ws.wsum[rid];
-          const double ua = ds_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
-          ev = !(ua < px / qx);
+          // u < p(x) / q(x) with p = w_p / W_p and q = qn / W_q (W_q = 1 for a sparse record),
+          // cross-multiplied: u qn W_p < w_p W_q, in float pairs
+          const rs::FF ua = rs::ff_uniform(vseed, step, uint32_t(j), DS_PURPOSE_ACCEPT);
+          const rs::FF lhs = rs::ff_mul(rs::ff_mul(ua, rs::FF{qn, 0.0f}), vf_ff(a.ws.wsum[rid]));
+          const rs::FF wp{a.ws.probe_w[rid], 0.0f};
+          const rs::FF rhs = a.q_form == QF_SPARSE ? wp : rs::ff_mul(wp, vf_ff(a.q.wsum[r * B + j]));
+          ev = !(rs::ff_diff(lhs, rhs) < 0.0f);
         }
         ev = ev || zq;
       }
@@ -194,7 +203,7 @@ DS_DEV void vf_accept_warp(const VerifyArgs& a, int64_t r, bool write, int* kind
       if (k < acc) {
         const int64_t rid = rbase + k;
         a.out_tokens[obase + k] = a.draft_tgt[r * B + k];
-        a.logprob[obase + k] = float(log(double(a.ws.probe_w[rid])) - log(a.ws.wsum[rid]));
+        a.logprob[obase + k] = __fsub_rn(logf(a.ws.probe_w[rid]), logf(float(a.ws.wsum[rid])));
       } else if (k > acc) {
         a.out_tokens[obase + k] = -1;
         a.logprob[obase + k] = 0.0f;
@@ -203,7 +212,7 @@ DS_DEV void vf_accept_warp(const VerifyArgs& a, int64_t r, bool write, int* kind
         // (the argmax has weight 1)
         const int64_t rid = rbase + acc;
         a.out_tokens[obase + acc] = a.ws.amax[rid];
-        a.logprob[obase + acc] = float(-log(a.ws.wsum[rid]));
+        a.logprob[obase + acc] = -logf(float(a.ws.wsum[rid]));
       }
     }
     if (lane == 0) a.n_accepted[r] = acc;
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
   constexpr int EPV = 16 / sizeof(T);
   constexpr int BATCH = 8;
   __shared__ float s_f[VS_WARPS];
-  __shared__ double s_d[VS_WARPS];
+  __shared__ rs::FF s_d[VS_WARPS];
   __shared__ uint32_t s_u[VS_WARPS];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -331,17 +340,18 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
     f = rs::warp_ff_reduce(f);
     amin = __reduce_min_sync(0xFFFFFFFFu, amin);
     if (lane == 0) {
-      s_d[warp] = rs::ff_value(f);
+      s_d[warp] = f;
       s_u[warp] = amin;
     }
     __syncthreads();
     if (tid == 0) {
-      double W = 0.0;
+      rs::FF Wf{0.0f, 0.0f};
       uint32_t am = 0xFFFFFFFFu;
       for (int k = 0; k < VS_WARPS; ++k) {
-        W += s_d[k];
+        rs::ff_acc(Wf, s_d[k]);
         am = min(am, s_u[k]);
       }
+      const double W = rs::ff_value(Wf);
       if (!finite) ds_set_error(a.status, DSPARK_ENONFINITE);
       a.ws.zmax[rid] = zmax;
       a.ws.wsum[rid] = W;
@@ -542,10 +552,8 @@ __global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const Verify
   constexpr int CPP = PART / VM_CELL;                      // cells per part
   constexpr int WARPS = VM_THREADS / 32;
   __shared__ float s_q[QF == QF_SPARSE ? VM_PART_SPARSE : 1];
-  __shared__ double s_run[VM_THREADS + 1];
+  __shared__ rs::PickShared<VM_THREADS> s_pk;
   __shared__ int s_last;
-  __shared__ int64_t s_cell, s_pick;
-  __shared__ double s_tau;
   ds_pdl_trigger();
   ds_pdl_wait();
   const int64_t r = blockIdx.y;
@@ -588,49 +596,14 @@ __global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const Verify
   if (!s_last) return;
   __threadfence();
 
-  // this thread's contiguous run of cells: its mass, the mass before it, the row's total
-  const int64_t ncell = a.ncell;
-  const int64_t per = (ncell + VM_THREADS - 1) / VM_THREADS;
-  const int64_t c0 = min(ncell, tid * per), c1 = min(ncell, c0 + per);
-  double mine = 0.0, before = 0.0, total = 0.0;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    rs::FF mf{0.0f, 0.0f};
-    for (int64_t c = c0; c < c1; ++c) {
-      const float2 cv = __ldcg(cells + c);
-      rs::ff_acc(mf, rs::FF{cv.x, cv.y});
-    }
-    mine = rs::ff_value(mf);
-    s_run[tid] = mine;                                     // exclusive prefix over threads (warp 0)
-    __syncthreads();
-    if (tid < 32) {
-      constexpr int PT = VM_THREADS / 32;
-      double loc = 0.0;
-#pragma unroll
-      for (int q = 0; q < PT; ++q) loc += s_run[lane * PT + q];
-      double incl = loc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += nb;
-      }
-      double run = incl - loc;
-#pragma unroll
-      for (int q = 0; q < PT; ++q) {
-        const double x = s_run[lane * PT + q];
-        s_run[lane * PT + q] = run;
-        run += x;
-      }
-      if (lane == 31) s_run[VM_THREADS] = incl;
-    }
-    __syncthreads();
-    before = s_run[tid];
-    total = s_run[VM_THREADS];
-    __syncthreads();
-    if (total > 0.0 || attempt == 1) break;
+  // the crossing cell: the first whose running sum exceeds u * total (float pairs)
+  const rs::FF u = rs::ff_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
+  rs::pick_cell<VM_THREADS>(cells, a.ncell, u, s_pk);
+  if (!(s_pk.total.hi > 0.0f)) {
     // the residual has no mass (possible only through rounding): draw from p, whose cells this CTA
     // recomputes over the whole row (rare)
     g.use_q = false;
-    for (int64_t c = warp; c < ncell; c += WARPS) {
+    for (int64_t c = warp; c < a.ncell; c += WARPS) {
       const int64_t t = c * VM_CELL + lane * 8;
       rs::FF v[8];
       rs::FF m{0.0f, 0.0f};
@@ -644,93 +617,29 @@ __global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const Verify
     }
     __threadfence_block();
     __syncthreads();
+    rs::pick_cell<VM_THREADS>(cells, a.ncell, u, s_pk);
   }
-
-  // the crossing cell: the first whose running sum exceeds u * total
-  const double u = ds_uniform(a.vseed[r], a.step[r], uint32_t(j), DS_PURPOSE_RESIDUAL);
-  const double target = u * total;
-  if (tid == 0) {
-    s_cell = -1;
-    s_pick = -1;
-  }
-  __syncthreads();
-  if (mine > 0.0 && target >= before && target < before + mine) {
-    double acc = before;
-    for (int64_t c = c0; c < c1; ++c) {
-      const float2 cv2 = __ldcg(cells + c);
-      const double cv = double(cv2.x) + double(cv2.y);
-      if (cv > 0.0 && target < acc + cv) {
-        s_cell = c;
-        s_tau = target - acc;
-        break;
-      }
-      acc += cv;
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && s_cell < 0) {                            // rounding: the last cell with mass
-    for (int64_t c = ncell - 1; c >= 0; --c) {
-      const float2 cv2 = __ldcg(cells + c);
-      if (double(cv2.x) + double(cv2.y) > 0.0) {
-        s_cell = c;
-        s_tau = INFINITY;
-        break;
-      }
-    }
-  }
-  __syncthreads();
-  const int64_t cell = s_cell;
+  const int64_t cell = s_pk.cell == ~0ull ? -1 : int64_t(s_pk.cell);
+  int64_t pick = -1;
   if (cell >= 0) {
     if (QF == QF_SPARSE && g.use_q) vf_stage_sparse(a, g.qrow, cell * VM_CELL, VM_CELL, s_q);
     if (warp == 0) {
       const int64_t t = cell * VM_CELL + lane * 8;
-      const double tau = s_tau;
       rs::FF v[8];
-      double rv[8], ls = 0.0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = rs::FF{0.0f, 0.0f};
       if (t < a.V) vf_rho8<T, QF, TONE>(a, g, t, s_q, cell * VM_CELL, v);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        rv[e] = rs::ff_value(v[e]);
-        ls += rv[e];
-      }
-      double incl = ls;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double nb = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += nb;
-      }
-      const double ex = incl - ls;
-      const unsigned withm = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
-      const int lastl = withm ? 31 - __clz(int(withm)) : -1;
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, ls > 0.0 && tau >= ex && tau < incl);
-      const int hl = hit ? __ffs(hit) - 1 : lastl;
-      if (lane == hl) {
-        double run = ex;
-        int64_t pick = -1, last = -1;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (pick < 0 && rv[e] > 0.0) {
-            run += rv[e];
-            last = t + e;
-            if (run > tau) pick = t + e;
-          }
-        }
-        s_pick = pick >= 0 ? pick : last;
-      }
+      pick = rs::warp_pick<8>(v, s_pk.tau, s_pk.tinf != 0, cell * VM_CELL);
     }
   }
-  __syncthreads();
   if (tid == 0) {
-    const int64_t pick = s_pick;
     float w = 0.0f;
     if (pick >= 0) {
       const float x = ds_load_elem<T>(g.row + pick);
       w = ds_weight(__fsub_rn(ds_temper_t<TONE>(x, a.T), g.zmax));
     }
     a.out_tokens[r * (a.B + 1) + j] = int32_t(pick);
-    a.logprob[r * (a.B + 1) + j] = float(log(double(w)) - log(g.Wp));
+    a.logprob[r * (a.B + 1) + j] = __fsub_rn(logf(w), logf(g.wp_hi));
   }
 }
 
