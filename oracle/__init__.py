@@ -21,7 +21,10 @@ Modules and what pins them (the tests under ``tests/test_oracle_*.py``):
   walk      dense Markov walk (pinned by the zero-table and K = V reductions);
   verify    rejection-sampling verification (pinned by chi-square fits of the emitted token
             to p, the closed-form acceptance rate sum min(p, q), the pages' worked example,
-            and greedy acceptance equal to argmax matching).
+            and greedy acceptance equal to argmax matching);
+  conv      DFlash-2 grouped dynamic convolution over packed block rows (pinned by one tap
+            equal to a per-group scaling, one block with fixed taps equal to numpy's causal
+            convolution of every channel, block isolation under perturbation, linearity).
 No function here is "parity unpinned".
 """
-from . import draft, fp32, philox, sampling, verify, walk  # noqa: F401
+from . import conv, draft, fp32, philox, sampling, verify, walk  # noqa: F401
