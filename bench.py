@@ -11,10 +11,11 @@ spread beside it.
 
 The other workloads of the hot path are timed by the same run the same way (`secondary`): the
 tiny lattice (latency), the pruned sampled DSpark draft, full-row top-p drafting on its rows, the
-gated DFlash v2 head, and the dense Markov walk with rejection-sampling verification.
+gated DFlash v2 head, the dense Markov walk with rejection-sampling verification, and the DFlash-2
+grouped dynamic convolution over packed block rows.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--repeats M] [--impl ours|reference]
-                    [--workloads c1,c2,c3,c3s,c4,c5] [--no-cpu-baseline]
+                    [--workloads c1,c2,c3,c3s,c4,c5,conv] [--no-cpu-baseline]
 
 Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak scaling, no
 collective on the data path); timing is the max over ranks after a barrier.
@@ -48,7 +49,7 @@ L2_BYTES = 129 * 2**20
 METRIC = "drafted blocks/s and logit HBM GB/s (fraction of ~8 TB/s peak), 1×GB300"
 UNIT = "blocks/s"
 PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_row_kernel_qwen3_4b_R32_B7_V151936.md")
-ALL_WORKLOADS = ("c2", "c1", "c3", "c3s", "c4", "c5")
+ALL_WORKLOADS = ("c2", "c1", "c3", "c3s", "c4", "c5", "conv")
 
 
 def peaks():
@@ -569,7 +570,29 @@ def bench_c5(ds, dev, stream, timer, hbm, args):
                         "kernels_ms": ker}}
 
 
-SECONDARY = {"c1": bench_c1, "c3": bench_c3, "c3s": bench_c3s, "c4": bench_c4, "c5": bench_c5}
+def bench_conv(ds, dev, stream, timer, hbm, args):
+    """DFlash-2 grouped dynamic convolution on C4-shaped packed rows: 128 requests x (1 context +
+    7 block rows) x 5,120 channels, 32 groups, 4 taps; six input/output sets (189 MB, larger
+    than L2) rotate between calls."""
+    import torch
+    w = di.conv_workload()
+    nsets = 6
+    x0 = to_device(w["x"], dev)
+    xs = [x0] + [torch.roll(x0, s, 1) for s in range(1, nsets)]
+    k, block = to_device(w["k"], dev), to_device(w["block"], dev)
+    ys = [torch.empty((w["N"], w["C"]), dtype=torch.float32, device=dev) for _ in range(nsets)]
+
+    def conv(s):
+        ds.dspark_grouped_conv(xs[s], k, block, out=ys[s], stream=stream)
+
+    ms, spread = timer.per_call([conv], nsets, 4, args.repeats)
+    nb = w["N"] * w["C"] * (2 + 4) + k.numel() * 4 + block.numel() * 4
+    return {w["name"]: {"ms_per_call": round(ms, 5), "ms_per_call_spread": spread,
+                        "gbs": round(nb / (ms / 1e3) / 1e9, 1), "frac": round(nb / (ms / 1e3) / 1e9 / hbm, 4),
+                        "bytes": nb, "kernels_ms": {"grouped_conv": round(ms, 5)}}}
+
+
+SECONDARY = {"c1": bench_c1, "c3": bench_c3, "c3s": bench_c3s, "c4": bench_c4, "c5": bench_c5, "conv": bench_conv}
 
 
 # ------------------------------------------------------------------------------------------------

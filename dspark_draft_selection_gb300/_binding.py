@@ -36,6 +36,7 @@ SIGNATURES = [
     ("dspark_lattice_chain", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
                                      c_i32, c_i32, c_i64, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_test_set_first_wait_polls", None, [ctypes.c_uint32]),
+    ("dspark_grouped_conv", c_i32, [c_vp, c_i32, c_i64, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp]),
     ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_vp, c_vp, c_vp,
                                     c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_sample", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_i64, c_f32, c_f32, c_f32, c_f32,
@@ -247,6 +248,19 @@ def dspark_lattice_chain(cand_val, cand_tgt, prev, E, W, mode="maxsum", *, hidde
                                       _p(out[0]), _p(out[1]), _p(out[2]), _p(status), _stream(stream)),
            "dspark_lattice_chain")
     return out + (status,)
+
+
+def dspark_grouped_conv(x, k, block, *, out=None, stream=None):
+    """DFlash-2 grouped dynamic convolution over packed block rows: x [N, C] (bf16/f32),
+    k [N, G, L] float32 taps, block [N] int32 -> y [N, C] float32."""
+    N, ldx = _rows(x)
+    C = x.shape[1]
+    G, L = k.shape[1], k.shape[2]
+    y = out if out is not None else torch.empty((N, C), dtype=torch.float32, device=x.device)
+    _, ldy = _rows(y)
+    _check(lib().dspark_grouped_conv(_p(x), _dt(x), N, C, ldx, G, L, _p(k), _p(block), _p(y), ldy, _stream(stream)),
+           "dspark_grouped_conv")
+    return y
 
 
 def dspark_test_set_first_wait_polls(polls: int) -> None:

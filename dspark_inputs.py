@@ -188,4 +188,18 @@ def config5(R: int = 64, V: int = 151936) -> dict:
     return w
 
 
+def conv_workload(cid: int = 6, R: int = 128, B: int = 7, C: int = 5120, G: int = 32, L: int = 4,
+                  ctx: int = 1, dtype: str = "bf16") -> dict:
+    """Packed block rows for the DFlash-2 grouped dynamic convolution: R requests, each `ctx`
+    context rows then B block rows (block ids 2r for the context rows, 2r + 1 for the block),
+    x ~ N(0, 1) [N, C], dynamic taps k ~ N(0, 0.5^2) [N, G, L] float32 (synthetic weights)."""
+    N = R * (ctx + B)
+    block = np.repeat(np.arange(R, dtype=np.int32) * 2, ctx + B)
+    block += np.tile(np.r_[np.zeros(ctx, np.int32), np.ones(B, np.int32)], R)
+    x = normal(generator(cid, S_HIDDEN), (N, C), 1.0, dtype)
+    k = normal(generator(cid, S_G), (N, G * L), 0.5, "f32").reshape(N, G, L)
+    return dict(name=f"dflash2_grouped_conv_R{R}_B{B}_C{C}_G{G}_L{L}", x=x, x_dtype=dtype, k=k, block=block,
+                R=R, B=B, C=C, G=G, L=L, N=N)
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

@@ -306,6 +306,24 @@ dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t 
                             dspark_stream_t stream);
 
 /*
+ * DFlash-2 grouped dynamic convolution over packed block rows.
+ * optimum-intel PR #2098 ("Export DFlash v2 and DSpark drafts for PagedAttention and continuous
+ * batching"), What does this PR do > DFlash v2: the draft's grouped dynamic convolution shifts its
+ * taps along the packed block rows and masks them to the block of the row they produce.
+ *   y[i, c] = sum over t < L of k[i, g(c), t] * x[i - t, c], counting a tap only when row i - t
+ *             exists and block[i - t] == block[i]; g(c) = c / (C / G).
+ * x: [N, C] rows of dtype (row stride ldx >= C), device; k: [N, G, L] float32 taps per produced
+ * row and channel group, contiguous, device; block: [N] int32 block of every row, device;
+ * y: [N, C] float32 out (row stride ldy >= C), device, caller-owned. Sums are float32 FMAs in tap
+ * order. Errors (returned before any launch): DSPARK_EINVAL for a bad dtype or shape, C % G != 0,
+ * L outside [1, 16] or a null or misaligned pointer. Nothing is detected on the device, so it
+ * takes no status word. Asynchronous on stream.
+ */
+dspark_status dspark_grouped_conv(const void* x, dspark_dtype dtype, int64_t N, int64_t C, int64_t ldx,
+                                  int32_t G, int32_t L, const float* k, const int32_t* block, float* y,
+                                  int64_t ldy, dspark_stream_t stream);
+
+/*
  * Failure-detection test hook (not part of the method): sets the poll limit of the first wait
  * for a tile's tensor-core MMAs in dspark_lattice_score, dspark_lattice_chain and
  * dspark_dense_walk, process-wide, for later calls (0xFFFFFFFF restores the default, about 6.7e7

@@ -65,4 +65,8 @@ def test_status_strings_and_host_checks(libpath):
     assert lib.dspark_chain_select(fake, fake, fake, 1, 7, 65, 0, 0.0, 1.0, None, None, fake, fake, fake, None,
                                    fake, None) == 1
     assert lib.dspark_d2t_check(fake, 10, 10, 1, None, 0, fake, None) == 8      # injectivity needs a workspace
+    # grouped convolution: channels not a multiple of the groups, too many taps, no-op on zero rows
+    assert lib.dspark_grouped_conv(fake, 0, 4, 10, 10, 3, 4, fake, fake, fake, 10, None) == 1
+    assert lib.dspark_grouped_conv(fake, 0, 4, 12, 12, 3, 17, fake, fake, fake, 12, None) == 1
+    assert lib.dspark_grouped_conv(None, 0, 0, 12, 12, 3, 4, None, None, None, 12, None) == 0
     assert ds.dspark_workspace_size(ds.OP_D2T_CHECK, 1, 1, 64, 0) >= 8
