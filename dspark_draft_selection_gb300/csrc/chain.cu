@@ -30,6 +30,8 @@ struct ChainArgs {
   const int32_t* cand_tgt;
   int32_t B, K, mode;
   float T, top_p;
+  const float* T_r;                   // [R] per-request temperature (<= 0: greedy), or null
+  const float* top_p_r;               // [R] per-request top-p, or null
   const uint64_t* seed;
   const uint64_t* step;
   int32_t* chain_rank;
@@ -119,7 +121,14 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
   }
 
   const bool maxsum = a.mode == DSPARK_MAXSUM;
-  const bool sample = (a.mode == DSPARK_SAMPLE) && (a.T > 0.0f);
+  // this request's sampling parameters: a mixed batch gives them per request
+  float Tq = a.T_r ? a.T_r[r] : a.T, tpq = a.top_p_r ? a.top_p_r[r] : a.top_p;
+  if (a.mode == DSPARK_SAMPLE && !(Tq == Tq && tpq > 0.0f)) {   // out of contract: greedy, reported
+    if (t == 0) ds_set_error(a.status, DSPARK_EINVAL);
+    Tq = 0.0f;
+    tpq = 1.0f;
+  }
+  const bool sample = (a.mode == DSPARK_SAMPLE) && (Tq > 0.0f);
   const uint64_t seed = sample ? a.seed[r] : 0, step = sample ? a.step[r] : 0;
   const int warp = t >> 5, lane = t & 31;
   int prevb = 0;
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         float zmax = -INFINITY, z[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          z[h] = (lane + 32 * h < K) ? ds_temper(v[h], a.T) : -INFINITY;
+          z[h] = (lane + 32 * h < K) ? ds_temper(v[h], Tq) : -INFINITY;
           zmax = fmaxf(zmax, z[h]);
         }
         zmax = ds_warp_max(zmax);
@@ -221,7 +230,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         const double wall = ds_warp_sum(double(w[0]) + double(w[1]));
         // kept[h]: nucleus membership of candidate lane + 32h
         bool kept[2] = {w[0] > 0.0f, w[1] > 0.0f};
-        if (a.top_p < 1.0f) {
+        if (tpq < 1.0f) {
           // (weight desc, rank asc) order by a warp bitonic sort of the 64 keys (position i = lane
           // + 32h holds one key), then the running mass in that order and the cut
           const uint64_t key0 = (lane < K) ? ds_key64(w[0], uint32_t(lane)) : 0ull;
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           const double inc0 = ch_warp_scan(pw[0]);
           const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
           const double inc1 = tot0 + ch_warp_scan(pw[1]);
-          const double tp = double(a.top_p) * wall;
+          const double tp = double(tpq) * wall;
           const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && inc0 > tp && pw[0] > 0.0);
           const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && inc1 > tp && pw[1] > 0.0);
           if (b0 | b1) {
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 extern "C" dspark_status dspark_chain_select(const float* cand_val, const float* trans,
                                              const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
                                              dspark_chain_mode mode, float temperature, float top_p,
+                                             const float* temperature_r, const float* top_p_r,
                                              const uint64_t* seed, const uint64_t* step,
                                              int32_t* chain_rank, int32_t* chain_tgt, float* score,
                                              const dspark_qrecord* q, int32_t* dev_status,
@@ -377,6 +387,8 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   a.mode = int(mode);
   a.T = temperature;
   a.top_p = top_p;
+  a.T_r = mode == DSPARK_SAMPLE ? temperature_r : nullptr;
+  a.top_p_r = mode == DSPARK_SAMPLE ? top_p_r : nullptr;
   a.seed = seed;
   a.step = step;
   a.chain_rank = chain_rank;
@@ -385,7 +397,7 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   a.status = dev_status;
   if (mode == DSPARK_SAMPLE) {
     DS_REQUIRE(temperature == temperature && top_p > 0.0f && top_p == top_p);
-    if (temperature > 0.0f) DS_REQUIRE(seed && step);
+    if (temperature > 0.0f || temperature_r) DS_REQUIRE(seed && step);
     if (q) {
       DS_REQUIRE(q->ids && q->p && q->n && q->cap >= K);
       a.q_ids = q->ids;

@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
   cg::cluster_group cl = cg::this_cluster();
   const int P = int(cl.num_blocks()), part = int(cl.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool greedy = !(a.T > 0.0f);
-  const float Tz = greedy ? 1.0f : a.T;
+  bool greedy = !(a.T > 0.0f);
+  float Tz = greedy ? 1.0f : a.T, top_p = a.top_p;
   auto zof = [&](float raw) { return ds_temper(sp_xform<XFORM>(raw, a.mult, a.softcap), Tz); };
 
   for (int64_t row_id = blockIdx.x / P; row_id < rows; row_id += gridDim.x / P) {
@@ -199,6 +199,23 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
     if (a.n_draft) {                                      // every part of the row skips it
       const int32_t nd = a.n_draft[r];                    // rows past n, and every row of a request
       if (nd < 0 || nd > a.B - 1 || j > nd) continue;     // whose n is out of range, are not needed
+    }
+    if (a.T_r) {                                          // a mixed batch: this request's values
+      const float Tq = a.T_r[r];
+      greedy = !(Tq > 0.0f);
+      Tz = greedy ? 1.0f : Tq;
+    }
+    if (a.top_p_r) top_p = a.top_p_r[r];
+    if (!(Tz == Tz) || !(top_p > 0.0f)) {                 // out of contract: greedy, reported
+      if (tid == 0 && part == 0) ds_set_error(a.status, DSPARK_EINVAL);
+      greedy = true;
+      Tz = 1.0f;
+      top_p = 1.0f;
+    }
+    if (a.no_draw && greedy) {                            // verification statistics of a greedy
+      greedy = false;                                     // request: its temperature-1 row, no
+      Tz = 1.0f;                                          // nucleus (the argmax comes from the
+      top_p = 1.0f;                                       // kept-mass pass)
     }
     const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
     SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
@@ -275,7 +292,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       // is fixed. Once that digit holds at most SP_CAP weights they are sorted by (weight desc,
       // index asc) and cut by a block scan. Only more than SP_CAP equal weights at the cut (a
       // flat row) fall back to a bisection over (weight, index) keys ----
-      if (NUC && a.top_p < 1.0f) {
+      if (NUC && top_p < 1.0f) {
         float2* s_accm = reinterpret_cast<float2*>(s_nuc);                    // [16][SR_THREADS]
         uint32_t* s_accc = reinterpret_cast<uint32_t*>(s_accm + 16 * SR_THREADS);
         uint32_t prefix = 0, pmask = 0, dcount = 0;
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
           if (first) {                                 // the first pass sees every positive weight
             double W = 0.0;
             for (int d = 0; d < 16; ++d) W += s_digm[d];
-            target = double(a.top_p) * W;
+            target = double(top_p) * W;
             first = false;
           }
           // the digit where the running mass from the top first exceeds the target (rounding can
@@ -782,7 +799,7 @@ cudaError_t sp_launch_v(const rs::SampleArgs& a, int64_t rows, cudaStream_t stre
 
 template <typename T, bool XFORM>
 cudaError_t sp_launch(const rs::SampleArgs& a, int64_t rows, cudaStream_t stream) {
-  const bool nuc = a.T > 0.0f && a.top_p < 1.0f;
+  const bool nuc = (a.T > 0.0f && a.top_p < 1.0f) || a.T_r != nullptr || a.top_p_r != nullptr;
   const bool spq = a.q_mode == 1;
   if (nuc) return spq ? sp_launch_v<T, XFORM, true, true>(a, rows, stream) : sp_launch_v<T, XFORM, true, false>(a, rows, stream);
   return spq ? sp_launch_v<T, XFORM, false, true>(a, rows, stream) : sp_launch_v<T, XFORM, false, false>(a, rows, stream);
@@ -801,6 +818,7 @@ extern "C" size_t dspark_internal_ws_sample(int64_t, int32_t, int64_t) { return 
 extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_d,
                                        int64_t ld, const int64_t* row_start, const int64_t* d2t, int64_t V_t,
                                        float mult, float softcap, float temperature, float top_p,
+                                       const float* temperature_r, const float* top_p_r,
                                        const uint64_t* seed, const uint64_t* step, int32_t* out_tgt,
                                        int32_t* out_idx, const dspark_qrecord* q, void* ws, size_t ws_bytes,
                                        int32_t* dev_status, dspark_stream_t stream) {
@@ -811,9 +829,11 @@ extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, i
   DS_REQUIRE(logits && out_tgt && dev_status && ds_aligned(logits, ds_dtype_size(dtype)));
   DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f);
   DS_REQUIRE(mult == mult && softcap == softcap && softcap >= 0.0f);
-  if (temperature > 0.0f) DS_REQUIRE(seed && step);
+  if (temperature > 0.0f || temperature_r) DS_REQUIRE(seed && step);
   if (d2t) DS_REQUIRE(V_t >= 1);
   rs::SampleArgs a = {};
+  a.T_r = temperature_r;
+  a.top_p_r = top_p_r;
   a.rows = logits;
   a.V = V_d;
   a.ld = ld;

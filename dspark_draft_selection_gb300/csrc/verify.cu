@@ -67,6 +67,8 @@ struct VerifyArgs {
   int q_form;
   int64_t V_q;
   float T, top_p;
+  const float* T_r;          // [R] per-request temperature (<= 0: greedy), or null
+  const float* top_p_r;      // [R] per-request top-p, or null
   const uint64_t* vseed;
   const uint64_t* step;
   int32_t* out_tokens;
@@ -76,6 +78,13 @@ struct VerifyArgs {
   int64_t ncell;
   VerifyWs ws;
 };
+
+// Request r's temperature: a mixed batch gives it per request (a NaN one counts as greedy; the
+// host or the statistics pass reports it)
+DS_DEV float vf_T(const VerifyArgs& a, int64_t r) {
+  const float T = a.T_r ? a.T_r[r] : a.T;
+  return T == T ? T : 0.0f;
+}
 
 DS_DEV bool vf_keep(float w, int64_t i, float wcut, int64_t icut) {
   return w > 0.0f && (w > wcut || (w == wcut && i <= icut));
@@ -150,7 +159,7 @@ DS_DEV void vf_accept_warp(const VerifyArgs& a, int64_t r, bool write, int* kind
     *kind = JOB_NONE;
     return;
   }
-  const bool greedy = !(a.T > 0.0f);
+  const bool greedy = !(vf_T(a, r) > 0.0f);
   const uint64_t vseed = greedy ? 0 : a.vseed[r], step = greedy ? 0 : a.step[r];
   int first = n;                                           // first position that is not accepted
   bool first_zero_q = false;
@@ -257,13 +266,14 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
   __shared__ uint32_t s_u[VS_WARPS];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool greedy = !(a.T > 0.0f);
-  const float Tz = greedy ? 1.0f : a.T;
   ds_pdl_trigger();
   ds_pdl_wait();                                   // drafted tokens and counts may come from before
   for (int64_t rid = blockIdx.x; rid < rows; rid += gridDim.x) {
     const int64_t r = rid / (a.B + 1);
     const int j = int(rid - r * (a.B + 1));
+    const float Tq = vf_T(a, r);
+    const bool greedy = !(Tq > 0.0f);
+    const float Tz = greedy ? 1.0f : Tq;
     const int32_t n = a.n_draft[r];
     if (n < 0 || n > a.B) {                        // out of contract: the first row's CTA reports it
       if (j == 0 && warp == 0) {
@@ -401,6 +411,7 @@ struct VfJob {
   float wp_hi, wp_lo, wq_hi, wq_lo;
   int64_t qrow;
   bool use_q;
+  float Tq;                  // the request's temperature
 };
 
 template <typename T>
@@ -415,6 +426,7 @@ DS_DEV VfJob<T> vf_job(const VerifyArgs& a, int64_t r, int j, bool use_q) {
   g.Wp = a.ws.wsum[rid];
   g.qrow = r * a.B + j;
   g.use_q = use_q;
+  g.Tq = vf_T(a, r);
   g.wp_hi = float(g.Wp);
   g.wp_lo = float(g.Wp - double(g.wp_hi));
   const double Wq = (use_q && a.q_form >= QF_DENSE) ? a.q.wsum[g.qrow] : 1.0;
@@ -519,8 +531,8 @@ DS_DEV void vf_rho8(const VerifyArgs& a, const VfJob<T>& g, int64_t t, const flo
   }
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
-    const float2 w2 = ds_weight2(__fsub_rn(ds_temper_t<TONE>(x[e], a.T), g.zmax),
-                                 __fsub_rn(ds_temper_t<TONE>(x[e + 1], a.T), g.zmax));
+    const float2 w2 = ds_weight2(__fsub_rn(ds_temper_t<TONE>(x[e], g.Tq), g.zmax),
+                                 __fsub_rn(ds_temper_t<TONE>(x[e + 1], g.Tq), g.zmax));
     float wp0 = w2.x, wp1 = w2.y;
     if (!(t + e < a.V) || !vf_keep(wp0, t + e, g.wcut, g.icut)) wp0 = 0.0f;
     if (!(t + e + 1 < a.V) || !vf_keep(wp1, t + e + 1, g.wcut, g.icut)) wp1 = 0.0f;
@@ -636,7 +648,7 @@ __global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const Verify
     float w = 0.0f;
     if (pick >= 0) {
       const float x = ds_load_elem<T>(g.row + pick);
-      w = ds_weight(__fsub_rn(ds_temper_t<TONE>(x, a.T), g.zmax));
+      w = ds_weight(__fsub_rn(ds_temper_t<TONE>(x, g.Tq), g.zmax));
     }
     a.out_tokens[r * (a.B + 1) + j] = int32_t(pick);
     a.logprob[r * (a.B + 1) + j] = __fsub_rn(logf(w), logf(g.wp_hi));
@@ -690,7 +702,7 @@ cudaError_t vf_launch_draws_form(const VerifyArgs& a, int64_t R, cudaStream_t st
 
 template <typename T>
 cudaError_t vf_launch_draws_any(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
-  return a.T == 1.0f ? vf_launch_draws_form<T, true>(a, R, stream) : vf_launch_draws_form<T, false>(a, R, stream);
+  return (a.T == 1.0f && !a.T_r) ? vf_launch_draws_form<T, true>(a, R, stream) : vf_launch_draws_form<T, false>(a, R, stream);
 }
 
 }  // namespace
@@ -704,7 +716,8 @@ extern "C" size_t dspark_internal_ws_verify(int64_t R, int32_t B, int64_t V) {
 extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_t,
                                        int64_t ld, const int64_t* row_start, const int32_t* draft_tgt,
                                        const int32_t* n_draft, const dspark_qrecord* q, int64_t V_q,
-                                       const int64_t* q_d2t, float temperature, float top_p, const uint64_t* vseed,
+                                       const int64_t* q_d2t, float temperature, float top_p,
+                                       const float* temperature_r, const float* top_p_r, const uint64_t* vseed,
                                        const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted, float* logprob,
                                        void* ws, size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
   DS_REQUIRE(ds_dtype_ok(dtype) && R >= 0 && B >= 1 && B <= 100 && V_t >= 1 && ld >= V_t);
@@ -712,7 +725,7 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   DS_REQUIRE(tgt_logits && draft_tgt && n_draft && out_tokens && n_accepted && logprob && dev_status);
   DS_REQUIRE(ds_aligned(tgt_logits, ds_dtype_size(dtype)));
   DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f);
-  const bool greedy = !(temperature > 0.0f);
+  const bool greedy = !(temperature > 0.0f) && !temperature_r;   // every request greedy
   int q_form = QF_NONE;
   if (!greedy) {
     DS_REQUIRE(vseed && step && q);
@@ -743,6 +756,8 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   a.V_q = V_q;
   a.T = temperature;
   a.top_p = top_p;
+  a.T_r = temperature_r;
+  a.top_p_r = top_p_r;
   a.vseed = vseed;
   a.step = step;
   a.out_tokens = out_tokens;
@@ -762,7 +777,7 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
 
   DS_CUDA_TRY(cudaMemsetAsync(a.ws.tk_stats, 0, size_t(R) * 2 * sizeof(int32_t), stream));
   // 1. statistics of every needed target row, and the acceptance tests
-  const bool lean = greedy || !(top_p < 1.0f);
+  const bool lean = greedy || (!(top_p < 1.0f) && !top_p_r);
   if (lean) {
     const int64_t grid = std::min<int64_t>(R * (B + 1), int64_t(ds_num_sms()) * VS_PER_SM);
     if (dtype == DSPARK_BF16)
@@ -784,6 +799,8 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.softcap = 0.0f;
   sa.T = greedy ? 1.0f : temperature;
   sa.top_p = greedy ? 1.0f : top_p;
+  sa.T_r = temperature_r;
+  sa.top_p_r = top_p_r;
   sa.position = -1;
   sa.out_mul = 1;
   sa.status = dev_status;
@@ -797,7 +814,7 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.probe_tgt = draft_tgt;
   sa.n_draft = n_draft;
   sa.probe_w = a.ws.probe_w;
-  sa.amax_out = greedy ? a.ws.amax : nullptr;
+  sa.amax_out = (greedy || temperature_r) ? a.ws.amax : nullptr;
   DS_CUDA_TRY(rs::sample_rows(sa, R * (B + 1), dtype == DSPARK_BF16, 0, stream));
   DS_CUDA_TRY(ds_launch(verify_accept_kernel, dim3(unsigned((R * 32 + 127) / 128)), dim3(128), 0, stream, a, R));
   }
