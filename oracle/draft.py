@@ -159,9 +159,9 @@ def chain_walk(u, A):
     return np.array(chain, dtype=np.int64), score
 
 
-def chain_sample(u, A, cand_tgt, T, top_p, seed, step):
+def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0):
     """Sampled walk [G]: at each position, sample the float32 lattice row after the token
-    before over the K' candidates at temperature T and top-p, with the request's draft
+    before over the K' candidates at temperature T, top-p and min-p, with the request's draft
     stream (purpose 0, position j). The candidate rank is the row index (ties in the
     nucleus order go to the lower rank). Returns (ranks, score, records) where each
     record holds the sparse q over kept ranks with their target ids."""
@@ -170,7 +170,7 @@ def chain_sample(u, A, cand_tgt, T, top_p, seed, step):
     for j in range(B):
         v = walk_rows(u, A, prev, j)
         uu = float(uniform(seed, step, j, PURPOSE_DRAFT))
-        b, rec = sample_row(v, T, top_p, uu)
+        b, rec = sample_row(v, T, top_p, uu, min_p)
         rec["ids"] = np.asarray(cand_tgt[j])[rec["kept"]]
         rec["u"] = uu
         rec["row"] = v

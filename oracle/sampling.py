@@ -20,6 +20,11 @@ Readings where the pages are silent (each listed in the design notes):
   * tokens of zero weight are never kept; with top_p >= 1, or when the mass never
     exceeds top_p, every token of positive weight is kept;
   * T <= 0 means greedy: the argmax, lowest index on ties, with q a point mass.
+  * min-p (commit on the thresholded filters: MinPFilter collects the tokens whose probability
+    is at least min_p times the top token's): applied after top-p, so the kept set is the
+    nucleus intersected with {p_i >= min_p * p_max}; the common normaliser cancels, so the test
+    is w_i >= min_p * w_max on the float32 weights (w_max = 1). The kept set stays a prefix of the
+    (weight desc, index asc) order; with min_p > 0 its record cut is that prefix's last token.
 """
 from __future__ import annotations
 
@@ -63,6 +68,33 @@ def nucleus_kept(w, top_p):
     return kept, w[order[k]], int(order[k])
 
 
+def min_p_kept(w, kept, min_p):
+    """The kept tokens whose probability is at least min_p times the top token's:
+    p_i >= min_p * p_max, i.e. w_i >= min_p * w_max (the normaliser cancels)."""
+    w = np.asarray(w, dtype=F32)
+    kept = np.asarray(kept)
+    thr = F64(F32(min_p)) * F64(w.max())
+    return kept[w[kept].astype(F64) >= thr]
+
+
+def kept_cut(w, kept):
+    """The cut (w_cut, i_cut) of a kept set that is a prefix of the (weight desc, index asc) order:
+    its last token, i.e. the smallest kept weight and the largest kept index with that weight."""
+    w = np.asarray(w, dtype=F32)
+    kept = np.asarray(kept)
+    wc = w[kept].min()
+    return wc, int(kept[w[kept] == wc].max())
+
+
+def filtered_kept(w, top_p, min_p=0.0):
+    """Top-p, then min-p: the kept indices (ascending) and their cut."""
+    kept, w_cut, i_cut = nucleus_kept(w, top_p)
+    if min_p > 0:
+        kept = min_p_kept(w, kept, min_p)
+        w_cut, i_cut = kept_cut(w, kept)
+    return kept, w_cut, i_cut
+
+
 def draw_from_weights(w, kept, u):
     """First kept index (ascending) whose running double sum exceeds u * W_kept."""
     kept = np.asarray(kept)
@@ -73,8 +105,8 @@ def draw_from_weights(w, kept, u):
     return kept[pos], c[-1]
 
 
-def sample_row(s, T, top_p, u):
-    """One draw from row s at temperature T and top-p, with the record of q.
+def sample_row(s, T, top_p, u, min_p=0.0):
+    """One draw from row s at temperature T, top-p and min-p, with the record of q.
 
     Returns (token, record) where record holds: z (float32 row), zmax, kept ids
     (ascending), q of each kept id (float32), W_kept (double), and the nucleus cut."""
@@ -85,7 +117,7 @@ def sample_row(s, T, top_p, u):
                    wsum=1.0, w_cut=F32(0.0), i_cut=-1)
         return tok, rec
     z, zmax, w = softmax_weights(s, T)
-    kept, w_cut, i_cut = nucleus_kept(w, top_p)
+    kept, w_cut, i_cut = filtered_kept(w, top_p, min_p)
     tok, wsum = draw_from_weights(w, kept, u)
     q = (w[kept].astype(F64) / wsum).astype(F32)
     rec = dict(kind="sampled", z=z, zmax=zmax, w=w, kept=kept, q=q, wsum=wsum, w_cut=w_cut, i_cut=i_cut)

@@ -27,15 +27,15 @@ import numpy as np
 
 from .fp32 import F32, F64
 from .philox import PURPOSE_ACCEPT, PURPOSE_RESIDUAL, uniform
-from .sampling import draw_from_weights, nucleus_kept, running_sum, softmax_weights
+from .sampling import draw_from_weights, filtered_kept, running_sum, softmax_weights
 
 EPROPOSAL = 4
 
 
 class TargetDist:
-    """The target's post-filter distribution of one row at (T, top_p)."""
+    """The target's post-filter distribution of one row at (T, top_p, min_p)."""
 
-    def __init__(self, row, T, top_p):
+    def __init__(self, row, T, top_p, min_p=0.0):
         row = np.asarray(row, dtype=F32)
         self.V = row.shape[0]
         self.greedy = T <= 0
@@ -43,7 +43,7 @@ class TargetDist:
         tp = 1.0 if self.greedy else top_p
         self.z, self.zmax, self.w = softmax_weights(row, Tw)
         self.argmax = int(np.argmax(row))
-        self.kept, self.w_cut, self.i_cut = nucleus_kept(self.w, tp)
+        self.kept, self.w_cut, self.i_cut = filtered_kept(self.w, tp, 0.0 if self.greedy else min_p)
         self.wsum = running_sum(self.w[self.kept])[-1]
         mask = np.zeros(self.V, dtype=bool)
         mask[self.kept] = True
@@ -86,7 +86,7 @@ def verify_step(p_full, q_full, x, u_accept, u_residual):
     return acc, np.where(acc, x, res)
 
 
-def verify_request(target_rows, drafted, n, q_rows, T, top_p, vseed, step, V_t=None):
+def verify_request(target_rows, drafted, n, q_rows, T, top_p, vseed, step, V_t=None, min_p=0.0):
     """Verify n drafted target tokens of one request.
 
     target_rows: [B+1, V_t] target logits; drafted: [B] target ids; q_rows(j) returns the
@@ -95,7 +95,7 @@ def verify_request(target_rows, drafted, n, q_rows, T, top_p, vseed, step, V_t=N
     logprobs, margins)."""
     out_tokens, logps, margins = [], [], []
     for j in range(n):
-        dist = TargetDist(target_rows[j], T, top_p)
+        dist = TargetDist(target_rows[j], T, top_p, min_p)
         x = int(drafted[j])
         if dist.greedy:
             if x == dist.argmax:
@@ -125,7 +125,7 @@ def verify_request(target_rows, drafted, n, q_rows, T, top_p, vseed, step, V_t=N
         out_tokens.append(t)
         logps.append(dist.logp(t))
         return dict(status=0, n_accepted=j, tokens=out_tokens, logprobs=logps, margins=margins)
-    dist = TargetDist(target_rows[n], T, top_p)
+    dist = TargetDist(target_rows[n], T, top_p, min_p)
     if dist.greedy:
         t = dist.argmax
     else:

@@ -313,3 +313,17 @@ def test_chain_sample_reads_the_row_after_the_token_before():
             assert chain[j] == (chain[j - 1] + 3) % K
             assert list(recs[j]["ids"]) == [ids[j, chain[j]]]
         assert abs(score - od.chain_score(u, A, chain)) < 1e-4
+
+
+def test_chain_sample_min_p_one_is_the_greedy_walk():
+    """min_p = 1 keeps only the top candidate of every lattice row, so the sampled walk is the
+    greedy walk, with q a point mass on its token."""
+    rng = np.random.default_rng(31)
+    B, K = 7, 16
+    u = rng.standard_normal((B, K)).astype(np.float32)
+    A = (rng.standard_normal((B, K, K)) * 0.5).astype(np.float32)
+    tgt = rng.integers(0, 1000, size=(B, K))
+    chain, _, recs = od.chain_sample(u, A, tgt, 0.8, 1.0, 12345, 9, min_p=1.0)
+    walk, _ = od.chain_walk(u, A)
+    assert np.array_equal(chain, walk)
+    assert all(len(r["kept"]) == 1 and r["q"][0] == 1.0 for r in recs)

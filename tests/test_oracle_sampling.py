@@ -149,3 +149,57 @@ def test_dense_q_matches_draw_frequencies():
     assert counts[dq == 0].sum() == 0
     ok, stat = chi2_ok(counts, dq)
     assert ok, stat
+
+
+# ---- min-p (pinned by hand-computed kept sets, the intersection with top-p, the record's cut and
+# the draws' frequencies) ------------------------------------------------------------------------
+
+def _halving_row():
+    # weights 1, 1/2, 1/4, 1/8 (to the polynomial's accuracy) and one flushed token
+    return np.array([0.0, -np.log(2.0), -2 * np.log(2.0), -3 * np.log(2.0), -80.0], dtype=np.float32)
+
+
+@pytest.mark.parametrize("min_p,want", [(0.0, [0, 1, 2, 3]), (0.3, [0, 1]), (0.2, [0, 1, 2]), (0.5001, [0]),
+                                        (1.0, [0]), (0.124, [0, 1, 2, 3])])
+def test_min_p_keeps_tokens_at_least_min_p_times_the_top(min_p, want):
+    from oracle.sampling import filtered_kept, softmax_weights
+    _, _, w = softmax_weights(_halving_row(), 1.0)
+    kept, w_cut, i_cut = filtered_kept(w, 1.0, min_p)
+    assert list(kept) == want
+
+
+def test_min_p_after_top_p_is_the_intersection():
+    from oracle.sampling import filtered_kept, softmax_weights
+    _, _, w = softmax_weights(_halving_row(), 1.0)
+    # p = (8, 4, 2, 1) / 15: the running mass 8/15, 12/15, 14/15 first exceeds 0.85 at the third token
+    assert list(filtered_kept(w, 0.85, 0.0)[0]) == [0, 1, 2]
+    assert list(filtered_kept(w, 0.85, 0.3)[0]) == [0, 1]          # min-p cuts inside the nucleus
+    assert list(filtered_kept(w, 0.85, 0.1)[0]) == [0, 1, 2]       # the nucleus cuts first
+    assert list(filtered_kept(w, 0.5, 0.3)[0]) == [0]              # 8/15 > 0.5 already
+
+
+def test_min_p_record_cut_describes_the_kept_set():
+    from oracle.sampling import dense_q, sample_row
+    rng = np.random.default_rng(17)
+    for trial in range(40):
+        s = np.round(rng.standard_normal(300) * 2, 1).astype(np.float32)   # many equal weights
+        T, top_p, min_p = [(1.0, 1.0, 0.05), (0.7, 0.9, 0.2), (1.3, 0.95, 0.01)][trial % 3]
+        tok, rec = sample_row(s, T, top_p, 0.37, min_p)
+        q = dense_q(rec["z"], rec["zmax"], rec["wsum"], rec["w_cut"], rec["i_cut"], np.arange(300))
+        kept = np.nonzero(q > 0)[0]
+        assert np.array_equal(kept, rec["kept"])
+        assert np.all(rec["w"][kept].astype(np.float64) >= np.float64(np.float32(min_p)))
+        np.testing.assert_allclose(q[kept], rec["q"].astype(np.float64), rtol=1e-6)
+
+
+def test_min_p_draws_follow_the_renormalised_kept_mass():
+    from scipy import stats
+    from oracle.sampling import sample_row
+    s = _halving_row()
+    n = 4000
+    u = (np.arange(n) + 0.5) / n                                  # an exact quadrature of the uniform
+    toks = np.array([sample_row(s, 1.0, 1.0, float(x), 0.2)[0] for x in u])
+    counts = np.bincount(toks, minlength=5)
+    assert counts[3] == 0 and counts[4] == 0
+    exp = np.array([4, 2, 1]) / 7 * n
+    assert stats.chisquare(counts[:3], exp).pvalue > 0.99

@@ -99,3 +99,19 @@ def test_zero_proposal_and_out_of_width_ids():
     for s in range(20):
         res = ov.verify_request(rows, [11, 1], 2, lambda j: qw, 1.0, 1.0, s, 0)
         assert res["n_accepted"] == 0 and res["tokens"][0] < 10
+
+
+def test_min_p_one_makes_verification_argmax_matching():
+    """With min_p = 1 the target's post-filter p is a point mass on its argmax: a drafted token
+    (with q > 0) is accepted exactly when it is the argmax, and a rejection emits the argmax."""
+    from oracle import verify as ov
+    rng = np.random.default_rng(5)
+    V, B = 50, 6
+    rows = rng.standard_normal((B + 1, V)).astype(np.float32) * 2
+    amax = rows.argmax(axis=1)
+    drafted = np.where(rng.random(B) < 0.5, amax[:B], (amax[:B] + 1) % V)
+    q = np.full(V, 1.0 / V)
+    res = ov.verify_request(rows, drafted, B, lambda j: q, 0.9, 1.0, 77, 3, min_p=1.0)
+    first_bad = next((j for j in range(B) if drafted[j] != amax[j]), B)
+    assert res["n_accepted"] == first_bad
+    assert list(res["tokens"]) == list(amax[:first_bad + 1]) if first_bad < B else list(res["tokens"][:B]) == list(amax[:B])
