@@ -24,7 +24,8 @@ Readings where the pages are silent (each listed in the design notes):
     is at least min_p times the top token's): applied after top-p, so the kept set is the
     nucleus intersected with {p_i >= min_p * p_max}; the common normaliser cancels, so the test
     is w_i >= min_p * w_max on the float32 weights (w_max = 1). The kept set stays a prefix of the
-    (weight desc, index asc) order; with min_p > 0 its record cut is that prefix's last token.
+    (weight desc, index asc) order; when min-p cuts inside the nucleus, the record's cut is
+    (min_p, the largest int32) (the pages leave the record's form open).
 """
 from __future__ import annotations
 
@@ -77,21 +78,18 @@ def min_p_kept(w, kept, min_p):
     return kept[w[kept].astype(F64) >= thr]
 
 
-def kept_cut(w, kept):
-    """The cut (w_cut, i_cut) of a kept set that is a prefix of the (weight desc, index asc) order:
-    its last token, i.e. the smallest kept weight and the largest kept index with that weight."""
-    w = np.asarray(w, dtype=F32)
-    kept = np.asarray(kept)
-    wc = w[kept].min()
-    return wc, int(kept[w[kept] == wc].max())
+MAX_INDEX = 2**31 - 1
 
 
 def filtered_kept(w, top_p, min_p=0.0):
-    """Top-p, then min-p: the kept indices (ascending) and their cut."""
+    """Top-p, then min-p: the kept indices (ascending) and their cut. When min-p cuts inside the
+    nucleus (or there is none), the cut is (min_p, the largest int32), which the cut's rule reads
+    as w_i >= min_p."""
     kept, w_cut, i_cut = nucleus_kept(w, top_p)
     if min_p > 0:
         kept = min_p_kept(w, kept, min_p)
-        w_cut, i_cut = kept_cut(w, kept)
+        if not (F32(w_cut) >= F32(min_p)):
+            w_cut, i_cut = F32(min_p), MAX_INDEX
     return kept, w_cut, i_cut
 
 
