@@ -37,15 +37,15 @@ SIGNATURES = [
                                      c_i32, c_i32, c_i64, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_test_set_first_wait_polls", None, [ctypes.c_uint32]),
     ("dspark_grouped_conv", c_i32, [c_vp, c_i32, c_i64, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp]),
-    ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_vp, c_vp, c_vp,
-                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_f32, c_vp, c_vp,
+                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_sample", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_i64, c_f32, c_f32, c_f32, c_f32,
-                              c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                              c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     ("dspark_dense_walk", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i64,
                                   c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_f32, c_f32, c_f32, c_f32, c_vp, c_vp, c_vp,
                                   c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     ("dspark_verify", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_f32,
-                              c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                              c_f32, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
 ]
 
 
@@ -202,7 +202,7 @@ def _qrec_sparse(ids, p, n):
 
 def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature=0.0, top_p=1.0, seed=None,
                         step=None, record=True, q=None, out=None, status=None, stream=None, temperature_r=None,
-                        top_p_r=None):
+                        top_p_r=None, min_p=0.0, min_p_r=None):
     """temperature_r / top_p_r: optional [R] float32 per-request values (a mixed greedy/sampled
     batch; temperature <= 0 walks greedily) that replace the scalars in the sampled mode."""
     R, B, K = cand_val.shape
@@ -223,8 +223,8 @@ def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature
                                                                                    device=dev),
               torch.zeros((R, B), dtype=torch.int32, device=dev))
         q = _qrec_sparse(*qt)
-    _check(lib().dspark_chain_select(_p(cand_val), _p(trans), _p(cand_tgt), R, B, K, m, temperature, top_p,
-                                     _p(temperature_r), _p(top_p_r), _p(seed),
+    _check(lib().dspark_chain_select(_p(cand_val), _p(trans), _p(cand_tgt), R, B, K, m, temperature, top_p, min_p,
+                                     _p(temperature_r), _p(top_p_r), _p(min_p_r), _p(seed),
                                      _p(step), _p(out[0]), _p(out[1]), _p(out[2]),
                                      ctypes.byref(q) if q is not None else None, _p(status), _stream(stream)),
            "dspark_chain_select")
@@ -295,8 +295,8 @@ def _qrec_any(q):
 
 def dspark_sample(logits, B, *, R=None, V_d=None, row_start=None, d2t=None, V_t=None, mult=1.0, softcap=0.0,
                   temperature=1.0, top_p=1.0, seed=None, step=None, q=None, out=None, ws=None, status=None,
-                  stream=None, temperature_r=None, top_p_r=None):
-    """temperature_r / top_p_r: optional [R] float32 per-request values (a mixed batch)."""
+                  stream=None, temperature_r=None, top_p_r=None, min_p=0.0, min_p_r=None):
+    """temperature_r / top_p_r / min_p_r: optional [R] float32 per-request values (a mixed batch)."""
     rows, ld = _rows(logits)
     V_d = logits.shape[1] if V_d is None else V_d
     R = rows // B if R is None else R
@@ -309,8 +309,8 @@ def dspark_sample(logits, B, *, R=None, V_d=None, row_start=None, d2t=None, V_t=
     wp, wn = _ws(ws)
     qr = _qrec_any(q)
     _check(lib().dspark_sample(_p(logits), _dt(logits), R, B, V_d, ld, _p(row_start), _p(d2t), V_t, mult, softcap,
-                               temperature, top_p, _p(temperature_r), _p(top_p_r), _p(seed), _p(step),
-                               _p(out[0]), _p(out[1]),
+                               temperature, top_p, min_p, _p(temperature_r), _p(top_p_r), _p(min_p_r), _p(seed),
+                               _p(step), _p(out[0]), _p(out[1]),
                                ctypes.byref(qr) if qr is not None else None, wp, wn, _p(status), _stream(stream)),
            "dspark_sample")
     return out + (status,)
@@ -345,8 +345,8 @@ def dspark_dense_walk(logits, B, prev, E, W, *, R=None, V_d=None, row_start=None
 
 def dspark_verify(tgt_logits, B, draft_tgt, n_draft, q, *, V_q=None, q_d2t=None, R=None, row_start=None,
                   temperature=1.0, top_p=1.0, vseed=None, step=None, out=None, ws=None, status=None, stream=None,
-                  temperature_r=None, top_p_r=None):
-    """temperature_r / top_p_r: optional [R] float32 per-request values (a mixed batch)."""
+                  temperature_r=None, top_p_r=None, min_p=0.0, min_p_r=None):
+    """temperature_r / top_p_r / min_p_r: optional [R] float32 per-request values (a mixed batch)."""
     rows, ld = _rows(tgt_logits)
     V_t = tgt_logits.shape[1]
     R = draft_tgt.shape[0] if R is None else R
@@ -362,7 +362,7 @@ def dspark_verify(tgt_logits, B, draft_tgt, n_draft, q, *, V_q=None, q_d2t=None,
         V_q = q[0].shape[1] if (q is not None and len(q) == 5) else V_t
     _check(lib().dspark_verify(_p(tgt_logits), _dt(tgt_logits), R, B, V_t, ld, _p(row_start), _p(draft_tgt),
                                _p(n_draft), ctypes.byref(qr) if qr is not None else None, V_q, _p(q_d2t),
-                               temperature, top_p, _p(temperature_r), _p(top_p_r),
+                               temperature, top_p, min_p, _p(temperature_r), _p(top_p_r), _p(min_p_r),
                                _p(vseed), _p(step), _p(out[0]), _p(out[1]), _p(out[2]), wp, wn, _p(status),
                                _stream(stream)), "dspark_verify")
     return out + (status,)

@@ -29,9 +29,10 @@ struct ChainArgs {
   const float* trans;
   const int32_t* cand_tgt;
   int32_t B, K, mode;
-  float T, top_p;
+  float T, top_p, min_p;
   const float* T_r;                   // [R] per-request temperature (<= 0: greedy), or null
   const float* top_p_r;               // [R] per-request top-p, or null
+  const float* min_p_r;               // [R] per-request min-p, or null
   const uint64_t* seed;
   const uint64_t* step;
   int32_t* chain_rank;
@@ -123,10 +124,12 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
   const bool maxsum = a.mode == DSPARK_MAXSUM;
   // this request's sampling parameters: a mixed batch gives them per request
   float Tq = a.T_r ? a.T_r[r] : a.T, tpq = a.top_p_r ? a.top_p_r[r] : a.top_p;
-  if (a.mode == DSPARK_SAMPLE && !(Tq == Tq && tpq > 0.0f)) {   // out of contract: greedy, reported
-    if (t == 0) ds_set_error(a.status, DSPARK_EINVAL);
-    Tq = 0.0f;
-    tpq = 1.0f;
+  float mpq = a.min_p_r ? a.min_p_r[r] : a.min_p;
+  if (a.mode == DSPARK_SAMPLE && !(Tq == Tq && tpq > 0.0f && mpq >= 0.0f && mpq <= 1.0f)) {   // out of
+    if (t == 0) ds_set_error(a.status, DSPARK_EINVAL);                                        // contract:
+    Tq = 0.0f;                                                                                // greedy,
+    tpq = 1.0f;                                                                               // reported
+    mpq = 0.0f;
   }
   const bool sample = (a.mode == DSPARK_SAMPLE) && (Tq > 0.0f);
   const uint64_t seed = sample ? a.seed[r] : 0, step = sample ? a.step[r] : 0;
@@ -276,6 +279,11 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
             kept[1] = kept[1] && key1 >= cutk;
           }
         }
+        // min-p after top-p: candidates whose weight is at least min_p times the top one's (1)
+        if (mpq > 0.0f) {
+          kept[0] = kept[0] && w[0] >= mpq;
+          kept[1] = kept[1] && w[1] >= mpq;
+        }
         // draw: kept candidates in ascending rank order; running sums by warp scan
         // (lane holds ranks lane and lane + 32: scan the first half, then the second)
         const double k0w = kept[0] ? double(w[0]) : 0.0, k1w = kept[1] ? double(w[1]) : 0.0;
@@ -369,7 +377,8 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
 extern "C" dspark_status dspark_chain_select(const float* cand_val, const float* trans,
                                              const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
                                              dspark_chain_mode mode, float temperature, float top_p,
-                                             const float* temperature_r, const float* top_p_r,
+                                             float min_p, const float* temperature_r, const float* top_p_r,
+                                             const float* min_p_r,
                                              const uint64_t* seed, const uint64_t* step,
                                              int32_t* chain_rank, int32_t* chain_tgt, float* score,
                                              const dspark_qrecord* q, int32_t* dev_status,
@@ -387,8 +396,10 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   a.mode = int(mode);
   a.T = temperature;
   a.top_p = top_p;
+  a.min_p = min_p;
   a.T_r = mode == DSPARK_SAMPLE ? temperature_r : nullptr;
   a.top_p_r = mode == DSPARK_SAMPLE ? top_p_r : nullptr;
+  a.min_p_r = mode == DSPARK_SAMPLE ? min_p_r : nullptr;
   a.seed = seed;
   a.step = step;
   a.chain_rank = chain_rank;
@@ -396,7 +407,7 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   a.score = score;
   a.status = dev_status;
   if (mode == DSPARK_SAMPLE) {
-    DS_REQUIRE(temperature == temperature && top_p > 0.0f && top_p == top_p);
+    DS_REQUIRE(temperature == temperature && top_p > 0.0f && top_p == top_p && min_p >= 0.0f && min_p <= 1.0f);
     if (temperature > 0.0f || temperature_r) DS_REQUIRE(seed && step);
     if (q) {
       DS_REQUIRE(q->ids && q->p && q->n && q->cap >= K);

@@ -330,9 +330,10 @@ struct SampleArgs {
   const int64_t* row_start;
   int64_t row_base, row_mul; // source row = row_base + row_id * row_mul when row_start is NULL
   int32_t B, C;              // C: 1 when the row length was checked by the caller
-  float mult, softcap, T, top_p;
+  float mult, softcap, T, top_p, min_p;
   const float* T_r;          // [requests] per-request temperature (<= 0: greedy), or null
   const float* top_p_r;      // [requests] per-request top-p, or null
+  const float* min_p_r;      // [requests] per-request min-p, or null
   const uint64_t* seed;
   const uint64_t* step;
   int32_t position;          // >= 0: counter position for every row; < 0: j = row_id % B

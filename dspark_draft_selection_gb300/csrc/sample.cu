@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
   const int P = int(cl.num_blocks()), part = int(cl.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   bool greedy = !(a.T > 0.0f);
-  float Tz = greedy ? 1.0f : a.T, top_p = a.top_p;
+  float Tz = greedy ? 1.0f : a.T, top_p = a.top_p, min_p = a.min_p;
   auto zof = [&](float raw) { return ds_temper(sp_xform<XFORM>(raw, a.mult, a.softcap), Tz); };
 
   for (int64_t row_id = blockIdx.x / P; row_id < rows; row_id += gridDim.x / P) {
@@ -206,16 +206,19 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
       Tz = greedy ? 1.0f : Tq;
     }
     if (a.top_p_r) top_p = a.top_p_r[r];
-    if (!(Tz == Tz) || !(top_p > 0.0f)) {                 // out of contract: greedy, reported
-      if (tid == 0 && part == 0) ds_set_error(a.status, DSPARK_EINVAL);
+    if (a.min_p_r) min_p = a.min_p_r[r];
+    if (!(Tz == Tz) || !(top_p > 0.0f) || !(min_p >= 0.0f && min_p <= 1.0f)) {   // out of contract:
+      if (tid == 0 && part == 0) ds_set_error(a.status, DSPARK_EINVAL);          // greedy, reported
       greedy = true;
       Tz = 1.0f;
       top_p = 1.0f;
+      min_p = 0.0f;
     }
     if (a.no_draw && greedy) {                            // verification statistics of a greedy
       greedy = false;                                     // request: its temperature-1 row, no
       Tz = 1.0f;                                          // nucleus (the argmax comes from the
       top_p = 1.0f;                                       // kept-mass pass)
+      min_p = 0.0f;
     }
     const int64_t prow = a.row_start ? a.row_start[r] + j : a.row_base + row_id * a.row_mul;
     SrRow<T> g = sr_row<T>(reinterpret_cast<const T*>(a.rows) + prow * a.ld, a.V);
@@ -436,9 +439,16 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         icut = int64_t(s_cut[1]);
       }
 
+      // ---- min-p after top-p: where it cuts inside the nucleus (or there is none) the cut becomes
+      // (min_p, the largest int32), which the cut's rule reads as w >= min_p ----
+      const bool mp_on = min_p > 0.0f;
+      if (mp_on && !(wcut >= min_p)) {
+        wcut = min_p;
+        icut = 0x7FFFFFFF;
+      }
       // ---- pass: kept mass per cell (float pairs per thread, double per warp), head and tail.
-      // Without a nucleus every positive weight is kept ----
-      auto keep = [&](float w, int64_t i) { return NUC ? sp_keep(w, i, wcut, icut) : (w > 0.0f); };
+      // Without a nucleus or min-p every positive weight is kept ----
+      auto keep = [&](float w, int64_t i) { return (NUC || mp_on) ? sp_keep(w, i, wcut, icut) : (w > 0.0f); };
       rs::FF mh{0.0f, 0.0f}, mt{0.0f, 0.0f};
       const bool want_amax = a.amax_out != nullptr;
       uint32_t amin = 0xFFFFFFFFu;                         // lowest index with z == zmax
@@ -818,7 +828,8 @@ extern "C" size_t dspark_internal_ws_sample(int64_t, int32_t, int64_t) { return 
 extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_d,
                                        int64_t ld, const int64_t* row_start, const int64_t* d2t, int64_t V_t,
                                        float mult, float softcap, float temperature, float top_p,
-                                       const float* temperature_r, const float* top_p_r,
+                                       float min_p, const float* temperature_r, const float* top_p_r,
+                                       const float* min_p_r,
                                        const uint64_t* seed, const uint64_t* step, int32_t* out_tgt,
                                        int32_t* out_idx, const dspark_qrecord* q, void* ws, size_t ws_bytes,
                                        int32_t* dev_status, dspark_stream_t stream) {
@@ -827,13 +838,15 @@ extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, i
   DS_REQUIRE(ds_dtype_ok(dtype));
   DS_REQUIRE(R >= 0 && B >= 1 && V_d >= 1 && ld >= V_d && V_d <= 0x7FFFFFFF && R * B <= 0x7FFFFFFF);
   DS_REQUIRE(logits && out_tgt && dev_status && ds_aligned(logits, ds_dtype_size(dtype)));
-  DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f);
+  DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f && min_p >= 0.0f && min_p <= 1.0f);
   DS_REQUIRE(mult == mult && softcap == softcap && softcap >= 0.0f);
   if (temperature > 0.0f || temperature_r) DS_REQUIRE(seed && step);
   if (d2t) DS_REQUIRE(V_t >= 1);
   rs::SampleArgs a = {};
   a.T_r = temperature_r;
   a.top_p_r = top_p_r;
+  a.min_p = min_p;
+  a.min_p_r = min_p_r;
   a.rows = logits;
   a.V = V_d;
   a.ld = ld;

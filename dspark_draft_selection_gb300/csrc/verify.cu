@@ -66,9 +66,10 @@ struct VerifyArgs {
   dspark_qrecord q;
   int q_form;
   int64_t V_q;
-  float T, top_p;
+  float T, top_p, min_p;
   const float* T_r;          // [R] per-request temperature (<= 0: greedy), or null
   const float* top_p_r;      // [R] per-request top-p, or null
+  const float* min_p_r;      // [R] per-request min-p, or null
   const uint64_t* vseed;
   const uint64_t* step;
   int32_t* out_tokens;
@@ -84,6 +85,12 @@ struct VerifyArgs {
 DS_DEV float vf_T(const VerifyArgs& a, int64_t r) {
   const float T = a.T_r ? a.T_r[r] : a.T;
   return T == T ? T : 0.0f;
+}
+
+// Request r's min-p (0 when out of [0, 1]; the host or the statistics pass reports it)
+DS_DEV float vf_mp(const VerifyArgs& a, int64_t r) {
+  const float m = a.min_p_r ? a.min_p_r[r] : a.min_p;
+  return (m >= 0.0f && m <= 1.0f) ? m : 0.0f;
 }
 
 DS_DEV bool vf_keep(float w, int64_t i, float wcut, int64_t icut) {
@@ -274,6 +281,7 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
     const float Tq = vf_T(a, r);
     const bool greedy = !(Tq > 0.0f);
     const float Tz = greedy ? 1.0f : Tq;
+    const float mp = greedy ? 0.0f : vf_mp(a, r);   // min-p: the kept weights are those >= mp
     const int32_t n = a.n_draft[r];
     if (n < 0 || n > a.B) {                        // out of contract: the first row's CTA reports it
       if (j == 0 && warp == 0) {
@@ -317,7 +325,8 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
     uint32_t amin = 0xFFFFFFFFu;
     auto scalar = [&](int64_t i) {
       const float z = ds_temper(ds_load_elem<T>(row + i), Tz);
-      rs::ff_add(sc, ds_weight(__fsub_rn(z, zmax)));
+      const float wi = ds_weight(__fsub_rn(z, zmax));
+      rs::ff_add(sc, wi >= mp ? wi : 0.0f);
       if (greedy && z == zmax) amin = min(amin, uint32_t(i));
     };
     if (finite && tid < head) scalar(tid);
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
           for (int e = 0; e < EPV; e += 2) {
             const float z0 = ds_temper(ds_vec_elem<T>(w[u], e), Tz), z1 = ds_temper(ds_vec_elem<T>(w[u], e + 1), Tz);
             const float2 w2 = ds_weight2(__fsub_rn(z0, zmax), __fsub_rn(z1, zmax));
-            rs::ff2_add(acc, ds_f2(w2.x, w2.y));
+            rs::ff2_add(acc, ds_f2(w2.x >= mp ? w2.x : 0.0f, w2.y >= mp ? w2.y : 0.0f));
             if (greedy) {
               const uint32_t i0 = uint32_t(head + v * EPV + e);
               if (z0 == zmax) amin = min(amin, i0);
@@ -365,13 +374,14 @@ __global__ void __launch_bounds__(VS_THREADS, VS_PER_SM) verify_stats_kernel(con
       if (!finite) ds_set_error(a.status, DSPARK_ENONFINITE);
       a.ws.zmax[rid] = zmax;
       a.ws.wsum[rid] = W;
-      a.ws.wcut[rid] = 0.0f;
-      a.ws.icut[rid] = -1;
+      a.ws.wcut[rid] = mp > 0.0f ? mp : 0.0f;          // min-p's cut (min_p, largest int32): w >= mp
+      a.ws.icut[rid] = mp > 0.0f ? 0x7FFFFFFF : -1;
       if (greedy) a.ws.amax[rid] = int32_t(am);
       float pw = 0.0f;
       if (finite && j < n) {
         const int64_t x = a.draft_tgt[r * a.B + j];
         if (x >= 0 && x < a.V) pw = ds_weight(__fsub_rn(ds_temper(ds_load_elem<T>(row + x), Tz), zmax));
+        if (pw < mp) pw = 0.0f;
       }
       a.ws.probe_w[rid] = pw;
       // the CTA that completes the request's last needed row runs its acceptance tests
@@ -716,15 +726,16 @@ extern "C" size_t dspark_internal_ws_verify(int64_t R, int32_t B, int64_t V) {
 extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_t,
                                        int64_t ld, const int64_t* row_start, const int32_t* draft_tgt,
                                        const int32_t* n_draft, const dspark_qrecord* q, int64_t V_q,
-                                       const int64_t* q_d2t, float temperature, float top_p,
-                                       const float* temperature_r, const float* top_p_r, const uint64_t* vseed,
+                                       const int64_t* q_d2t, float temperature, float top_p, float min_p,
+                                       const float* temperature_r, const float* top_p_r, const float* min_p_r,
+                                       const uint64_t* vseed,
                                        const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted, float* logprob,
                                        void* ws, size_t ws_bytes, int32_t* dev_status, dspark_stream_t stream) {
   DS_REQUIRE(ds_dtype_ok(dtype) && R >= 0 && B >= 1 && B <= 100 && V_t >= 1 && ld >= V_t);
   DS_REQUIRE(V_t <= 0x7FFFFFFF && R * (B + 1) <= 0x7FFFFFFF);
   DS_REQUIRE(tgt_logits && draft_tgt && n_draft && out_tokens && n_accepted && logprob && dev_status);
   DS_REQUIRE(ds_aligned(tgt_logits, ds_dtype_size(dtype)));
-  DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f);
+  DS_REQUIRE(temperature == temperature && top_p == top_p && top_p > 0.0f && min_p >= 0.0f && min_p <= 1.0f);
   const bool greedy = !(temperature > 0.0f) && !temperature_r;   // every request greedy
   int q_form = QF_NONE;
   if (!greedy) {
@@ -758,6 +769,8 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   a.top_p = top_p;
   a.T_r = temperature_r;
   a.top_p_r = top_p_r;
+  a.min_p = min_p;
+  a.min_p_r = min_p_r;
   a.vseed = vseed;
   a.step = step;
   a.out_tokens = out_tokens;
@@ -801,6 +814,8 @@ extern "C" dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtyp
   sa.top_p = greedy ? 1.0f : top_p;
   sa.T_r = temperature_r;
   sa.top_p_r = top_p_r;
+  sa.min_p = greedy ? 0.0f : min_p;
+  sa.min_p_r = min_p_r;
   sa.position = -1;
   sa.out_mul = 1;
   sa.status = dev_status;

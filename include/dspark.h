@@ -199,11 +199,14 @@ dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int32_t* prev,
  *   DSPARK_SAMPLE: the same row, sampled at `temperature`/`top_p` over the K candidates
  *     (candidate rank is the index), uniform U(seed[r], step[r], j, purpose 0); the sparse
  *     q of every position goes to q->ids/p/n with q->cap >= K. temperature <= 0 is greedy.
+ *     min_p in [0, 1] (0: off) [G: commit on the thresholded filters - MinPFilter]: after top-p,
+ *     only candidates whose probability is at least min_p times the top candidate's are kept.
  * Mixed batches [G: Change > Sampled drafting - greedy and sampled requests share one
  * continuous-batching step]: temperature_r / top_p_r, when not NULL, are [R] float32 device
  * arrays of per-request values that replace the scalars in DSPARK_SAMPLE (a request with
- * temperature <= 0 walks greedily and records q = 1 on its token); a NaN temperature or a
- * top_p <= 0 there sets DSPARK_EINVAL on *dev_status and walks that request greedily.
+ * temperature <= 0 walks greedily and records q = 1 on its token), and so does min_p_r for min_p;
+ * a NaN temperature, a top_p <= 0 or a min_p outside [0, 1] there sets DSPARK_EINVAL on
+ * *dev_status and walks that request greedily.
  * Outputs: chain_rank [R, B] int32, chain_tgt [R, B] int32 (= cand_tgt at the rank),
  * score [R] float32 (sum of the chosen row entries; the max for MAXSUM).
  * seed, step: [R] uint64 (SAMPLE with a sampled request). No workspace.
@@ -211,7 +214,8 @@ dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int32_t* prev,
 dspark_status dspark_chain_select(const float* cand_val, const float* trans,
                                   const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
                                   dspark_chain_mode mode, float temperature, float top_p,
-                                  const float* temperature_r, const float* top_p_r,
+                                  float min_p, const float* temperature_r, const float* top_p_r,
+                                  const float* min_p_r,
                                   const uint64_t* seed, const uint64_t* step,
                                   int32_t* chain_rank, int32_t* chain_tgt, float* score,
                                   const dspark_qrecord* q, int32_t* dev_status,
@@ -244,15 +248,20 @@ dspark_status dspark_lattice_chain(const float* cand_val, const int32_t* cand_tg
  * indices (nullable). q: NULL, or a record (sparse with cap >= the nucleus size, else
  * DSPARK_EINVAL on *dev_status and n = -1; or dense with ldz >= V_d). ws: see
  * dspark_workspace_size(DSPARK_OP_SAMPLE, R, B, V_d, 0).
- * Mixed batches: temperature_r / top_p_r, when not NULL, are [R] float32 device arrays of
- * per-request values replacing the scalars (temperature <= 0: that request's rows take the
- * argmax); a NaN temperature or top_p <= 0 there sets DSPARK_EINVAL and takes the argmax.
+ * min_p in [0, 1] (0: off) [G: commit on the thresholded filters - MinPFilter]: after the
+ * nucleus, only indices whose probability is at least min_p times the top one's are kept (the
+ * weight test w >= min_p); where that cuts inside the nucleus, a dense record's cut is
+ * (wcut, icut) = (min_p, 0x7FFFFFFF).
+ * Mixed batches: temperature_r / top_p_r / min_p_r, when not NULL, are [R] float32 device arrays
+ * of per-request values replacing the scalars (temperature <= 0: that request's rows take the
+ * argmax); a NaN temperature, top_p <= 0 or min_p outside [0, 1] there sets DSPARK_EINVAL and
+ * takes the argmax.
  */
 dspark_status dspark_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
                             int64_t V_d, int64_t ld, const int64_t* row_start,
                             const int64_t* d2t, int64_t V_t, float mult, float softcap,
-                            float temperature, float top_p, const float* temperature_r,
-                            const float* top_p_r, const uint64_t* seed,
+                            float temperature, float top_p, float min_p, const float* temperature_r,
+                            const float* top_p_r, const float* min_p_r, const uint64_t* seed,
                             const uint64_t* step, int32_t* out_tgt, int32_t* out_idx,
                             const dspark_qrecord* q, void* ws, size_t ws_bytes,
                             int32_t* dev_status, dspark_stream_t stream);
@@ -311,13 +320,15 @@ dspark_status dspark_dense_walk(const void* logits, dspark_dtype dtype, int64_t 
  * matching, temperature-1 log-probabilities), the others by the rejection test with their own
  * temperature and top_p; q, vseed and step are then required. A top_p <= 0 there sets
  * DSPARK_EINVAL and verifies that request without a nucleus. n_draft < B validates a prefix.
+ * min_p (and min_p_r per request) in [0, 1]: the target's post-filter p keeps, after top-p, only
+ * the ids whose probability is at least min_p times the top id's, as the draft's filters did.
  */
 dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t R, int32_t B,
                             int64_t V_t, int64_t ld, const int64_t* row_start,
                             const int32_t* draft_tgt, const int32_t* n_draft,
                             const dspark_qrecord* q, int64_t V_q, const int64_t* q_d2t,
-                            float temperature, float top_p, const float* temperature_r,
-                            const float* top_p_r, const uint64_t* vseed,
+                            float temperature, float top_p, float min_p, const float* temperature_r,
+                            const float* top_p_r, const float* min_p_r, const uint64_t* vseed,
                             const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted,
                             float* logprob, void* ws, size_t ws_bytes, int32_t* dev_status,
                             dspark_stream_t stream);

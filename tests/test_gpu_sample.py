@@ -41,14 +41,15 @@ def seeds(R, cid=60):
             g.integers(0, 2**40, size=R, dtype=np.int64).astype(np.uint64))
 
 
-def check_rows(s, B, T, top_p, seed, step, got_idx, d2t=None, rec=None, record=None, mult=1.0, softcap=0.0):
+def check_rows(s, B, T, top_p, seed, step, got_idx, d2t=None, rec=None, record=None, mult=1.0, softcap=0.0,
+               min_p=0.0):
     amb = 0
     R = s.shape[0] // B
     for r in range(R):
         for j in range(B):
             row = od.row_transform(s[r * B + j], mult, softcap)
             u = float(uniform(seed[r], step[r], j, 0)) if T > 0 else 0.0
-            tok, orec = sample_row(row, T, top_p, u)
+            tok, orec = sample_row(row, T, top_p, u, min_p)
             gi = int(got_idx[r, j])
             if gi != tok:
                 assert T > 0 and draw_margin(orec["w"], orec["kept"], u) < 1e-12, (r, j, gi, tok)

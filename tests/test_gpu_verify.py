@@ -28,14 +28,14 @@ def gpu_verify(target, B, drafted, n, q, T, top_p, vseed, step, V_q=None):
     return host(toks), host(nacc), host(lp), ds.read_status(st)
 
 
-def oracle_check(target, B, drafted, n, qfun, T, top_p, vseed, step, toks, nacc, lp):
+def oracle_check(target, B, drafted, n, qfun, T, top_p, vseed, step, toks, nacc, lp, min_p=0.0):
     t = as_f32(target)
     R = drafted.shape[0]
     amb = 0
     for r in range(R):
         rows = t[r * (B + 1):(r + 1) * (B + 1)]
         res = ov.verify_request(rows, drafted[r], int(n[r]), lambda j: qfun(r, j), T, top_p, int(vseed[r]),
-                                int(step[r]))
+                                int(step[r]), min_p=min_p)
         if res["n_accepted"] != nacc[r] or list(res["tokens"]) != list(toks[r, :len(res["tokens"])]):
             m = min(res["margins"]) if res["margins"] else 1.0
             assert m < 1e-12, (r, res["n_accepted"], nacc[r], res["tokens"], toks[r])
