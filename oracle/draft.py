@@ -145,21 +145,42 @@ def walk_rows(u, A, chain_prefix_rank, j):
     return (np.asarray(u[j], dtype=F32) + np.asarray(row, dtype=F32)).astype(F32)
 
 
-def chain_walk(u, A):
+def penalize(v, ids, history, repetition=1.0, presence=0.0):
+    """Repetition, then presence penalty on the row entries whose target id is in the history
+    ([G] commit on the penalty history: the penalties apply to every token in the history whatever
+    its count): s -> s / repetition if s > 0 else s * repetition, then s -> s - presence, in
+    float32. repetition = 1 and presence = 0 leave the row unchanged."""
+    v = np.asarray(v, dtype=F32).copy()
+    hit = np.isin(np.asarray(ids), np.asarray(sorted(history), dtype=np.int64))
+    if repetition != 1.0:
+        r = F32(repetition)
+        v[hit] = np.where(v[hit] > 0, (v[hit] / r).astype(F32), (v[hit] * r).astype(F32))
+    if presence != 0.0:
+        v[hit] = (v[hit] - F32(presence)).astype(F32)
+    return v
+
+
+def chain_walk(u, A, cand_tgt=None, history=None, repetition=1.0, presence=0.0):
     """Greedy walk [G]: b_0 = argmax(u_0 + A_0), b_j = argmax(u_j + A_j[b_{j-1}]) on float32
-    rows, lowest rank on ties. Score: double sum of the chosen row entries."""
+    rows, lowest rank on ties. Score: double sum of the chosen row entries. With a history (target
+    ids), every row is penalized first over the history and the tokens drafted before it."""
     B = np.asarray(u).shape[0]
     chain, score, prev = [], 0.0, None
+    seen = set(int(x) for x in history) if history is not None else None
     for j in range(B):
         v = walk_rows(u, A, prev, j)
+        if seen is not None:
+            v = penalize(v, cand_tgt[j], seen, repetition, presence)
         b = int(np.argmax(v))
         chain.append(b)
         score += float(v[b])
         prev = b
+        if seen is not None:
+            seen.add(int(cand_tgt[j][b]))
     return np.array(chain, dtype=np.int64), score
 
 
-def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0):
+def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0, history=None, repetition=1.0, presence=0.0):
     """Sampled walk [G]: at each position, sample the float32 lattice row after the token
     before over the K' candidates at temperature T, top-p and min-p, with the request's draft
     stream (purpose 0, position j). The candidate rank is the row index (ties in the
@@ -167,8 +188,11 @@ def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0):
     record holds the sparse q over kept ranks with their target ids."""
     B = np.asarray(u).shape[0]
     chain, score, recs, prev = [], 0.0, [], None
+    seen = set(int(x) for x in history) if history is not None else None
     for j in range(B):
         v = walk_rows(u, A, prev, j)
+        if seen is not None:
+            v = penalize(v, cand_tgt[j], seen, repetition, presence)
         uu = float(uniform(seed, step, j, PURPOSE_DRAFT))
         b, rec = sample_row(v, T, top_p, uu, min_p)
         rec["ids"] = np.asarray(cand_tgt[j])[rec["kept"]]
@@ -178,6 +202,8 @@ def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0):
         score += float(v[b])
         recs.append(rec)
         prev = b
+        if seen is not None:
+            seen.add(int(cand_tgt[j][b]))
     return np.array(chain, dtype=np.int64), score, recs
 
 

@@ -327,3 +327,67 @@ def test_chain_sample_min_p_one_is_the_greedy_walk():
     walk, _ = od.chain_walk(u, A)
     assert np.array_equal(chain, walk)
     assert all(len(r["kept"]) == 1 and r["q"][0] == 1.0 for r in recs)
+
+
+# ---- repetition / presence penalties over the history and the tokens drafted before -------------
+
+def _rows2(v0, v1):
+    """u rows for a 2-position walk with zero transitions (each row is its own lattice row)."""
+    u = np.array([v0, v1], dtype=np.float32)
+    A = np.zeros((2, len(v0), len(v0)), dtype=np.float32)
+    return u, A
+
+
+def test_penalties_neutral_values_leave_the_walk_unchanged():
+    rng = np.random.default_rng(3)
+    u = rng.standard_normal((6, 16)).astype(np.float32)
+    A = (rng.standard_normal((6, 16, 16)) * 0.5).astype(np.float32)
+    tgt = rng.integers(0, 40, size=(6, 16))
+    plain, _ = od.chain_walk(u, A)
+    pen, _ = od.chain_walk(u, A, tgt, history=set(range(40)), repetition=1.0, presence=0.0)
+    assert np.array_equal(plain, pen)
+
+
+def test_repetition_divides_positive_and_multiplies_negative_logits():
+    tgt = np.array([[10, 11, 12], [10, 11, 12]])
+    u, A = _rows2([2.0, 1.5, -1.0], [-1.0, -1.5, -3.0])
+    # position 0: 2.0 / 2 = 1.0 < 1.5 -> candidate 1 (id 11); position 1: id 10 is in the history
+    # (-1.0 * 2 = -2.0) and id 11 was drafted (-1.5 * 2 = -3.0), id 12 stays -3.0 -> candidate 0
+    chain, score = od.chain_walk(u, A, tgt, history={10}, repetition=2.0)
+    v1 = od.penalize(np.array([-1.0, -1.5, -3.0], np.float32), tgt[1], {10, 11}, 2.0, 0.0)
+    assert list(v1) == [-2.0, -3.0, -3.0]
+    assert list(chain) == [1, 0]
+
+
+def test_presence_subtracts_and_drafted_tokens_join_the_history():
+    tgt = np.array([[7, 8, 9], [9, 7, 5]])
+    u, A = _rows2([2.0, 1.5, 0.0], [3.0, 2.9, 1.0])
+    # position 0: id 7 (2.0) is not in the history: chosen; position 1: id 7 (2.9) was drafted and
+    # id 9 (3.0) is in the history: 3.0 - 0.4 = 2.6, 2.9 - 0.4 = 2.5, 1.0 -> id 9
+    chain, _ = od.chain_walk(u, A, tgt, history={9}, presence=0.4)
+    assert list(chain) == [0, 0]
+    # a large presence penalty pushes both penalized ids below id 5
+    chain, _ = od.chain_walk(u, A, tgt, history={9}, presence=5.0)
+    assert list(chain) == [0, 2]
+    # position 0 is penalized too when its best id is in the history
+    chain, _ = od.chain_walk(u, A, tgt, history={7}, presence=0.6)
+    assert chain[0] == 1
+
+
+def test_penalized_sampled_row_follows_the_penalized_softmax():
+    from scipy import stats
+    tgt = np.array([[1, 2, 3, 4]])
+    u = np.array([[0.0, np.log(2.0), -1.0, 0.5]], dtype=np.float32)
+    A = np.zeros((1, 4, 4), dtype=np.float32)
+    hist = {2, 4}
+    v = od.penalize(u[0], tgt[0], hist, 1.5, 0.3)        # ln2/1.5 - 0.3, 0.5/1.5 - 0.3
+    p = np.exp(v.astype(np.float64) - v.max())
+    p /= p.sum()
+    n = 3000
+    counts = np.zeros(4)
+    for s in range(n):
+        chain, _, recs = od.chain_sample(u, A, tgt, 1.0, 1.0, 1000 + s, 5, history=hist, repetition=1.5,
+                                         presence=0.3)
+        counts[chain[0]] += 1
+    assert stats.chisquare(counts, p * n).pvalue > 1e-3
+    np.testing.assert_allclose(np.asarray(recs[0]["q"], np.float64), p, rtol=2e-6)
