@@ -38,7 +38,7 @@ SIGNATURES = [
     ("dspark_test_set_first_wait_polls", None, [ctypes.c_uint32]),
     ("dspark_grouped_conv", c_i32, [c_vp, c_i32, c_i64, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp]),
     ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_f32, c_vp, c_vp,
-                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_sample", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_i64, c_f32, c_f32, c_f32, c_f32,
                               c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     ("dspark_dense_walk", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i64,
@@ -53,6 +53,11 @@ class QRecord(ctypes.Structure):
     """dspark_qrecord: the proposal record (sparse or dense form)."""
     _fields_ = [("ids", c_vp), ("p", c_vp), ("n", c_vp), ("cap", c_i32), ("z", c_vp), ("ldz", c_i64),
                 ("zmax", c_vp), ("wsum", c_vp), ("wcut", c_vp), ("icut", c_vp)]
+
+
+class Penalties(ctypes.Structure):
+    """dspark_penalties: the history and the repetition / presence penalties of a walk."""
+    _fields_ = [("ids", c_vp), ("n", c_vp), ("cap", c_i32), ("repetition", c_f32), ("presence", c_f32)]
 
 
 class DsparkError(RuntimeError):
@@ -202,7 +207,7 @@ def _qrec_sparse(ids, p, n):
 
 def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature=0.0, top_p=1.0, seed=None,
                         step=None, record=True, q=None, out=None, status=None, stream=None, temperature_r=None,
-                        top_p_r=None, min_p=0.0, min_p_r=None):
+                        top_p_r=None, min_p=0.0, min_p_r=None, history=None, repetition=1.0, presence=0.0):
     """temperature_r / top_p_r: optional [R] float32 per-request values (a mixed greedy/sampled
     batch; temperature <= 0 walks greedily) that replace the scalars in the sampled mode."""
     R, B, K = cand_val.shape
@@ -223,8 +228,13 @@ def dspark_chain_select(cand_val, trans, cand_tgt, mode="maxsum", *, temperature
                                                                                    device=dev),
               torch.zeros((R, B), dtype=torch.int32, device=dev))
         q = _qrec_sparse(*qt)
+    pen = None
+    if history is not None:                                 # (ids [R, cap] int32, n [R] int32)
+        ids, nh = history
+        pen = Penalties(_p(ids), _p(nh), ids.shape[1], repetition, presence)
     _check(lib().dspark_chain_select(_p(cand_val), _p(trans), _p(cand_tgt), R, B, K, m, temperature, top_p, min_p,
-                                     _p(temperature_r), _p(top_p_r), _p(min_p_r), _p(seed),
+                                     _p(temperature_r), _p(top_p_r), _p(min_p_r),
+                                     ctypes.byref(pen) if pen is not None else None, _p(seed),
                                      _p(step), _p(out[0]), _p(out[1]), _p(out[2]),
                                      ctypes.byref(q) if q is not None else None, _p(status), _stream(stream)),
            "dspark_chain_select")

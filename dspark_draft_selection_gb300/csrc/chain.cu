@@ -23,6 +23,7 @@ constexpr int CH_THREADS = 256;
 constexpr int CH_MAXK = 64;
 constexpr int CH_MAXB = 128;
 constexpr int CH_MAXNS = 16;          // tiles requested together (batch path)
+constexpr int CH_MAXH = 1024;         // history ids staged in shared memory (the rest read from L2)
 
 struct ChainArgs {
   const float* u;
@@ -33,6 +34,10 @@ struct ChainArgs {
   const float* T_r;                   // [R] per-request temperature (<= 0: greedy), or null
   const float* top_p_r;               // [R] per-request top-p, or null
   const float* min_p_r;               // [R] per-request min-p, or null
+  const int32_t* hist_ids;            // [R, hist_cap] penalty history (target ids), or null
+  const int32_t* hist_n;              // [R]
+  int32_t hist_cap;
+  float rep, pres;                    // repetition (1: off) and presence (0: off) penalties
   const uint64_t* seed;
   const uint64_t* step;
   int32_t* chain_rank;
@@ -135,6 +140,27 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
   const uint64_t seed = sample ? a.seed[r] : 0, step = sample ? a.step[r] : 0;
   const int warp = t >> 5, lane = t & 31;
   int prevb = 0;
+  // penalties: which candidates' target ids are in the request's history (a bit per (position,
+  // rank)); tokens drafted at earlier positions are added as the walk goes
+  __shared__ uint32_t s_hitw[CH_MAXB * CH_MAXK / 32];
+  __shared__ int32_t s_hist[CH_MAXH];
+  __shared__ int32_t s_drafted[CH_MAXB];
+  const bool pen = a.hist_ids != nullptr;
+  if (pen) {
+    const int hn = max(0, min(a.hist_n[r], a.hist_cap));
+    const int32_t* hg = a.hist_ids + int64_t(r) * a.hist_cap;
+    for (int i = t; i < min(hn, CH_MAXH); i += CH_THREADS) s_hist[i] = hg[i];
+    for (int i = t; i < (B * K + 31) / 32; i += CH_THREADS) s_hitw[i] = 0u;
+    ch_wait_all();                               // the candidate ids (and the first tiles) are in
+    __syncthreads();
+    for (int i = t; i < B * K; i += CH_THREADS) {
+      const int32_t c = s_ct[i];
+      bool hit = false;
+      for (int k = 0; k < hn && !hit; ++k) hit = (k < CH_MAXH ? s_hist[k] : hg[k]) == c;
+      if (hit) atomicOr(&s_hitw[i >> 5], 1u << (i & 31));
+    }
+    __syncthreads();
+  }
   double score = 0.0;
 
   for (int j = 0; j < B; ++j) {
@@ -203,6 +229,17 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
       for (int h = 0; h < 2; ++h) {
         const int b = lane + 32 * h;
         v[h] = (b < K) ? __fadd_rn(uj[b], row[b]) : -INFINITY;
+        if (pen && b < K) {
+          // repetition, then presence, on candidates in the history or drafted before
+          const int i = j * K + b;
+          const int32_t c = s_ct[i];
+          bool hit = (s_hitw[i >> 5] >> (i & 31)) & 1u;
+          for (int k = 0; k < j && !hit; ++k) hit = s_drafted[k] == c;
+          if (hit) {
+            if (a.rep != 1.0f) v[h] = v[h] > 0.0f ? __fdiv_rn(v[h], a.rep) : __fmul_rn(v[h], a.rep);
+            if (a.pres != 0.0f) v[h] = __fsub_rn(v[h], a.pres);
+          }
+        }
       }
       int pick;
       const int64_t qrow = int64_t(r) * B + j;
@@ -327,7 +364,9 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
       if (lane == 0) {
         a.chain_rank[r * B + j] = pick;
         a.chain_tgt[r * B + j] = s_ct[j * K + pick];
+        s_drafted[j] = s_ct[j * K + pick];
       }
+      __syncwarp();
       prevb = pick;
     }
     __syncthreads();
@@ -378,7 +417,7 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
                                              const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
                                              dspark_chain_mode mode, float temperature, float top_p,
                                              float min_p, const float* temperature_r, const float* top_p_r,
-                                             const float* min_p_r,
+                                             const float* min_p_r, const dspark_penalties* penalties,
                                              const uint64_t* seed, const uint64_t* step,
                                              int32_t* chain_rank, int32_t* chain_tgt, float* score,
                                              const dspark_qrecord* q, int32_t* dev_status,
@@ -400,6 +439,16 @@ extern "C" dspark_status dspark_chain_select(const float* cand_val, const float*
   a.T_r = mode == DSPARK_SAMPLE ? temperature_r : nullptr;
   a.top_p_r = mode == DSPARK_SAMPLE ? top_p_r : nullptr;
   a.min_p_r = mode == DSPARK_SAMPLE ? min_p_r : nullptr;
+  if (penalties) {
+    // penalties change a walk's rows by the tokens drafted before: walks only, not max-sum
+    DS_REQUIRE(mode != DSPARK_MAXSUM && penalties->ids && penalties->n && penalties->cap >= 0);
+    DS_REQUIRE(penalties->repetition > 0.0f && penalties->repetition < INFINITY && penalties->presence == penalties->presence);
+    a.hist_ids = penalties->ids;
+    a.hist_n = penalties->n;
+    a.hist_cap = penalties->cap;
+    a.rep = penalties->repetition;
+    a.pres = penalties->presence;
+  }
   a.seed = seed;
   a.step = step;
   a.chain_rank = chain_rank;

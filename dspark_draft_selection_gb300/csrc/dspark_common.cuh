@@ -149,7 +149,8 @@ DS_DEV float ds_weight(float d) {
 
 // ---- packed float32 pairs (sm_100 family f32x2): each lane is one IEEE round-to-nearest
 // operation, so a packed evaluation gives the same bits as two scalar ones. There is no packed
-// multiply here: a packed product feeding a packed add can come out fused (unrounded) ----
+// multiply here: a packed product feeding a packed add can come out fused (unrounded), so a
+// rounded product is an FMA with a zero addend ----
 DS_DEV uint64_t ds_f2(float lo, float hi) {
   return (uint64_t(__float_as_uint(hi)) << 32) | uint64_t(__float_as_uint(lo));
 }
@@ -171,15 +172,17 @@ DS_DEV uint64_t ds_sub2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// ds_weight of two exponents at once, with the same bits. The reduction t = fl(d / ln 2),
-// n = rint(t), f = t - n runs as scalar operations: a packed multiply feeding a packed add or
-// subtract can come out fused (the product unrounded), which would change f. The polynomial is a
-// chain of explicit packed FMAs, and 2^n * P(f) adds n to the exponent field of P(f) (P(f) in
-// [0.70, 1.42] and n >= -93, so the result is a normal float).
+// ds_weight of two exponents at once, with the same bits: t = fl(d / ln 2) is an explicit FMA
+// with a zero addend (the product's rounding; a packed multiply feeding the packed add below could
+// come out fused, unrounded), rint(t) is taken by adding and removing 1.5 * 2^23 (round to nearest,
+// ties to even, for |t| < 2^22), and 2^n * P(f) adds n to the exponent field of P(f) (P(f) in
+// [0.70, 1.42] and n >= -93, so the result is a normal float); the integer n sits in the low
+// mantissa bits of t + 1.5 * 2^23, so (bits << 23) is n << 23.
 DS_DEV float2 ds_weight2(float d0, float d1) {
-  const float t0 = __fmul_rn(d0, 0x1.715476p+0f), t1 = __fmul_rn(d1, 0x1.715476p+0f);
-  const float n0 = rintf(t0), n1 = rintf(t1);
-  const uint64_t f = ds_f2(__fsub_rn(t0, n0), __fsub_rn(t1, n1));
+  const uint64_t M = ds_f2(12582912.0f, 12582912.0f);
+  const uint64_t t = ds_fma2(ds_f2(d0, d1), ds_f2(0x1.715476p+0f, 0x1.715476p+0f), ds_f2(0.0f, 0.0f));
+  const uint64_t tm = ds_add2(t, M);
+  const uint64_t f = ds_sub2(t, ds_sub2(tm, M));
   uint64_t p = ds_f2(0x1.ffcbfcp-17f, 0x1.ffcbfcp-17f);
   p = ds_fma2(p, f, ds_f2(0x1.430912p-13f, 0x1.430912p-13f));
   p = ds_fma2(p, f, ds_f2(0x1.5d87fep-10f, 0x1.5d87fep-10f));
@@ -188,8 +191,8 @@ DS_DEV float2 ds_weight2(float d0, float d1) {
   p = ds_fma2(p, f, ds_f2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
   p = ds_fma2(p, f, ds_f2(0x1.62e430p-1f, 0x1.62e430p-1f));
   p = ds_fma2(p, f, ds_f2(1.0f, 1.0f));
-  const uint32_t w0 = uint32_t(p) + (uint32_t(int(n0)) << 23);
-  const uint32_t w1 = uint32_t(p >> 32) + (uint32_t(int(n1)) << 23);
+  const uint32_t w0 = uint32_t(p) + (uint32_t(tm) << 23);
+  const uint32_t w1 = uint32_t(p >> 32) + (uint32_t(tm >> 32) << 23);
   return make_float2((d0 >= -64.0f) ? __uint_as_float(w0) : 0.0f, (d1 >= -64.0f) ? __uint_as_float(w1) : 0.0f);
 }
 

@@ -537,7 +537,7 @@ extern "C" dspark_status dspark_lattice_chain(const float* cand_val, const int32
                                                   hidden_dtype, H, ldh, row_start, trans, gate, dev_status, stream);
     if (st != DSPARK_OK) return st;
     return dspark_chain_select(cand_val, trans, cand_tgt, R, B, K, mode, 0.0f, 1.0f, 0.0f, nullptr, nullptr, nullptr,
-                               nullptr, nullptr, chain_rank,
+                               nullptr, nullptr, nullptr, chain_rank,
                                chain_tgt, score, nullptr, dev_status, stream);
   }
   if (R == 0) return DSPARK_OK;

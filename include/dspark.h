@@ -96,6 +96,22 @@ typedef enum {
  *          kept iff w_i > wcut[row], or w_i == wcut[row] and i <= icut[row] (w_i > 0
  *          always required). q(i) = kept ? w(z_i - zmax) / wsum : 0.
  */
+/*
+ * Repetition / presence penalties of a sampled or greedy walk [G: commit on the penalty history -
+ * the penalties apply to every token in the history whatever its count; rejected tokens leave it]:
+ * ids [R, cap] int32 target ids of each request's history (device), n [R] int32 their number
+ * (device); on a candidate whose target id is in the history or was drafted at an earlier position
+ * of the block, the walk row entry s becomes s / repetition (s > 0) or s * repetition (s <= 0),
+ * then s - presence, in float32. repetition = 1 and presence = 0 leave the rows unchanged.
+ */
+typedef struct {
+  const int32_t* ids;
+  const int32_t* n;
+  int32_t cap;
+  float repetition;
+  float presence;
+} dspark_penalties;
+
 typedef struct {
   int32_t* ids;
   float* p;
@@ -207,15 +223,17 @@ dspark_status dspark_lattice_score(const int32_t* cand_tgt, const int32_t* prev,
  * temperature <= 0 walks greedily and records q = 1 on its token), and so does min_p_r for min_p;
  * a NaN temperature, a top_p <= 0 or a min_p outside [0, 1] there sets DSPARK_EINVAL on
  * *dev_status and walks that request greedily.
+ * penalties: NULL, or the repetition/presence penalties of DSPARK_WALK and DSPARK_SAMPLE
+ * (DSPARK_EINVAL with DSPARK_MAXSUM: the penalty of a row depends on the path before it).
  * Outputs: chain_rank [R, B] int32, chain_tgt [R, B] int32 (= cand_tgt at the rank),
- * score [R] float32 (sum of the chosen row entries; the max for MAXSUM).
+ * score [R] float32 (sum of the chosen, penalized row entries; the max for MAXSUM).
  * seed, step: [R] uint64 (SAMPLE with a sampled request). No workspace.
  */
 dspark_status dspark_chain_select(const float* cand_val, const float* trans,
                                   const int32_t* cand_tgt, int64_t R, int32_t B, int32_t K,
                                   dspark_chain_mode mode, float temperature, float top_p,
                                   float min_p, const float* temperature_r, const float* top_p_r,
-                                  const float* min_p_r,
+                                  const float* min_p_r, const dspark_penalties* penalties,
                                   const uint64_t* seed, const uint64_t* step,
                                   int32_t* chain_rank, int32_t* chain_tgt, float* score,
                                   const dspark_qrecord* q, int32_t* dev_status,

@@ -62,8 +62,8 @@ def test_status_strings_and_host_checks(libpath):
     # an empty batch is a no-op that launches nothing
     assert lib.dspark_topk(fake, 0, 0, 1, 10, 10, None, 8, 1.0, 0.0, None, 10, fake, fake, fake, fake, None) == 0
     assert ds.dspark_workspace_size(ds.OP_TOPK, 32, 7, 151936, 64) == 0
-    assert lib.dspark_chain_select(fake, fake, fake, 1, 7, 65, 0, 0.0, 1.0, 0.0, None, None, None, None, None, fake, fake,
-                                   fake, None,
+    assert lib.dspark_chain_select(fake, fake, fake, 1, 7, 65, 0, 0.0, 1.0, 0.0, None, None, None, None, None, None, fake,
+                                   fake, fake, None,
                                    fake, None) == 1
     assert lib.dspark_d2t_check(fake, 10, 10, 1, None, 0, fake, None) == 8      # injectivity needs a workspace
     # grouped convolution: channels not a multiple of the groups, too many taps, no-op on zero rows
