@@ -207,6 +207,30 @@ def chain_sample(u, A, cand_tgt, T, top_p, seed, step, min_p=0.0, history=None, 
     return np.array(chain, dtype=np.int64), score, recs
 
 
+def lattice_row_sample(rows, cand_draft, u, A, T, top_p, seed, step, min_p=0.0, mult=1.0, softcap=0.0):
+    """The block sampler's branch for any other request [G]: at position j, sample the lattice row
+    after the token before over the whole draft vocabulary - the transformed row s_j with every
+    candidate's entry replaced by its walk value fl32(u_j[b] + A_j[prev, b]) (position 0: A_0's
+    row 0) - as a full-row multinomial request (temperature, top-p, min-p, U(seed, step, j, 0));
+    a drawn token outside the candidates ends the block (no transition follows it).
+    Returns (draft indices drawn, records); the number drawn is the block's length."""
+    B = len(rows)
+    toks, recs, prev = [], [], None
+    for j in range(B):
+        full = row_transform(rows[j], mult, softcap).copy()
+        full[np.asarray(cand_draft[j])] = walk_rows(u, A, prev, j)
+        uu = float(uniform(seed, step, j, PURPOSE_DRAFT)) if T > 0 else 0.0
+        tok, rec = sample_row(full, T, top_p, uu, min_p)
+        rec["row"] = full
+        toks.append(int(tok))
+        recs.append(rec)
+        hit = np.nonzero(np.asarray(cand_draft[j]) == tok)[0]
+        if hit.size == 0:
+            break
+        prev = int(hit[0])
+    return np.array(toks, dtype=np.int64), recs
+
+
 def select_request(logits_rows, K, E, W, prev, mode, d2t=None, hidden_rows=None, g=None,
                    mult=1.0, softcap=0.0, T=0.0, top_p=1.0, seed=0, step=0):
     """The whole Top-K scorer path for one request: rows -> candidates -> lattice -> chain."""

@@ -391,3 +391,52 @@ def test_penalized_sampled_row_follows_the_penalized_softmax():
         counts[chain[0]] += 1
     assert stats.chisquare(counts, p * n).pvalue > 1e-3
     np.testing.assert_allclose(np.asarray(recs[0]["q"], np.float64), p, rtol=2e-6)
+
+
+# ---- the lattice-row branch: full-row samples of the walk row, ending outside the candidates ----
+
+def test_lattice_row_sample_with_zero_transitions_samples_each_row():
+    """A zero table leaves every candidate at its own logit, so each position is a plain full-row
+    sample of its row (and a drawn non-candidate ends the block)."""
+    from oracle.sampling import sample_row
+    from oracle.philox import uniform
+    rng = np.random.default_rng(8)
+    B, V, K = 6, 200, 16
+    rows = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    cand = np.array([od.topk_row(r, K)[0] for r in rows])
+    u = np.array([od.topk_row(r, K)[1] for r in rows], dtype=np.float32)
+    A = np.zeros((B, K, K), dtype=np.float32)
+    toks, recs = od.lattice_row_sample(rows, cand, u, A, 0.9, 1.0, 4242, 17)
+    for j, t in enumerate(toks):
+        want, _ = sample_row(rows[j], 0.9, 1.0, float(uniform(4242, 17, j, 0)))
+        assert t == want
+    ends = [j for j, t in enumerate(toks) if t not in cand[j]]
+    assert ends == ([len(toks) - 1] if len(toks) < B else [])
+
+
+def test_lattice_row_sample_with_every_token_a_candidate_is_the_sampled_walk():
+    """K = V with the candidates in index order: the row is the walk row itself, ranks are indices,
+    so the branch equals the sampled walk (tokens and q) and never ends early."""
+    rng = np.random.default_rng(9)
+    B, V = 5, 24
+    rows = (rng.standard_normal((B, V)) * 1.5).astype(np.float32)
+    cand = np.tile(np.arange(V), (B, 1))
+    u = rows.copy()
+    A = (rng.standard_normal((B, V, V)) * 0.7).astype(np.float32)
+    toks, recs = od.lattice_row_sample(rows, cand, u, A, 0.8, 0.9, 777, 3)
+    chain, _, crecs = od.chain_sample(u, A, cand, 0.8, 0.9, 777, 3)
+    assert len(toks) == B and np.array_equal(toks, chain)
+    for a, b in zip(recs, crecs):
+        assert np.array_equal(a["kept"], b["kept"]) and np.array_equal(a["q"], b["q"])
+
+
+def test_lattice_row_sample_ends_at_a_token_outside_the_candidates():
+    """Candidates pushed far below the rest: the first draw is a non-candidate and ends the block."""
+    rng = np.random.default_rng(10)
+    B, V, K = 4, 50, 8
+    rows = rng.standard_normal((B, V)).astype(np.float32)
+    cand = np.tile(np.arange(K), (B, 1))
+    u = rows[:, :K].copy()
+    A = np.full((B, K, K), -200.0, dtype=np.float32)        # every walk value far below the rest
+    toks, recs = od.lattice_row_sample(rows, cand, u, A, 1.0, 1.0, 5, 6)
+    assert len(toks) == 1 and toks[0] >= K
