@@ -18,7 +18,7 @@ c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 
 DSPARK_BF16, DSPARK_F32 = 0, 1
 DSPARK_MAXSUM, DSPARK_WALK, DSPARK_SAMPLE = 0, 1, 2
-OP_TOPK, OP_LATTICE, OP_CHAIN, OP_SAMPLE, OP_DENSE_WALK, OP_VERIFY, OP_D2T_CHECK = range(7)
+OP_TOPK, OP_LATTICE, OP_CHAIN, OP_SAMPLE, OP_DENSE_WALK, OP_VERIFY, OP_D2T_CHECK, OP_LATTICE_ROW = range(8)
 STATUS = {0: "DSPARK_OK", 1: "DSPARK_EINVAL", 2: "DSPARK_ERANGE", 3: "DSPARK_EDUP", 4: "DSPARK_EPROPOSAL",
           5: "DSPARK_ENONFINITE", 6: "DSPARK_ETIMEOUT", 7: "DSPARK_ECUDA", 8: "DSPARK_EWORKSPACE"}
 MODES = {"maxsum": DSPARK_MAXSUM, "walk": DSPARK_WALK, "sample": DSPARK_SAMPLE}
@@ -36,6 +36,9 @@ SIGNATURES = [
     ("dspark_lattice_chain", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp,
                                      c_i32, c_i32, c_i64, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     ("dspark_test_set_first_wait_polls", None, [ctypes.c_uint32]),
+    ("dspark_lattice_row_sample", c_i32, [c_vp, c_i32, c_i64, c_i32, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_i32,
+                                          c_vp, c_i64, c_f32, c_f32, c_f32, c_f32, c_f32, c_vp, c_vp, c_vp, c_vp,
+                                          c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     ("dspark_grouped_conv", c_i32, [c_vp, c_i32, c_i64, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp]),
     ("dspark_chain_select", c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_f32, c_f32, c_f32, c_vp, c_vp,
                                     c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
@@ -261,6 +264,31 @@ def dspark_lattice_chain(cand_val, cand_tgt, prev, E, W, mode="maxsum", *, hidde
                                       _p(hidden), _p(g), hdt, H, ldh, _p(row_start), m, _p(trans), _p(gate),
                                       _p(out[0]), _p(out[1]), _p(out[2]), _p(status), _stream(stream)),
            "dspark_lattice_chain")
+    return out + (status,)
+
+
+def dspark_lattice_row_sample(logits, B, cand_draft, cand_val, trans, *, R=None, V_d=None, row_start=None, d2t=None,
+                              V_t=None, mult=1.0, softcap=0.0, temperature=1.0, top_p=1.0, min_p=0.0, seed=None,
+                              step=None, q=None, out=None, ws=None, status=None, stream=None):
+    """The lattice-row branch: returns (out_tgt [R, B], out_idx [R, B], n_drafted [R], status)."""
+    rows, ld = _rows(logits)
+    V_d = logits.shape[1] if V_d is None else V_d
+    R = cand_draft.shape[0] if R is None else R
+    K = cand_draft.shape[2]
+    dev = logits.device
+    V_t = (V_d if d2t is None else V_t) if V_t is None else V_t
+    if out is None:
+        out = (torch.empty((R, B), dtype=torch.int32, device=dev), torch.empty((R, B), dtype=torch.int32, device=dev),
+               torch.empty((R,), dtype=torch.int32, device=dev))
+    status = new_status(dev) if status is None else status
+    ws = workspace(OP_LATTICE_ROW, R, B, V_d, K, dev) if ws is None else ws
+    wp, wn = _ws(ws)
+    qr = _qrec_any(q)
+    _check(lib().dspark_lattice_row_sample(_p(logits), _dt(logits), R, B, V_d, ld, _p(row_start), _p(cand_draft),
+                                           _p(cand_val), _p(trans), K, _p(d2t), V_t, mult, softcap, temperature, top_p,
+                                           min_p, _p(seed), _p(step), _p(out[0]), _p(out[1]), _p(out[2]),
+                                           ctypes.byref(qr) if qr is not None else None, wp, wn, _p(status),
+                                           _stream(stream)), "dspark_lattice_row_sample")
     return out + (status,)
 
 

@@ -47,6 +47,7 @@ cudaError_t ds_ensure_smem(const void* func, size_t bytes) {
 extern "C" size_t dspark_internal_ws_sample(int64_t R, int32_t B, int64_t V);
 extern "C" size_t dspark_internal_ws_dense_walk(int64_t R, int32_t B, int64_t V);
 extern "C" size_t dspark_internal_ws_verify(int64_t R, int32_t B, int64_t V);
+extern "C" size_t dspark_internal_ws_lattice_row(int64_t R, int32_t B, int64_t V);
 
 extern "C" size_t dspark_workspace_size(dspark_op op, int64_t R, int32_t B, int64_t V, int32_t K) {
   (void)K;
@@ -62,6 +63,8 @@ extern "C" size_t dspark_workspace_size(dspark_op op, int64_t R, int32_t B, int6
       return dspark_internal_ws_dense_walk(R, B, V);
     case DSPARK_OP_VERIFY:
       return dspark_internal_ws_verify(R, B, V);
+    case DSPARK_OP_LATTICE_ROW:
+      return dspark_internal_ws_lattice_row(R, B, V);
     default:
       return 0;
   }

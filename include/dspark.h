@@ -81,7 +81,8 @@ typedef enum {
   DSPARK_OP_SAMPLE = 3,
   DSPARK_OP_DENSE_WALK = 4,
   DSPARK_OP_VERIFY = 5,
-  DSPARK_OP_D2T_CHECK = 6
+  DSPARK_OP_D2T_CHECK = 6,
+  DSPARK_OP_LATTICE_ROW = 7
 } dspark_op;
 
 /*
@@ -350,6 +351,31 @@ dspark_status dspark_verify(const void* tgt_logits, dspark_dtype dtype, int64_t 
                             const uint64_t* step, int32_t* out_tokens, int32_t* n_accepted,
                             float* logprob, void* ws, size_t ws_bytes, int32_t* dev_status,
                             dspark_stream_t stream);
+
+/*
+ * The block sampler's lattice-row branch [G: block-sampler commit - any request that neither
+ * walks the lattice greedily nor samples the walk samples the lattice row after the token before,
+ * ending the block at a token outside the candidates]. Per request and position j: the whole
+ * transformed row s_j (rows and transform as in dspark_topk) with every candidate's entry replaced
+ * by its walk value fl32(cand_val[r, j, b] + trans[r, j, prev, b]) (position 0: prev = 0, the row
+ * dspark_lattice_score writes from the previous token), sampled as in dspark_sample (temperature,
+ * top_p, min_p, U(seed[r], step[r], j, purpose 0), d2t to target ids, q record); prev is the rank
+ * of the drawn index among position j's candidates, and a drawn index outside them ends the block.
+ * cand_draft [R, B, K] int32 draft indices and cand_val [R, B, K] float32 (from dspark_topk),
+ * trans [R, B, K, K] float32 (dspark_lattice_score), all device. Outputs: out_tgt [R, B] and
+ * out_idx [R, B] (nullable) int32, -1 after the block's end; n_drafted [R] int32 the block length
+ * (1..B); q as in dspark_sample (sparse rows after the end get n = 0). K <= 64.
+ * ws: dspark_workspace_size(DSPARK_OP_LATTICE_ROW, R, B, V_d, K).
+ */
+dspark_status dspark_lattice_row_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B,
+                                        int64_t V_d, int64_t ld, const int64_t* row_start,
+                                        const int32_t* cand_draft, const float* cand_val,
+                                        const float* trans, int32_t K, const int64_t* d2t, int64_t V_t,
+                                        float mult, float softcap, float temperature, float top_p,
+                                        float min_p, const uint64_t* seed, const uint64_t* step,
+                                        int32_t* out_tgt, int32_t* out_idx, int32_t* n_drafted,
+                                        const dspark_qrecord* q, void* ws, size_t ws_bytes,
+                                        int32_t* dev_status, dspark_stream_t stream);
 
 /*
  * DFlash-2 grouped dynamic convolution over packed block rows.
