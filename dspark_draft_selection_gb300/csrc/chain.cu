@@ -16,6 +16,7 @@
 // with the row after the previous choice.
 #include "dspark_common.cuh"
 #include "host_common.h"
+#include "rowsample.cuh"
 
 namespace {
 
@@ -68,15 +69,19 @@ DS_DEV void ch_issue_tile(float* dst, const float* src, int n) {
 DS_DEV void ch_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 DS_DEV void ch_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// warp inclusive scan of doubles
-DS_DEV double ch_warp_scan(double v) {
+// warp inclusive scan of float pairs (the running sums of the sampled walk: a double instruction
+// costs about 64 single-precision ones on this part)
+DS_DEV rs::FF ch_warp_scan(rs::FF v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xFFFFFFFFu, v, o);
-    if (lane >= o) v += n;
+    const rs::FF n{__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+    if (lane >= o) rs::ff_acc(v, n);
   }
   return v;
+}
+DS_DEV rs::FF ch_shfl(const rs::FF& v, int src) {
+  return rs::FF{__shfl_sync(0xFFFFFFFFu, v.hi, src), __shfl_sync(0xFFFFFFFFu, v.lo, src)};
 }
 
 template <bool RING>
@@ -267,7 +272,9 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           w[h] = (b < K) ? ds_weight(__fsub_rn(z[h], zmax)) : 0.0f;
         }
         __syncwarp();
-        const double wall = ds_warp_sum(double(w[0]) + double(w[1]));
+        rs::FF wsum2{w[0], 0.0f};
+        rs::ff_add(wsum2, w[1]);
+        const rs::FF wall = rs::warp_ff_reduce(wsum2);
         // kept[h]: nucleus membership of candidate lane + 32h
         bool kept[2] = {w[0] > 0.0f, w[1] > 0.0f};
         if (tpq < 1.0f) {
@@ -299,15 +306,15 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           }
           // sorted position i = lane + 32h: running weight sums over positions 0..63, compared
           // with top_p * W (no division per candidate on the narrow FP64 pipe)
-          double pw[2];
+          float pw[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? double(ds_key64_val(x[h])) : 0.0;
-          const double inc0 = ch_warp_scan(pw[0]);
-          const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
-          const double inc1 = tot0 + ch_warp_scan(pw[1]);
-          const double tp = double(tpq) * wall;
-          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && inc0 > tp && pw[0] > 0.0);
-          const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && inc1 > tp && pw[1] > 0.0);
+          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? ds_key64_val(x[h]) : 0.0f;
+          const rs::FF inc0 = ch_warp_scan(rs::FF{pw[0], 0.0f});
+          rs::FF inc1 = ch_warp_scan(rs::FF{pw[1], 0.0f});
+          rs::ff_acc(inc1, ch_shfl(inc0, 31));
+          const rs::FF tp = rs::ff_mul(rs::FF{tpq, 0.0f}, wall);
+          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && rs::ff_diff(inc0, tp) > 0.0f && pw[0] > 0.0f);
+          const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && rs::ff_diff(inc1, tp) > 0.0f && pw[1] > 0.0f);
           if (b0 | b1) {
             // first sorted position whose running mass exceeds top_p: keys at or above it are kept
             const int cl_ = b0 ? __ffs(b0) - 1 : __ffs(b1) - 1;
@@ -323,14 +330,20 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         }
         // draw: kept candidates in ascending rank order; running sums by warp scan
         // (lane holds ranks lane and lane + 32: scan the first half, then the second)
-        const double k0w = kept[0] ? double(w[0]) : 0.0, k1w = kept[1] ? double(w[1]) : 0.0;
-        const double inc0 = ch_warp_scan(k0w);
-        const double tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31);
-        const double inc1 = tot0 + ch_warp_scan(k1w);
-        const double wk = __shfl_sync(0xFFFFFFFFu, inc1, 31);
-        const double target = ds_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT) * wk;
-        const unsigned c0 = __ballot_sync(0xFFFFFFFFu, kept[0] && inc0 > target);
-        const unsigned c1 = __ballot_sync(0xFFFFFFFFu, kept[1] && inc1 > target);
+        const rs::FF inc0 = ch_warp_scan(rs::FF{kept[0] ? w[0] : 0.0f, 0.0f});
+        rs::FF inc1 = ch_warp_scan(rs::FF{kept[1] ? w[1] : 0.0f, 0.0f});
+        rs::ff_acc(inc1, ch_shfl(inc0, 31));
+        const rs::FF wkf = ch_shfl(inc1, 31);
+        const rs::FF target = rs::ff_mul(rs::ff_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT), wkf);
+        const unsigned c0 = __ballot_sync(0xFFFFFFFFu, kept[0] && rs::ff_diff(inc0, target) > 0.0f);
+        const unsigned c1 = __ballot_sync(0xFFFFFFFFu, kept[1] && rs::ff_diff(inc1, target) > 0.0f);
+        // q = w / W_kept rounded to float: q0 = w / W_hi, then the remainder w - q0 W (an FMA and the
+        // low term) corrects it to the nearest float of the float-pair quotient
+        auto qdiv = [&](float wv) {
+          const float q0 = __fdiv_rn(wv, wkf.hi);
+          const float rem = __fsub_rn(__fmaf_rn(-q0, wkf.hi, wv), __fmul_rn(q0, wkf.lo));
+          return __fadd_rn(q0, __fdiv_rn(rem, wkf.hi));
+        };
         if (c0) pick = __ffs(c0) - 1;
         else if (c1) pick = 32 + __ffs(c1) - 1;
         else {
@@ -346,14 +359,14 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
             const int o = __popc(m0 & below);
             if (o < a.q_cap) {
               a.q_ids[qrow * a.q_cap + o] = s_ct[j * K + lane];
-              a.q_p[qrow * a.q_cap + o] = float(double(w[0]) / wk);
+              a.q_p[qrow * a.q_cap + o] = qdiv(w[0]);
             }
           }
           if (kept[1]) {
             const int o = n0 + __popc(m1 & below);
             if (o < a.q_cap) {
               a.q_ids[qrow * a.q_cap + o] = s_ct[j * K + lane + 32];
-              a.q_p[qrow * a.q_cap + o] = float(double(w[1]) / wk);
+              a.q_p[qrow * a.q_cap + o] = qdiv(w[1]);
             }
           }
           if (lane == 0) a.q_n[qrow] = n0 + __popc(m1);
