@@ -22,7 +22,8 @@
 //     u_j < p_j(x_j) / q_j(x_j) of different positions are independent, and the first failing
 //     position (a ballot) ends the window. They leave at most one draw: the residual at the first
 //     rejection, or the bonus draw at n (greedy requests need none).
-//  2. verify_draw_kernel - one CTA per part of VM_PART ids of a request's draw row forms
+//  2. verify_draw_kernel - one CTA per part of a request's draw row (as many parts as keep all
+//     requests' parts in one wave of resident CTAs; 8,192 ids with a sparse record) forms
 //     rho = max(0, p - q) (p alone for the bonus draw) scaled by W_p * W_q, so no element needs a
 //     division, as float pairs, and writes the mass of every cell of VM_CELL consecutive ids; the
 //     part that finishes last scans all cells in double, finds the cell whose running sum crosses
@@ -34,7 +35,7 @@ namespace {
 
 constexpr int VM_THREADS = 512;            // residual-mass CTAs
 constexpr int VM_CELL = 256;               // ids per cell: one warp, eight consecutive ids a lane
-constexpr int VM_PART = 32768;             // ids per draw CTA (128 cells) for dense records
+constexpr int VM_PART_MIN_CELLS = 16;      // the smallest dense part (4,096 ids)
 constexpr int VM_PART_SPARSE = 8192;       // ... for sparse records (staged in shared memory by id)
 
 enum : int32_t { JOB_NONE = 0, JOB_RESIDUAL = 1, JOB_BONUS = 2 };
@@ -77,6 +78,7 @@ struct VerifyArgs {
   float* logprob;
   int32_t* status;
   int64_t ncell;
+  int32_t part_cells;  // cells per draw CTA (dense and no record; sparse records use VM_PART_SPARSE)
   VerifyWs ws;
 };
 
@@ -570,8 +572,8 @@ DS_DEV void vf_stage_sparse(const VerifyArgs& a, int64_t qrow, int64_t lo, int l
 // whose running sum crosses u * sum(rho), and re-evaluates that cell's ids.
 template <typename T, int QF, bool TONE>
 __global__ void __launch_bounds__(VM_THREADS, 2) verify_draw_kernel(const VerifyArgs a) {
-  constexpr int PART = (QF == QF_SPARSE) ? VM_PART_SPARSE : VM_PART;
-  constexpr int CPP = PART / VM_CELL;                      // cells per part
+  const int CPP = (QF == QF_SPARSE) ? VM_PART_SPARSE / VM_CELL : a.part_cells;   // cells per part
+  const int64_t PART = int64_t(CPP) * VM_CELL;
   constexpr int WARPS = VM_THREADS / 32;
   __shared__ float s_q[QF == QF_SPARSE ? VM_PART_SPARSE : 1];
   __shared__ rs::PickShared<VM_THREADS> s_pk;
@@ -696,9 +698,19 @@ VerifyWs vf_layout(void* base, int64_t R, int32_t B, int64_t V, size_t* total) {
 
 template <typename T, int QF, bool TONE>
 cudaError_t vf_launch_draws(const VerifyArgs& a, int64_t R, cudaStream_t stream) {
-  constexpr int PART = (QF == QF_SPARSE) ? VM_PART_SPARSE : VM_PART;
-  const dim3 grid(unsigned((a.V + PART - 1) / PART), unsigned(R));
-  return ds_launch(verify_draw_kernel<T, QF, TONE>, grid, dim3(VM_THREADS), 0, stream, a);
+  VerifyArgs b = a;
+  if (QF == QF_SPARSE) {
+    b.part_cells = VM_PART_SPARSE / VM_CELL;
+  } else {
+    // as many parts per request as leave every request's parts in one wave of resident CTAs (two
+    // per SM): a second, nearly empty wave would double the kernel's time
+    const int64_t slots = int64_t(2) * ds_num_sms();
+    int64_t np = std::max<int64_t>(1, slots / std::max<int64_t>(R, 1));
+    np = std::min<int64_t>(np, std::max<int64_t>(1, a.ncell / VM_PART_MIN_CELLS));
+    b.part_cells = int32_t((a.ncell + np - 1) / np);
+  }
+  const dim3 grid(unsigned((b.ncell + b.part_cells - 1) / b.part_cells), unsigned(R));
+  return ds_launch(verify_draw_kernel<T, QF, TONE>, grid, dim3(VM_THREADS), 0, stream, b);
 }
 
 template <typename T, bool TONE>
