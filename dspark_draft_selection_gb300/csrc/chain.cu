@@ -13,7 +13,9 @@
 // batch as soon as one is consumed), so the lattice is read once and its latency is paid once per
 // batch rather than once per position; odd K' or unaligned lattices take double-buffered tiles.
 // Max-sum uses all threads (4 threads per column b, 16 predecessors each); the walks use warp 0
-// with the row after the previous choice.
+// with the row after the previous choice, except that every thread helps with the sampled walk's
+// top-p nucleus (4 threads per candidate sum the weights of the keys above its key), and the
+// draws' uniforms are made ahead of the walk.
 #include "dspark_common.cuh"
 #include "host_common.h"
 #include "rowsample.cuh"
@@ -167,6 +169,20 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
     __syncthreads();
   }
   double score = 0.0;
+  // the draws' uniforms, which the walk's path does not change, ahead of the walk (visible after
+  // the first position's barrier)
+  __shared__ float2 s_ud[CH_MAXB];
+  if (sample)
+    for (int j = t; j < B; j += CH_THREADS) {
+      const rs::FF uj = rs::ff_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT);
+      s_ud[j] = make_float2(uj.hi, uj.lo);
+    }
+  // the nucleus of a sampled position: the keys and weights of its candidates, the mass bound
+  // top_p * W and the membership that every thread helps to find
+  __shared__ uint64_t s_nk[CH_MAXK];
+  __shared__ float s_nw[CH_MAXK];
+  __shared__ float s_tp[2];
+  __shared__ uint8_t s_keep[CH_MAXK];
 
   for (int j = 0; j < B; ++j) {
     const float* Aj;
@@ -227,9 +243,14 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         __syncthreads();
         if (t < K) s_delta[t] = nd;
       }
-    } else if (warp == 0) {
+    } else {
+      // ---- warp 0: the row's values (penalties applied) and, when sampling, the weights and
+      // their total ----
+      const bool nuc = sample && tpq < 1.0f;
+      float v[2] = {-INFINITY, -INFINITY}, w[2] = {0.0f, 0.0f};
+      rs::FF wall{0.0f, 0.0f};
+      if (warp == 0) {
       const float* row = (j == 0) ? Aj : Aj + prevb * K;
-      float v[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int b = lane + 32 * h;
@@ -246,6 +267,61 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           }
         }
       }
+      if (sample) {
+        float zmax = -INFINITY, z[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          z[h] = (lane + 32 * h < K) ? ds_temper(v[h], Tq) : -INFINITY;
+          zmax = fmaxf(zmax, z[h]);
+        }
+        zmax = ds_warp_max(zmax);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int b = lane + 32 * h;
+          w[h] = (b < K) ? ds_weight(__fsub_rn(z[h], zmax)) : 0.0f;
+        }
+        __syncwarp();
+        rs::FF wsum2{w[0], 0.0f};
+        rs::ff_add(wsum2, w[1]);
+        wall = rs::warp_ff_reduce(wsum2);
+        if (nuc) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int b = lane + 32 * h;
+            s_nk[b] = (b < K) ? ds_key64(w[h], uint32_t(b)) : 0ull;
+            s_nw[b] = w[h];
+          }
+          if (lane == 0) {
+            const rs::FF tp = rs::ff_mul(rs::FF{tpq, 0.0f}, wall);
+            s_tp[0] = tp.hi;
+            s_tp[1] = tp.lo;
+          }
+        }
+      }
+      }
+      // ---- every thread: top-p nucleus membership. Candidate i is kept when the mass of the
+      // candidates before it in the (weight desc, rank asc) order - the keys above its key - is at
+      // most top_p * W; then the first candidate whose running mass exceeds top_p * W is the last
+      // kept one. Four threads share a candidate's sum (16 keys each, in float pairs) ----
+      if (nuc) {
+        __syncthreads();
+        const int i = t >> 2, qq = t & 3;
+        rs::FF e0{0.0f, 0.0f}, e1{0.0f, 0.0f};
+        const uint64_t ki = (i < CH_MAXK) ? s_nk[i] : 0ull;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const int k0 = qq * 16 + k;
+          if (s_nk[k0] > ki) rs::ff_add(e0, s_nw[k0]);
+          if (s_nk[k0 + 1] > ki) rs::ff_add(e1, s_nw[k0 + 1]);
+        }
+        rs::ff_acc(e0, e1);
+        rs::ff_acc(e0, rs::FF{__shfl_xor_sync(0xFFFFFFFFu, e0.hi, 1), __shfl_xor_sync(0xFFFFFFFFu, e0.lo, 1)});
+        rs::ff_acc(e0, rs::FF{__shfl_xor_sync(0xFFFFFFFFu, e0.hi, 2), __shfl_xor_sync(0xFFFFFFFFu, e0.lo, 2)});
+        if (qq == 0 && i < CH_MAXK)
+          s_keep[i] = (ki != 0ull && s_nw[i] > 0.0f && !(rs::ff_diff(e0, rs::FF{s_tp[0], s_tp[1]}) > 0.0f)) ? 1 : 0;
+        __syncthreads();
+      }
+      if (warp == 0) {
       int pick;
       const int64_t qrow = int64_t(r) * B + j;
       if (!sample) {
@@ -258,70 +334,11 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
           a.q_p[qrow * a.q_cap] = 1.0f;
         }
       } else {
-        float zmax = -INFINITY, z[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          z[h] = (lane + 32 * h < K) ? ds_temper(v[h], Tq) : -INFINITY;
-          zmax = fmaxf(zmax, z[h]);
-        }
-        zmax = ds_warp_max(zmax);
-        float w[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int b = lane + 32 * h;
-          w[h] = (b < K) ? ds_weight(__fsub_rn(z[h], zmax)) : 0.0f;
-        }
-        __syncwarp();
-        rs::FF wsum2{w[0], 0.0f};
-        rs::ff_add(wsum2, w[1]);
-        const rs::FF wall = rs::warp_ff_reduce(wsum2);
-        // kept[h]: nucleus membership of candidate lane + 32h
+        // kept[h]: membership of candidate lane + 32h (positive weight, the nucleus)
         bool kept[2] = {w[0] > 0.0f, w[1] > 0.0f};
-        if (tpq < 1.0f) {
-          // (weight desc, rank asc) order by a warp bitonic sort of the 64 keys (position i = lane
-          // + 32h holds one key), then the running mass in that order and the cut
-          const uint64_t key0 = (lane < K) ? ds_key64(w[0], uint32_t(lane)) : 0ull;
-          const uint64_t key1 = (lane + 32 < K) ? ds_key64(w[1], uint32_t(lane + 32)) : 0ull;
-          uint64_t x[2] = {key0, key1};
-#pragma unroll
-          for (int kk = 2; kk <= 64; kk <<= 1) {
-#pragma unroll
-            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-              if (jj == 32) {
-                // partner is the other key of this lane; the whole 64 sorts descending
-                const uint64_t hi = x[0] > x[1] ? x[0] : x[1], lo = x[0] > x[1] ? x[1] : x[0];
-                x[0] = hi;
-                x[1] = lo;
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int i = lane + 32 * h;
-                  const uint64_t y = __shfl_xor_sync(0xFFFFFFFFu, x[h], jj);
-                  const bool up = (i & kk) == 0;          // this run of kk sorts descending
-                  const bool keep_max = ((lane & jj) == 0) == up;
-                  x[h] = keep_max ? (x[h] > y ? x[h] : y) : (x[h] < y ? x[h] : y);
-                }
-              }
-            }
-          }
-          // sorted position i = lane + 32h: running weight sums over positions 0..63, compared
-          // with top_p * W (no division per candidate on the narrow FP64 pipe)
-          float pw[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) pw[h] = (x[h] != 0ull) ? ds_key64_val(x[h]) : 0.0f;
-          const rs::FF inc0 = ch_warp_scan(rs::FF{pw[0], 0.0f});
-          rs::FF inc1 = ch_warp_scan(rs::FF{pw[1], 0.0f});
-          rs::ff_acc(inc1, ch_shfl(inc0, 31));
-          const rs::FF tp = rs::ff_mul(rs::FF{tpq, 0.0f}, wall);
-          const unsigned b0 = __ballot_sync(0xFFFFFFFFu, x[0] != 0ull && rs::ff_diff(inc0, tp) > 0.0f && pw[0] > 0.0f);
-          const unsigned b1 = __ballot_sync(0xFFFFFFFFu, x[1] != 0ull && rs::ff_diff(inc1, tp) > 0.0f && pw[1] > 0.0f);
-          if (b0 | b1) {
-            // first sorted position whose running mass exceeds top_p: keys at or above it are kept
-            const int cl_ = b0 ? __ffs(b0) - 1 : __ffs(b1) - 1;
-            const uint64_t cutk = __shfl_sync(0xFFFFFFFFu, b0 ? x[0] : x[1], cl_);
-            kept[0] = kept[0] && key0 >= cutk;
-            kept[1] = kept[1] && key1 >= cutk;
-          }
+        if (nuc) {
+          kept[0] = kept[0] && s_keep[lane] != 0;
+          kept[1] = kept[1] && s_keep[lane + 32] != 0;
         }
         // min-p after top-p: candidates whose weight is at least min_p times the top one's (1)
         if (mpq > 0.0f) {
@@ -334,7 +351,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
         rs::FF inc1 = ch_warp_scan(rs::FF{kept[1] ? w[1] : 0.0f, 0.0f});
         rs::ff_acc(inc1, ch_shfl(inc0, 31));
         const rs::FF wkf = ch_shfl(inc1, 31);
-        const rs::FF target = rs::ff_mul(rs::ff_uniform(seed, step, uint32_t(j), DS_PURPOSE_DRAFT), wkf);
+        const rs::FF target = rs::ff_mul(rs::FF{s_ud[j].x, s_ud[j].y}, wkf);
         const unsigned c0 = __ballot_sync(0xFFFFFFFFu, kept[0] && rs::ff_diff(inc0, target) > 0.0f);
         const unsigned c1 = __ballot_sync(0xFFFFFFFFu, kept[1] && rs::ff_diff(inc1, target) > 0.0f);
         // q = w / W_kept rounded to float: q0 = w / W_hi, then the remainder w - q0 W (an FMA and the
@@ -381,6 +398,7 @@ __global__ void __launch_bounds__(CH_THREADS) chain_kernel(const ChainArgs a) {
       }
       __syncwarp();
       prevb = pick;
+      }
     }
     __syncthreads();
     if (RING && j % NS == NS - 1 && j + 1 < B) {
