@@ -138,7 +138,7 @@ def _ws(t):
         return None, 0
     p = t.data_ptr()
     off = (-p) % 256
-    return p + off, t.numel() - off
+    return p + off, max(0, t.numel() - off)
 
 
 def dspark_status_string(code: int) -> str:

@@ -354,6 +354,11 @@ struct SampleArgs {
   float* probe_w;                // [rows] weight of the probed id if kept, else 0
   int32_t* amax_out;             // [rows] argmax index (lowest on ties)
   int32_t* status;
+  // top-p rows: a block's scratch row for the weights of its row's vectors (block b at
+  // wscr + b * wscr_ld), so the nucleus passes after the first read them instead of recomputing
+  // them; null: recomputed
+  float* wscr;
+  int64_t wscr_ld;
 };
 
 // Launches the row sampler (defined in sample.cu).

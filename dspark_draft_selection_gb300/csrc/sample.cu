@@ -161,6 +161,44 @@ DS_DEV void sr_pass(const SrRow<T>& g, F&& f, FC&& fc) {
   if (g.own_tail && tid < g.ntail) f(ds_load_elem<T>(g.row + g.tail0 + tid), g.tail0 + tid, g.nchunk);
 }
 
+// The same over the weights of the row: those of its vectors read from the block's scratch row wr
+// (vector v's weights at wr + v * EPV, stored by an earlier pass), those of the few head and tail
+// elements computed by wf from the row; calls f(weight, index).
+template <typename T, typename WF, typename F>
+DS_DEV void sr_wpass(const SrRow<T>& g, const float* wr, WF&& wf, F&& f) {
+  constexpr int EPV = 16 / sizeof(T);
+  constexpr int NF4 = EPV / 4;                 // 16-byte weight loads per vector
+  const int tid = threadIdx.x;
+  if (g.own_head && tid < g.head) f(wf(ds_load_elem<T>(g.row + tid)), int64_t(tid));
+  const float4* wv = reinterpret_cast<const float4*>(wr);
+  for (int c0 = g.c_lo; c0 < g.c_hi; c0 += SR_U) {
+    float4 buf[SR_U][NF4];
+#pragma unroll
+    for (int u = 0; u < SR_U; ++u) {
+      const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
+      if (c0 + u < g.c_hi && v < g.nvec) {
+#pragma unroll
+        for (int h = 0; h < NF4; ++h) buf[u][h] = __ldcg(wv + v * NF4 + h);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < SR_U; ++u) {
+      const int64_t v = int64_t(c0 + u) * SR_THREADS + tid;
+      if (c0 + u < g.c_hi && v < g.nvec) {
+        const int64_t i0 = g.head + v * EPV;
+#pragma unroll
+        for (int h = 0; h < NF4; ++h) {
+          f(buf[u][h].x, i0 + 4 * h);
+          f(buf[u][h].y, i0 + 4 * h + 1);
+          f(buf[u][h].z, i0 + 4 * h + 2);
+          f(buf[u][h].w, i0 + 4 * h + 3);
+        }
+      }
+    }
+  }
+  if (g.own_tail && tid < g.ntail) f(wf(ds_load_elem<T>(g.row + g.tail0 + tid)), g.tail0 + tid);
+}
+
 // NUC: rows may need a top-p nucleus; SPQ: a sparse record is written. The common case (neither)
 // is compiled separately with a register budget for two blocks per SM.
 template <typename T, bool XFORM, bool NUC, bool SPQ>
@@ -287,6 +325,8 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         continue;
       }
       auto wof = [&](float raw) { return ds_weight(__fsub_rn(zof(raw), zmax)); };
+      float* wr = nullptr;                               // the block's scratch row of weights
+      bool wready = false;                               // ... once written
 
       // ---- top-p nucleus: the cut (wcut, icut) of the (weight desc, index asc) order. A radix
       // select on the weight bits by mass: each pass sorts the weights that match the digits fixed
@@ -302,6 +342,7 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         double above = 0.0, target = 0.0;
         int shift = 30;                                // weights <= 1: bit 30 and up are zero
         bool first = true;
+        wr = a.wscr ? a.wscr + int64_t(blockIdx.x) * a.wscr_ld : nullptr;
         while (true) {
           const int width = min(4, shift);
           shift -= width;
@@ -311,21 +352,31 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
             s_accm[d * SR_THREADS + tid] = make_float2(0.0f, 0.0f);
             s_accc[d * SR_THREADS + tid] = 0u;
           }
-          sr_pass(g,
-                  [&](float raw, int64_t, int) {
-                    const float w = wof(raw);
-                    const uint32_t kb = __float_as_uint(w);
-                    if (w > 0.0f && (kb & pmask) == prefix) {
-                      const int o = int((kb >> shift) & dmask) * SR_THREADS + tid;
-                      const float2 m = s_accm[o];
-                      rs::FF f{m.x, m.y};
-                      rs::ff_add(f, w);
-                      s_accm[o] = make_float2(f.hi, f.lo);
-                      s_accc[o] += 1u;
-                    }
-                  },
-                  [](int) {});
+          auto radix = [&](float w) {
+            const uint32_t kb = __float_as_uint(w);
+            if (w > 0.0f && (kb & pmask) == prefix) {
+              const int o = int((kb >> shift) & dmask) * SR_THREADS + tid;
+              const float2 m = s_accm[o];
+              rs::FF f{m.x, m.y};
+              rs::ff_add(f, w);
+              s_accm[o] = make_float2(f.hi, f.lo);
+              s_accc[o] += 1u;
+            }
+          };
+          if (wready) {
+            sr_wpass(g, wr, wof, [&](float w, int64_t) { radix(w); });
+          } else {
+            // the first pass computes the weights (and keeps those of the vectors in the scratch row)
+            sr_pass(g,
+                    [&](float raw, int64_t i, int c) {
+                      const float w = wof(raw);
+                      if (wr && c >= 0 && c < g.nchunk) wr[i - g.head] = w;
+                      radix(w);
+                    },
+                    [](int) {});
+          }
           __syncthreads();
+          wready = wr != nullptr;
           {                                            // digit `warp`'s mass and count
             rs::FF f{0.0f, 0.0f};
             uint32_t c = 0;
@@ -383,15 +434,14 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
           // the weights of the selected digit, sorted, and the first whose running mass crosses
           if (tid == 0) s_cnt = 0;
           __syncthreads();
-          sr_pass(g,
-                  [&](float raw, int64_t i, int) {
-                    const float w = wof(raw);
-                    if (w > 0.0f && (__float_as_uint(w) & pmask) == prefix) {
-                      const uint32_t slot = atomicAdd(&s_cnt, 1u);
-                      if (slot < uint32_t(SP_CAP)) s_keys[slot] = ds_key64(w, uint32_t(i));
-                    }
-                  },
-                  [](int) {});
+          auto collect = [&](float w, int64_t i) {
+            if (w > 0.0f && (__float_as_uint(w) & pmask) == prefix) {
+              const uint32_t slot = atomicAdd(&s_cnt, 1u);
+              if (slot < uint32_t(SP_CAP)) s_keys[slot] = ds_key64(w, uint32_t(i));
+            }
+          };
+          if (wready) sr_wpass(g, wr, wof, collect);
+          else sr_pass(g, [&](float raw, int64_t i, int) { collect(wof(raw), i); }, [](int) {});
           __syncthreads();
           const int n = int(min(s_cnt, uint32_t(SP_CAP)));
           int n2 = 1;
@@ -462,7 +512,40 @@ __global__ void __launch_bounds__(SR_THREADS, (NUC || SPQ || XFORM) ? 1 : 2)
         if (keep(w, g.tail0 + tid)) rs::ff_add(mt, w);
         if (z == zmax) amin = min(amin, uint32_t(g.tail0 + tid));
       }
-      {
+      if (wready && !want_amax) {
+        // the weights of the vectors from the scratch row
+        constexpr int NF4 = EPV / 4;
+        const float4* wv = reinterpret_cast<const float4*>(wr);
+        for (int cb = g.c_lo; cb < g.c_hi; cb += SR_U) {
+          float4 wb[SR_U][NF4];
+#pragma unroll
+          for (int u = 0; u < SR_U; ++u) {
+            const int64_t v = int64_t(cb + u) * SR_THREADS + tid;
+            if (cb + u < g.c_hi && v < g.nvec) {
+#pragma unroll
+              for (int h = 0; h < NF4; ++h) wb[u][h] = __ldcg(wv + v * NF4 + h);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < SR_U; ++u) {
+            if (cb + u >= g.c_hi) break;
+            const int64_t v = int64_t(cb + u) * SR_THREADS + tid;
+            rs::FF m{0.0f, 0.0f};
+            if (v < g.nvec) {
+              const int64_t i0 = g.head + v * EPV;
+#pragma unroll
+              for (int h = 0; h < NF4; ++h) {
+                const float w4[4] = {wb[u][h].x, wb[u][h].y, wb[u][h].z, wb[u][h].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (keep(w4[e], i0 + 4 * h + e)) rs::ff_add(m, w4[e]);
+              }
+            }
+            const rs::FF cw = rs::warp_ff_reduce(m);
+            if (lane == 0) s_cellf[(cb + u - g.c_lo) * SR_WARPS + warp] = make_float2(cw.hi, cw.lo);
+          }
+        }
+      } else {
         const uint4* vp = reinterpret_cast<const uint4*>(g.row + g.head);
         for (int cb = g.c_lo; cb < g.c_hi; cb += SR_U) {
           uint4 buf[SR_U];
@@ -823,7 +906,14 @@ cudaError_t rs::sample_rows(const rs::SampleArgs& a, int64_t rows, int is_bf16, 
   return xform ? sp_launch<float, true>(a, rows, stream) : sp_launch<float, false>(a, rows, stream);
 }
 
-extern "C" size_t dspark_internal_ws_sample(int64_t, int32_t, int64_t) { return 0; }
+// The nucleus path's scratch rows: one per resident block (one block per SM), each the row length
+// rounded up to 64 floats.
+int64_t sp_wscr_ld(int64_t V) { return (V + 63) / 64 * 64; }
+
+extern "C" size_t dspark_internal_ws_sample(int64_t, int32_t, int64_t V) {
+  if (V <= 0) return 0;
+  return size_t(ds_num_sms()) * size_t(sp_wscr_ld(V)) * sizeof(float);
+}
 
 extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, int64_t R, int32_t B, int64_t V_d,
                                        int64_t ld, const int64_t* row_start, const int64_t* d2t, int64_t V_t,
@@ -833,8 +923,6 @@ extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, i
                                        const uint64_t* seed, const uint64_t* step, int32_t* out_tgt,
                                        int32_t* out_idx, const dspark_qrecord* q, void* ws, size_t ws_bytes,
                                        int32_t* dev_status, dspark_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   DS_REQUIRE(ds_dtype_ok(dtype));
   DS_REQUIRE(R >= 0 && B >= 1 && V_d >= 1 && ld >= V_d && V_d <= 0x7FFFFFFF && R * B <= 0x7FFFFFFF);
   DS_REQUIRE(logits && out_tgt && dev_status && ds_aligned(logits, ds_dtype_size(dtype)));
@@ -882,6 +970,12 @@ extern "C" dspark_status dspark_sample(const void* logits, dspark_dtype dtype, i
     }
   }
   if (R == 0) return DSPARK_OK;
+  // with the workspace, top-p rows keep their weights in it between the nucleus passes
+  const size_t wbytes = dspark_internal_ws_sample(R, B, V_d);
+  if (ws && ws_bytes >= wbytes && ds_aligned(ws, 16)) {
+    a.wscr = static_cast<float*>(ws);
+    a.wscr_ld = sp_wscr_ld(V_d);
+  }
   const int xform = (mult != 1.0f) || (softcap > 0.0f);
   const cudaError_t e = rs::sample_rows(a, R * B, dtype == DSPARK_BF16, xform, stream);
   if (e != cudaSuccess) {

@@ -265,8 +265,10 @@ dspark_status dspark_lattice_chain(const float* cand_val, const int32_t* cand_tg
  * with U(seed[r], step[r], j, purpose 0) walking kept indices in ascending order.
  * temperature <= 0: argmax. out_tgt [R, B] int32 target ids, out_idx [R, B] int32 draft
  * indices (nullable). q: NULL, or a record (sparse with cap >= the nucleus size, else
- * DSPARK_EINVAL on *dev_status and n = -1; or dense with ldz >= V_d). ws: see
- * dspark_workspace_size(DSPARK_OP_SAMPLE, R, B, V_d, 0).
+ * DSPARK_EINVAL on *dev_status and n = -1; or dense with ldz >= V_d). ws: optional device
+ * scratch; with at least dspark_workspace_size(DSPARK_OP_SAMPLE, R, B, V_d, 0) bytes (one row of
+ * V_d floats per SM, 16-byte aligned) the top-p rows keep their weights there between the nucleus
+ * passes instead of recomputing them; smaller or NULL: recomputed, same results.
  * min_p in [0, 1] (0: off) [G: commit on the thresholded filters - MinPFilter]: after the
  * nucleus, only indices whose probability is at least min_p times the top one's are kept (the
  * weight test w >= min_p); where that cuts inside the nucleus, a dense record's cut is

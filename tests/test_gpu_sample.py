@@ -154,3 +154,26 @@ def test_dense_walk_shaped_rows_full_size():
     tgt, idx, st, rec = gpu_sample(w["logits"], B, 1.0, 1.0, w["seed"], w["step"], record="dense")
     assert st == 0
     assert check_rows(as_f32(w["logits"]), B, 1.0, 1.0, w["seed"], w["step"], idx, rec=rec, record="dense") <= 1
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_weight_scratch_and_recomputed_weights_agree(f32):
+    """The nucleus passes read the weights from the workspace when it is large enough and recompute
+    them otherwise: both give the same draws and records (unaligned rows, head and tail elements)."""
+    import dspark_draft_selection_gb300 as ds
+    R, B, V = 3, 4, 30011
+    w = di.lattice_workload(64, R=R, B=B, V_d=V, K=1, rank=8)
+    seed, step = seeds(R)
+    x = dev(w["logits"])
+    if f32:
+        x = x.float()
+    outs = []
+    for ws in (None, torch.empty(1024, dtype=torch.uint8, device="cuda")):   # large enough / too small
+        q = ds.dense_record(R * B, V)
+        tgt, idx, st = ds.dspark_sample(x, B, temperature=0.8, top_p=0.9, seed=dev(seed), step=dev(step), q=q, ws=ws)
+        torch.cuda.synchronize()
+        assert ds.read_status(st) == 0
+        outs.append((host(tgt), host(idx)) + tuple(host(t) for t in q))
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    assert check_rows(host(x.float()), B, 0.8, 0.9, seed, step, outs[0][1], rec=outs[0][2:], record="dense") == 0
