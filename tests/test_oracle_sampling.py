@@ -203,3 +203,28 @@ def test_min_p_draws_follow_the_renormalised_kept_mass():
     assert counts[3] == 0 and counts[4] == 0
     exp = np.array([4, 2, 1]) / 7 * n
     assert stats.chisquare(counts[:3], exp).pvalue > 0.99
+
+
+def test_nucleus_membership_is_the_mass_above_at_most_top_p():
+    """The sampled walk decides membership without sorting: candidate i is kept when the mass of
+    the candidates above it in the (weight desc, index asc) order is at most top_p. Against the
+    oracle's sorted prefix, with that mass summed exactly (math.fsum): equal except where a running
+    sum lies within rounding of top_p."""
+    import math
+    rng = np.random.default_rng(17)
+    for trial in range(5000):
+        V = int(rng.integers(2, 65))
+        s = (rng.standard_normal(V) * float(rng.choice([0.3, 2.0, 8.0]))).astype(F32)
+        if trial % 2 == 0:
+            s = np.round(s)            # ties in weight: the index decides the order
+        top_p = float(rng.choice([0.2, 0.5, 0.9, 0.95]))
+        _, _, w = softmax_weights(s, 1.0)
+        kept, _, _ = nucleus_kept(w, top_p)
+        total = math.fsum(float(x) for x in w)
+        tp = float(F32(top_p))
+        above = [math.fsum(float(w[k]) for k in range(V) if (w[k], -k) > (w[i], -i)) / total for i in range(V)]
+        by_mass = [i for i in range(V) if w[i] > 0 and above[i] <= tp]
+        if by_mass != list(kept):
+            near = min(abs(a - tp) for a in above) < 1e-12 or \
+                min(abs(a + float(w[i]) / total - tp) for i, a in enumerate(above)) < 1e-12
+            assert near, (trial, by_mass, list(kept))
