@@ -71,3 +71,7 @@ def test_status_strings_and_host_checks(libpath):
     assert lib.dspark_grouped_conv(fake, 0, 4, 12, 12, 3, 17, fake, fake, fake, 12, None) == 1
     assert lib.dspark_grouped_conv(None, 0, 0, 12, 12, 3, 4, None, None, None, 12, None) == 0
     assert ds.dspark_workspace_size(ds.OP_D2T_CHECK, 1, 1, 64, 0) >= 8
+    # the sampler's optional weight scratch: whole 256-byte rows of V floats, none for an empty row
+    ws_s = ds.dspark_workspace_size(ds.OP_SAMPLE, 16, 15, 114688, 0)
+    assert ws_s > 0 and ws_s % 256 == 0 and ws_s % (114688 * 4) == 0
+    assert ds.dspark_workspace_size(ds.OP_SAMPLE, 16, 15, 0, 0) == 0
